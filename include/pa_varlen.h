@@ -1,0 +1,155 @@
+/*
+ * pa_varlen.h -- C ABI of the GB300 (sm_103a) paged-KV varlen flash-attention
+ * forward library (libpa_varlen.so).
+ *
+ * The operation is the forward pass of variable-length attention over a paged
+ * KV cache, as validated by candle-flash-attn's varlen wrapper
+ * (huggingface/candle@d5fee525bf, as explained by the pages
+ * "flash-attn-varlen expects input tensors of rank 3",
+ * "flash-attn-varlen paged expects k/v tensors of rank 4",
+ * "paged flash-attn requires page_block_size",
+ * "page_block_size ... does not match k shape" and
+ * "paged flash-attn requires page_block_size to be a multiple of 32").
+ *
+ * For every sequence b, query head h (kv head hk = h / (num_heads/num_heads_k))
+ * and query i < sq_b, with sq_b = cu_seqlens_q[b+1]-cu_seqlens_q[b],
+ * sk_b = cu_seqlens_k[b+1]-cu_seqlens_k[b] and c_b = sk_b - sq_b:
+ *   J      = { j in [0, sk_b) : (wl < 0 or j >= i+c_b-wl) and (wr < 0 or j <= i+c_b+wr) }
+ *   s_j    = softmax_scale * q[cu_q[b]+i, h, :] . K_j,
+ *            K_j = k_cache[block_table[b, j / P], j mod P, hk, :] (paged)
+ *   out    = sum_{j in J} softmax(s)_j V_j   (rounded to the input dtype)
+ *   lse    = ln sum_{j in J} exp(s_j)          (fp32; -inf and out = 0 when J is empty)
+ * Causal attention is (window_left, window_right) = (-1, 0), aligned to the
+ * bottom-right corner of each sequence's (sq_b x sk_b) score matrix.
+ *
+ * Everything runs asynchronously on the caller's CUDA stream; no call reads
+ * device memory on the host or synchronises, except pa_device_status().
+ */
+#ifndef PA_VARLEN_H
+#define PA_VARLEN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types of a tensor descriptor. */
+typedef enum pa_dtype { PA_F16 = 0, PA_BF16 = 1, PA_F32 = 2, PA_I32 = 3 } pa_dtype;
+
+/* A borrowed strided tensor: `data` is a device address (the caller owns it and
+ * keeps it alive until the stream has finished the call); `shape` and `stride`
+ * hold `ndim` (1..4) entries; strides are in elements, not bytes. */
+typedef struct pa_tensor {
+    void* data;
+    int32_t dtype;  /* pa_dtype */
+    int32_t ndim;
+    int64_t shape[4];
+    int64_t stride[4];
+} pa_tensor;
+
+/* Status codes.  The messages (pa_last_error) word the page conditions the
+ * way candle's wrapper words them. */
+enum {
+    PA_OK = 0,
+    PA_ERR_RANK = 1,            /* q not rank 3, or non-paged k/v not rank 3
+                                   ("flash-attn-varlen expects input tensors of rank 3", Source) */
+    PA_ERR_RANK_PAGED = 2,      /* paged and k/v not rank 4
+                                   ("flash-attn-varlen paged expects k/v tensors of rank 4", Source) */
+    PA_ERR_NONCONTIG = 3,       /* last dim of q/k/v (or an index tensor) not contiguous
+                                   (same Source; "Related errors" of the page-size pages) */
+    PA_ERR_SHAPE = 4,           /* k vs v shape, or k head size vs q head size
+                                   ("paged flash-attn requires page_block_size", Source) */
+    PA_ERR_PAGE_UNSET = 5,      /* paged and page_block_size <= 0
+                                   ("paged flash-attn requires page_block_size") */
+    PA_ERR_PAGE_MISMATCH = 6,   /* page_block_size != k_cache.shape[1]
+                                   ("page_block_size ... does not match k shape") */
+    PA_ERR_PAGE_MULT32 = 7,     /* page_block_size % 32 != 0
+                                   ("paged flash-attn requires page_block_size to be a multiple of 32") */
+    PA_ERR_HEADDIM = 8,         /* head_dim > 512 (same Source: "supports head sizes up to 512") */
+    PA_ERR_NOT_DEVICE = 9,      /* a tensor is not in device memory ("block_table must be a cuda
+                                   tensor", "seqlens_k must be a cuda tensor": Related errors) */
+    PA_ERR_ARG = 10,            /* a scalar disagrees with a descriptor, dtype mismatch, H % Hkv != 0,
+                                   bad out/lse/index shapes, block table too narrow for max_seqlen_k */
+    PA_ERR_UNSUPPORTED = 11,    /* an implementation limit, not a page condition: head_dim not a
+                                   multiple of 8, a stride or address not 16-byte aligned */
+    PA_ERR_CUDA = 12,           /* a CUDA runtime call or launch failed */
+    PA_ERR_DEVICE_TIMEOUT = 13, /* (pa_device_status) a kernel gave up a bounded wait */
+    PA_ERR_DEVICE_BOUNDS = 14,  /* (pa_device_status) a kernel saw a block id outside [0, num_blocks),
+                                   a page past the block table, non-monotone cu_seqlens, or a
+                                   sequence longer than max_seqlen_q / max_seqlen_k; the offending
+                                   work was skipped, its output is undefined */
+    PA_ERR_WORKSPACE = 15       /* split-KV workspace must grow while the stream is capturing */
+};
+
+/*
+ * pa_varlen_fwd -- forward paged (or non-paged) varlen attention.
+ *
+ *  q             (total_q, num_heads, head_dim), f16 or bf16, last dim contiguous.
+ *  k_cache,
+ *  v_cache       paged:     (num_blocks, page_block_size, num_heads_k, head_dim), same dtype
+ *                non-paged: (total_k, num_heads_k, head_dim) when block_table is NULL
+ *                last dim contiguous; other strides free (multiples of 8 elements).
+ *  cu_seqlens_q,
+ *  cu_seqlens_k  int32 (batch + 1), contiguous, cumulative offsets starting at 0.  In paged
+ *                mode only the differences sk_b are used: the keys of sequence b are the
+ *                logical positions 0..sk_b-1 of row b of the block table.
+ *  block_table   int32 (batch, max_pages), last dim contiguous; entry [b, p] is the
+ *                physical block of logical page p of sequence b.  Entries at or past
+ *                ceil(sk_b / page_block_size) are never read.  NULL selects non-paged mode.
+ *  max_seqlen_q,
+ *  max_seqlen_k  upper bounds of sq_b and sk_b (grid sizing; a kernel that sees a longer
+ *                sequence flags PA_ERR_DEVICE_BOUNDS and skips the excess).
+ *  num_heads, num_heads_k, head_dim
+ *                must equal the descriptors' sizes; num_heads % num_heads_k == 0.
+ *  page_block_size  paged mode: the cache's page size (0 = not set -> PA_ERR_PAGE_UNSET).
+ *  softmax_scale    multiplies q.k before the softmax.
+ *  window_left, window_right   window sides in keys; a negative side is unbounded.
+ *  out           (total_q, num_heads, head_dim), dtype of q, last dim contiguous.
+ *  softmax_lse   f32 (num_heads, total_q), last dim contiguous.
+ *  stream        a cudaStream_t (NULL = the legacy default stream).
+ *
+ * Checks run in the pages' order: ranks, last-dim contiguity, k/v shapes, page size set,
+ * page size == k shape, page size % 32, head size <= 512; then device residency, then the
+ * library's own argument checks.  Returns PA_OK or a status (message: pa_last_error()).
+ * Memory: the library keeps one grow-only split-KV workspace per device; it is allocated
+ * on first need with cudaMalloc and never while `stream` is capturing (PA_ERR_WORKSPACE).
+ * Thread safety: calls from several host threads are safe.
+ */
+int pa_varlen_fwd(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                  const pa_tensor* cu_seqlens_q, const pa_tensor* cu_seqlens_k,
+                  const pa_tensor* block_table, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                  int32_t num_heads, int32_t num_heads_k, int32_t head_dim,
+                  int32_t page_block_size, float softmax_scale, int32_t window_left,
+                  int32_t window_right, const pa_tensor* out, const pa_tensor* softmax_lse,
+                  void* stream);
+
+/*
+ * pa_varlen_check -- the host-side checks of pa_varlen_fwd alone: no device-residency
+ * check, no CUDA call, no launch.  Same arguments (no stream), same status codes.
+ * Lets a caller (or a test without a GPU) validate descriptors ahead of time.
+ */
+int pa_varlen_check(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                    const pa_tensor* cu_seqlens_q, const pa_tensor* cu_seqlens_k,
+                    const pa_tensor* block_table, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                    int32_t num_heads, int32_t num_heads_k, int32_t head_dim,
+                    int32_t page_block_size, float softmax_scale, int32_t window_left,
+                    int32_t window_right, const pa_tensor* out, const pa_tensor* softmax_lse);
+
+/* Message of the calling thread's last failed call ("" after a success).  The string
+ * stays valid until that thread's next call into the library. */
+const char* pa_last_error(void);
+
+/* Synchronises `stream`, then reads and clears the current device's error word set by
+ * the kernels (bounded-wait timeouts, out-of-range metadata).  Returns PA_OK,
+ * PA_ERR_DEVICE_TIMEOUT, PA_ERR_DEVICE_BOUNDS or PA_ERR_CUDA. */
+int pa_device_status(void* stream);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_VARLEN_H */
