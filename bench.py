@@ -1,0 +1,414 @@
+#!/usr/bin/env python
+"""Benchmark of the paged-KV varlen attention forward on one GB300 (or N replicas).
+
+A step is one pa_varlen_fwd call over one synthetic serving batch (default: the
+decode batch -- 64 sequences, q_len 1, sk ~ U[512, 4096], H=32, Hkv=8, D=128,
+page 32, bf16).  The headline value is the algorithmic KV GB/s of that step; the
+roofline object compares it with the measured HBM copy bandwidth.  A secondary
+measurement reports the causal-prefill workload in TFLOP/s against the measured
+dense bf16 peak.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica (the path needs no
+exchange); rank 0 prints one JSON line with the whole-job value.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "paged-attn TFLOP/s (prefill) and KV GB/s (decode), % of GB300 roofline"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ---- algorithmic work (closed form per query row) -----------------------------------------
+
+def algorithmic(lay, seqs=None):
+    """(FLOPs, bytes) of one pass: FLOPs = 4 * D * H * sum over rows of attended keys;
+    bytes = K+V of the union of attended keys per sequence and kv head, plus q, out
+    (input dtype) and lse (fp32)."""
+    elt = 2
+    H, Hkv, D = lay.num_heads, lay.num_heads_k, lay.head_dim
+    wl, wr = lay.window_left, lay.window_right
+    flops = 0
+    keys = 0
+    rows = 0
+    for b in (range(lay.batch) if seqs is None else seqs):
+        sq, sk = lay.seqlens_q[b], lay.seqlens_k[b]
+        if sq == 0:
+            continue
+        i = np.arange(sq, dtype=np.int64)
+        c = sk - sq
+        lo = np.maximum(0, i + c - wl) if wl >= 0 else np.zeros(sq, dtype=np.int64)
+        hi = np.minimum(sk - 1, i + c + wr) if wr >= 0 else np.full(sq, sk - 1, dtype=np.int64)
+        n = np.maximum(0, hi - lo + 1)
+        flops += 4 * D * H * int(n.sum())
+        live = n > 0
+        if live.any():
+            keys += int(hi[live].max() - lo[live].min() + 1)
+        rows += sq
+    kv = 2 * Hkv * D * elt * keys
+    qo = 2 * rows * H * D * elt
+    lse = 4 * H * rows
+    return flops, kv + qo + lse
+
+
+# ---- peaks, profiles, clocks ------------------------------------------------------------------
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            p = json.load(open(path))
+            return (float(p["hbm_gbs"]), float(p["bf16_tflops"]),
+                    float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured")
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def csrc_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "paged_kv_varlen_flashattention_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh", ".cpp", ".h")):
+            h.update(open(os.path.join(d, f), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "pa_varlen.h"), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary of this workload, or None if
+    the summary is missing or was taken on different kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_bytes = re.search(r"dram_bytes_per_call:\s*([0-9.eE+]+)", text)
+    m_hash = re.search(r"csrc_sha256_16:\s*([0-9a-f]+)", text)
+    if not m_bytes or not m_hash or m_hash.group(1) != csrc_hash():
+        return None
+    return float(m_bytes.group(1))
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---- the measured arm ----------------------------------------------------------------------------
+
+def _call(binding, g, lay, out, lse, stream=None):
+    binding.varlen_fwd(g.q, g.k_cache, g.v_cache, g.cu_seqlens_q, g.cu_seqlens_k, g.block_table,
+                       max_seqlen_q=lay.max_seqlen_q, max_seqlen_k=lay.max_seqlen_k,
+                       softmax_scale=lay.softmax_scale, window_left=lay.window_left,
+                       window_right=lay.window_right, out=out, softmax_lse=lse, stream=stream)
+
+
+def time_device(binding, g, lay, steps, warmup, dist):
+    import torch
+    out = torch.empty_like(g.q)
+    lse = torch.empty((lay.num_heads, lay.total_q), dtype=torch.float32, device=g.q.device)
+    for _ in range(warmup):
+        _call(binding, g, lay, out, lse)
+    torch.cuda.synchronize()
+    st = binding.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {binding.last_error()}")
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    n0 = binding.kernel_launches()
+    e0.record(stream)
+    for _ in range(steps):
+        _call(binding, g, lay, out, lse)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    launches = binding.kernel_launches() - n0
+    return e0.elapsed_time(e1) / steps, launches
+
+
+def time_e2e(binding, g, lay, steps, warmup):
+    """Same step through the public call with host-resident inputs: pinned host -> device
+    copies of every input, the call, and device -> host copies of out and lse, all timed."""
+    import torch
+    host = [t.cpu().pin_memory() if t is not None else None
+            for t in (g.q, g.k_cache, g.v_cache, g.cu_seqlens_q, g.cu_seqlens_k, g.block_table)]
+    dev = [torch.empty_like(t, device="cuda") if t is not None else None for t in host]
+    out_h = torch.empty(g.q.shape, dtype=g.q.dtype).pin_memory()
+    lse_h = torch.empty((lay.num_heads, lay.total_q), dtype=torch.float32).pin_memory()
+    out_d = torch.empty_like(g.q)
+    lse_d = torch.empty((lay.num_heads, lay.total_q), dtype=torch.float32, device="cuda")
+    h2d = sum(t.numel() * t.element_size() for t in host if t is not None)
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+
+    def step():
+        for d, h in zip(dev, host):
+            if d is not None:
+                d.copy_(h, non_blocking=True)
+        binding.varlen_fwd(dev[0], dev[1], dev[2], dev[3], dev[4], dev[5], max_seqlen_q=lay.max_seqlen_q,
+                           max_seqlen_k=lay.max_seqlen_k, softmax_scale=lay.softmax_scale,
+                           window_left=lay.window_left, window_right=lay.window_right, out=out_d,
+                           softmax_lse=lse_d)
+        out_h.copy_(out_d, non_blocking=True)
+        lse_h.copy_(lse_d, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps, h2d, d2h
+
+
+def cpu_baseline(lay, inp_cpu, budget_s=20.0):
+    """The oracle, as it stands, on the host cores over a bounded sample of the workload
+    (whole sequences, all heads); returns (GB/s, seconds, threads, sample text)."""
+    import oracle
+    order = list(range(lay.batch))
+    rng = np.random.default_rng(0)
+    rng.shuffle(order)
+    cq, _ = lay.cu_seqlens()
+    bt = inp_cpu.block_table.numpy() if inp_cpu.block_table is not None else None
+    done, t_total = [], 0.0
+    for b in order:
+        rows = np.arange(cq[b] * lay.num_heads, cq[b + 1] * lay.num_heads, dtype=np.int64)
+        if len(rows) == 0:
+            continue
+        t0 = time.perf_counter()
+        oracle.attention(lay.dtype, inp_cpu.q, inp_cpu.k_cache, inp_cpu.v_cache, inp_cpu.cu_seqlens_q.numpy(),
+                         inp_cpu.cu_seqlens_k.numpy(), bt, lay.softmax_scale, lay.window_left, lay.window_right,
+                         rows=rows)
+        t_total += time.perf_counter() - t0
+        done.append(b)
+        if t_total > budget_s:
+            break
+    _, nbytes = algorithmic(lay, done)
+    sample = f"{len(done)} of {lay.batch} sequences (all heads), {t_total:.1f} s"
+    return nbytes / t_total / 1e9, t_total, oracle.threads(), sample
+
+
+def run_ours(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl")
+        dist = tdist
+    else:
+        torch.cuda.set_device(0)
+    from paged_kv_varlen_flashattention_gb300 import binding, workloads
+
+    lay = workloads.CONFIGS[args.workload]()
+    lay.nan_fill = False
+    g = workloads.materialize(lay, device="cuda")
+    flops, nbytes = algorithmic(lay)
+    hbm, bf16, bf16_sus, peak_kind = peaks()
+
+    # a sustained run of the same step while the clock sampler warms up
+    sampler = ClockSampler(torch.cuda.current_device() if world == 1 else local)
+    sampler.start()
+    t_end = time.time() + 1.0
+    out = torch.empty_like(g.q)
+    lse = torch.empty((lay.num_heads, lay.total_q), dtype=torch.float32, device="cuda")
+    while time.time() < t_end:
+        for _ in range(20):
+            _call(binding, g, lay, out, lse)
+        torch.cuda.synchronize()
+    ms, launches = time_device(binding, g, lay, args.steps, args.warmup, dist)
+    clocks = sampler.stop()
+    ms_t = torch.tensor([ms], device="cuda")
+    if dist:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms = float(ms_t.item())
+    value = world * nbytes / (ms * 1e-3) / 1e9
+    achieved = nbytes / (ms * 1e-3) / 1e9
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if lay.dtype == "bf16" else "f16", "data": "synthetic",
+        "config": {"workload": lay.name, "batch": lay.batch, "num_heads": lay.num_heads,
+                   "num_heads_k": lay.num_heads_k, "head_dim": lay.head_dim,
+                   "page_block_size": lay.page_block_size, "max_seqlen_k": lay.max_seqlen_k,
+                   "total_keys": lay.total_k, "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+                   "l2": "inputs larger than L2 (no flush)" if nbytes > 2 * L2_BYTES else "L2 not flushed; inputs fit",
+                   "parallelism": f"replicas{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": profiled_traffic(lay.name),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s",
+                     "timed": "whole pa_varlen_fwd call (split-KV kernel + combine) per step"},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_e2e:
+        ms_e2e, h2d, d2h = time_e2e(binding, g, lay, max(3, min(args.steps, 10)), 2)
+        result["e2e"] = {"value": round(nbytes / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
+                         "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                         "ms_per_step": round(ms_e2e, 4)}
+    if rank == 0 and not args.no_secondary:
+        try:
+            lay2 = workloads.CONFIGS["prefill_bf16"]()
+            lay2.nan_fill = False
+            g2 = workloads.materialize(lay2, device="cuda")
+            f2, b2 = algorithmic(lay2)
+            ms2, l2 = time_device(binding, g2, lay2, 3, 2, None)
+            tf = f2 / (ms2 * 1e-3) / 1e12
+            result["secondary"] = {"workload": lay2.name, "value": round(tf, 2), "unit": "TFLOP/s",
+                                   "ms_per_step": round(ms2, 4), "algorithmic_flops": f2,
+                                   "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": bf16,
+                                                "unit": "TFLOP/s", "frac": round(tf / bf16, 4)},
+                                   "gpu_launches": int(l2)}
+            del g2
+        except Exception as e:  # reported, not hidden
+            result["secondary"] = {"error": str(e)[:300]}
+    if rank == 0 and not args.no_cpu_baseline:
+        inp_cpu = g.to("cpu")
+        gbs, secs, cores, sample = cpu_baseline(lay, inp_cpu, budget_s=args.cpu_budget)
+        result["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                  "sample": sample}
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def run_reference(args):
+    """The oracle on the host cores, timed per step over a bounded sample of the workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from paged_kv_varlen_flashattention_gb300 import workloads
+
+    lay = workloads.CONFIGS[args.workload]()
+    lay.nan_fill = False
+    inp = workloads.materialize(lay, device="cpu")
+    cq, _ = lay.cu_seqlens()
+    bt = inp.block_table.numpy() if inp.block_table is not None else None
+    rng = np.random.default_rng(1)
+    n_seq = max(1, min(lay.batch, args.ref_sequences))
+    seqs = sorted(rng.choice(lay.batch, size=n_seq, replace=False).tolist())
+    rows = np.concatenate([np.arange(cq[b] * lay.num_heads, cq[b + 1] * lay.num_heads) for b in seqs]).astype(np.int64)
+    _, nbytes = algorithmic(lay, seqs)
+
+    def step():
+        oracle.attention(lay.dtype, inp.q, inp.k_cache, inp.v_cache, inp.cu_seqlens_q.numpy(),
+                         inp.cu_seqlens_k.numpy(), bt, lay.softmax_scale, lay.window_left, lay.window_right,
+                         rows=rows)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    secs = (time.perf_counter() - t0) / args.steps
+    value = nbytes / secs / 1e9
+    sample = f"{n_seq} of {lay.batch} sequences (all heads) per step"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": lay.name, "sample": sample, "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode_bf16")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-sequences", type=int, default=16)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -148,6 +148,10 @@ int pa_device_status(void* stream);
 /* Library version, major * 10000 + minor * 100 + patch. */
 int pa_version(void);
 
+/* Number of kernels this library has launched in this process (all threads, all
+ * devices), for profiling: a caller reads it before and after a region. */
+uint64_t pa_kernel_launches(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -5,6 +5,6 @@ kernels); :mod:`.binding` marshals torch tensors into its descriptors.  Importin
 this package does not load the library; the first call does, and raises if the
 library is missing.
 """
-from .binding import varlen_fwd, last_error, device_status, library_path, PaError  # noqa: F401
+from .binding import varlen_fwd, last_error, device_status, library_path, kernel_launches, PaError  # noqa: F401
 
-__all__ = ["varlen_fwd", "last_error", "device_status", "library_path", "PaError"]
+__all__ = ["varlen_fwd", "last_error", "device_status", "library_path", "kernel_launches", "PaError"]

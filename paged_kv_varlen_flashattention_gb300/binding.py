@@ -1,6 +1,166 @@
-"""placeholder"""
-def varlen_fwd(*a, **k): raise RuntimeError("not built")
-def last_error(): return ""
-def device_status(*a): raise RuntimeError("not built")
-def library_path(): return None
-class PaError(RuntimeError): pass
+"""ctypes binding of libpa_varlen (argument marshalling only).
+
+Every step of the attention runs in the library's CUDA kernels; this module only
+turns torch tensors into ``pa_tensor`` descriptors, passes the current CUDA
+stream, and raises :class:`PaError` with the library's message on failure.
+There is no fallback: if the library is missing, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libpa_varlen.so")
+_lib = None
+
+PA_F16, PA_BF16, PA_F32, PA_I32 = 0, 1, 2, 3
+
+STATUS = {
+    0: "PA_OK", 1: "PA_ERR_RANK", 2: "PA_ERR_RANK_PAGED", 3: "PA_ERR_NONCONTIG", 4: "PA_ERR_SHAPE",
+    5: "PA_ERR_PAGE_UNSET", 6: "PA_ERR_PAGE_MISMATCH", 7: "PA_ERR_PAGE_MULT32", 8: "PA_ERR_HEADDIM",
+    9: "PA_ERR_NOT_DEVICE", 10: "PA_ERR_ARG", 11: "PA_ERR_UNSUPPORTED", 12: "PA_ERR_CUDA",
+    13: "PA_ERR_DEVICE_TIMEOUT", 14: "PA_ERR_DEVICE_BOUNDS", 15: "PA_ERR_WORKSPACE",
+}
+
+
+class PaError(RuntimeError):
+    """A non-zero status from the library; ``code`` is the status, ``name`` its enum name."""
+
+    def __init__(self, code: int, message: str):
+        self.code = code
+        self.name = STATUS.get(code, str(code))
+        super().__init__(f"{self.name}: {message}")
+
+
+class PaTensor(ctypes.Structure):
+    _fields_ = [
+        ("data", ctypes.c_void_p),
+        ("dtype", ctypes.c_int32),
+        ("ndim", ctypes.c_int32),
+        ("shape", ctypes.c_int64 * 4),
+        ("stride", ctypes.c_int64 * 4),
+    ]
+
+
+_TP = ctypes.POINTER(PaTensor)
+_FWD_ARGS = [_TP, _TP, _TP, _TP, _TP, _TP, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+             ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_int32, ctypes.c_int32, _TP, _TP]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Open libpa_varlen.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"libpa_varlen.so is not built ({_LIB_PATH}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(_LIB_PATH)
+        lib.pa_varlen_fwd.restype = ctypes.c_int
+        lib.pa_varlen_fwd.argtypes = _FWD_ARGS + [ctypes.c_void_p]
+        lib.pa_varlen_check.restype = ctypes.c_int
+        lib.pa_varlen_check.argtypes = list(_FWD_ARGS)
+        lib.pa_last_error.restype = ctypes.c_char_p
+        lib.pa_device_status.restype = ctypes.c_int
+        lib.pa_device_status.argtypes = [ctypes.c_void_p]
+        lib.pa_version.restype = ctypes.c_int
+        lib.pa_kernel_launches.restype = ctypes.c_uint64
+        _lib = lib
+    return _lib
+
+
+def _dtype_code(t) -> int:
+    import torch
+    return {torch.float16: PA_F16, torch.bfloat16: PA_BF16, torch.float32: PA_F32, torch.int32: PA_I32}.get(t.dtype, -1)
+
+
+def describe(t) -> Optional[PaTensor]:
+    """A pa_tensor descriptor borrowing a torch tensor's storage (None stays None)."""
+    if t is None:
+        return None
+    d = PaTensor()
+    d.data = t.data_ptr()
+    d.dtype = _dtype_code(t)
+    d.ndim = t.dim()
+    for i in range(min(t.dim(), 4)):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _ref(d):
+    return ctypes.byref(d) if d is not None else None
+
+
+def kernel_launches() -> int:
+    """Kernels the library has launched in this process so far."""
+    return int(load().pa_kernel_launches())
+
+
+def last_error() -> str:
+    return load().pa_last_error().decode()
+
+
+def device_status(stream=None) -> int:
+    """Synchronise ``stream`` and return (and clear) the kernels' device error status."""
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return load().pa_device_status(ctypes.c_void_p(s.cuda_stream))
+
+
+def check(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, max_seqlen_q, max_seqlen_k,
+          softmax_scale, window_left, window_right, out, softmax_lse, page_block_size=None,
+          num_heads=None, num_heads_k=None, head_dim=None, descriptors=None) -> int:
+    """Host-only validation (no CUDA call); returns the status code."""
+    lib = load()
+    ds = descriptors or [describe(t) for t in (q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table,
+                                                out, softmax_lse)]
+    H = num_heads if num_heads is not None else q.shape[1]
+    D = head_dim if head_dim is not None else q.shape[-1]
+    Hkv = num_heads_k if num_heads_k is not None else k_cache.shape[-2]
+    P = page_block_size if page_block_size is not None else (k_cache.shape[1] if block_table is not None else 0)
+    return lib.pa_varlen_check(_ref(ds[0]), _ref(ds[1]), _ref(ds[2]), _ref(ds[3]), _ref(ds[4]), _ref(ds[5]),
+                               int(max_seqlen_q), int(max_seqlen_k), int(H), int(Hkv), int(D), int(P),
+                               float(softmax_scale), int(window_left), int(window_right), _ref(ds[6]),
+                               _ref(ds[7]))
+
+
+def varlen_fwd(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table=None, max_seqlen_q=None,
+               max_seqlen_k=None, softmax_scale=None, window_left=-1, window_right=0, out=None,
+               softmax_lse=None, page_block_size=None, num_heads=None, num_heads_k=None, head_dim=None,
+               stream=None) -> Tuple[object, object]:
+    """pa_varlen_fwd on torch CUDA tensors; returns (out, softmax_lse).
+
+    ``out`` (total_q, H, D) and ``softmax_lse`` (H, total_q) fp32 are allocated with torch
+    when not given.  ``max_seqlen_q/k`` must be given (no device read is made to find them).
+    ``page_block_size`` defaults to ``k_cache.shape[1]`` in paged mode.
+    """
+    import torch
+    lib = load()
+    if max_seqlen_q is None or max_seqlen_k is None:
+        raise ValueError("max_seqlen_q and max_seqlen_k are required")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(q.shape[-1])
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    if softmax_lse is None:
+        softmax_lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=q.device)
+    H = num_heads if num_heads is not None else q.shape[1]
+    D = head_dim if head_dim is not None else q.shape[-1]
+    Hkv = num_heads_k if num_heads_k is not None else k_cache.shape[-2]
+    if page_block_size is None:
+        page_block_size = k_cache.shape[1] if block_table is not None and k_cache.dim() == 4 else 0
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    ds = [describe(t) for t in (q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, out, softmax_lse)]
+    rc = lib.pa_varlen_fwd(_ref(ds[0]), _ref(ds[1]), _ref(ds[2]), _ref(ds[3]), _ref(ds[4]), _ref(ds[5]),
+                           int(max_seqlen_q), int(max_seqlen_k), int(H), int(Hkv), int(D), int(page_block_size),
+                           float(softmax_scale), int(window_left), int(window_right), _ref(ds[6]), _ref(ds[7]),
+                           ctypes.c_void_p(s.cuda_stream))
+    if rc != 0:
+        raise PaError(rc, lib.pa_last_error().decode())
+    return out, softmax_lse

@@ -1,0 +1,469 @@
+// C-ABI front end of libpa_varlen: argument validation in the order candle's
+// varlen wrapper checks (ranks, last-dim contiguity, k/v shapes, page size set,
+// page size matches k, page size multiple of 32, head size <= 512 -- the Source
+// excerpts of "flash-attn-varlen expects input tensors of rank 3" and
+// "paged flash-attn requires page_block_size"), device residency of the index
+// tensors (their "Related errors"), then this library's own limits; workspace
+// management; and dispatch to the kernels.
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+
+#include "pa_internal.h"
+
+namespace {
+
+thread_local char g_msg[1024] = "";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+std::string dims(const pa_tensor* t) {
+    std::string s = "[";
+    for (int i = 0; i < t->ndim && i < 4; ++i) {
+        if (i) s += ", ";
+        s += std::to_string(t->shape[i]);
+    }
+    return s + "]";
+}
+
+std::string strides(const pa_tensor* t) {
+    std::string s = "[";
+    for (int i = 0; i < t->ndim && i < 4; ++i) {
+        if (i) s += ", ";
+        s += std::to_string(t->stride[i]);
+    }
+    return s + "]";
+}
+
+bool same_shape(const pa_tensor* a, const pa_tensor* b) {
+    if (a->ndim != b->ndim) return false;
+    for (int i = 0; i < a->ndim; ++i)
+        if (a->shape[i] != b->shape[i]) return false;
+    return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool is_device_memory(const void* p) {
+    cudaPointerAttributes attr{};
+    cudaError_t e = cudaPointerGetAttributes(&attr, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged;
+}
+
+int validate(const pa_tensor* q, const pa_tensor* k, const pa_tensor* v, const pa_tensor* cu_q,
+             const pa_tensor* cu_k, const pa_tensor* bt, int32_t max_sq, int32_t max_sk, int32_t num_heads,
+             int32_t num_heads_k, int32_t head_dim, int32_t page_block_size, float softmax_scale, int32_t wl,
+             int32_t wr, const pa_tensor* out, const pa_tensor* lse, bool check_device, pa::Args* a) {
+    if (!q || !k || !v || !cu_q || !cu_k || !out || !lse)
+        return fail(PA_ERR_ARG, "a tensor descriptor is NULL (only block_table may be NULL)");
+    const bool paged = bt != nullptr;
+    const int q_rank = q->ndim, k_rank = k->ndim, v_rank = v->ndim;
+
+    // -- ranks
+    if (q_rank != 3 || (!paged && k_rank != 3) || (!paged && v_rank != 3))
+        return fail(PA_ERR_RANK, "flash-attn-varlen expects input tensors of rank 3 (q: %d, k: %d, v: %d)", q_rank,
+                    k_rank, v_rank);
+    if (paged && (k_rank != 4 || v_rank != 4))
+        return fail(PA_ERR_RANK_PAGED, "flash-attn-varlen paged expects k/v tensors of rank 4 (k: %d, v: %d)",
+                    k_rank, v_rank);
+    // -- last-dim contiguity
+    if (q->stride[q_rank - 1] != 1)
+        return fail(PA_ERR_NONCONTIG, "the last dim of q must be contiguous %s", strides(q).c_str());
+    if (k->stride[k_rank - 1] != 1)
+        return fail(PA_ERR_NONCONTIG, "the last dim of k must be contiguous %s", strides(k).c_str());
+    if (v->stride[v_rank - 1] != 1)
+        return fail(PA_ERR_NONCONTIG, "the last dim of v must be contiguous %s", strides(v).c_str());
+
+    const int64_t total_q = q->shape[0], hq = q->shape[1], head_size = q->shape[2];
+    int64_t hkv = 0, num_blocks = 0, page = 0;
+    if (paged) {
+        // -- paged shape branch
+        page = k->shape[1];
+        hkv = k->shape[2];
+        num_blocks = k->shape[0];
+        if (!same_shape(k, v))
+            return fail(PA_ERR_SHAPE, "shape mismatch k %s and v %s", dims(k).c_str(), dims(v).c_str());
+        if (k->shape[3] != head_size)
+            return fail(PA_ERR_SHAPE, "shape mismatch q %s and k %s", dims(q).c_str(), dims(k).c_str());
+        if (page_block_size <= 0) return fail(PA_ERR_PAGE_UNSET, "paged flash-attn requires page_block_size");
+        if (page_block_size != page)
+            return fail(PA_ERR_PAGE_MISMATCH, "page_block_size %d does not match k shape %s", page_block_size,
+                        dims(k).c_str());
+        if (page % 32 != 0)
+            return fail(PA_ERR_PAGE_MULT32,
+                        "paged flash-attn requires page_block_size to be a multiple of 32 (got %lld)",
+                        (long long)page);
+        if (head_size > 512)
+            return fail(PA_ERR_HEADDIM, "paged flash-attn supports head sizes up to 512 (got %lld)",
+                        (long long)head_size);
+    } else {
+        // -- non-paged branch: k and v are (total_k, num_heads_k, head_size)
+        hkv = k->shape[1];
+        num_blocks = k->shape[0];
+        if (!(k->shape[0] == num_blocks && k->shape[1] == hkv && k->shape[2] == head_size))
+            return fail(PA_ERR_SHAPE, "shape mismatch q %s and k %s", dims(q).c_str(), dims(k).c_str());
+        if (!(v->shape[0] == num_blocks && v->shape[1] == hkv && v->shape[2] == head_size))
+            return fail(PA_ERR_SHAPE, "shape mismatch q %s and v %s", dims(q).c_str(), dims(v).c_str());
+    }
+
+    // -- index tensors
+    if (cu_q->ndim != 1) return fail(PA_ERR_ARG, "seqlens_q must be rank 1, got rank %d", cu_q->ndim);
+    if (cu_k->ndim != 1) return fail(PA_ERR_ARG, "seqlens_k must be rank 1, got rank %d", cu_k->ndim);
+    if (cu_q->stride[0] != 1) return fail(PA_ERR_NONCONTIG, "seqlens_q has to be contiguous");
+    if (cu_k->stride[0] != 1) return fail(PA_ERR_NONCONTIG, "seqlens_k has to be contiguous");
+    if (paged) {
+        if (bt->ndim != 2) return fail(PA_ERR_ARG, "block_table must be rank 2, got rank %d", bt->ndim);
+        if (bt->stride[1] != 1) return fail(PA_ERR_NONCONTIG, "block_table last dimension must be contiguous");
+    }
+    if (check_device) {
+        if (paged && !is_device_memory(bt->data)) return fail(PA_ERR_NOT_DEVICE, "block_table must be a cuda tensor");
+        if (!is_device_memory(cu_q->data)) return fail(PA_ERR_NOT_DEVICE, "seqlens_q must be a cuda tensor");
+        if (!is_device_memory(cu_k->data)) return fail(PA_ERR_NOT_DEVICE, "seqlens_k must be a cuda tensor");
+        if (!is_device_memory(q->data)) return fail(PA_ERR_NOT_DEVICE, "q must be a cuda tensor");
+        if (!is_device_memory(k->data)) return fail(PA_ERR_NOT_DEVICE, "k must be a cuda tensor");
+        if (!is_device_memory(v->data)) return fail(PA_ERR_NOT_DEVICE, "v must be a cuda tensor");
+        if (!is_device_memory(out->data)) return fail(PA_ERR_NOT_DEVICE, "out must be a cuda tensor");
+        if (!is_device_memory(lse->data)) return fail(PA_ERR_NOT_DEVICE, "softmax_lse must be a cuda tensor");
+    }
+
+    // -- this library's own argument checks
+    if (q->dtype != PA_F16 && q->dtype != PA_BF16)
+        return fail(PA_ERR_UNSUPPORTED, "q dtype %d: only f16 and bf16 are supported", q->dtype);
+    if (k->dtype != q->dtype || v->dtype != q->dtype || out->dtype != q->dtype)
+        return fail(PA_ERR_ARG, "q, k, v and out must share one dtype (q %d, k %d, v %d, out %d)", q->dtype,
+                    k->dtype, v->dtype, out->dtype);
+    if (lse->dtype != PA_F32) return fail(PA_ERR_ARG, "softmax_lse must be f32");
+    if (cu_q->dtype != PA_I32 || cu_k->dtype != PA_I32 || (paged && bt->dtype != PA_I32))
+        return fail(PA_ERR_ARG, "cu_seqlens and block_table must be int32");
+    if (num_heads != hq || head_dim != head_size || num_heads_k != hkv)
+        return fail(PA_ERR_ARG,
+                    "scalars disagree with the tensors: num_heads %d vs %lld, num_heads_k %d vs %lld, head_dim %d "
+                    "vs %lld",
+                    num_heads, (long long)hq, num_heads_k, (long long)hkv, head_dim, (long long)head_size);
+    if (hkv <= 0 || hq <= 0 || hq % hkv != 0)
+        return fail(PA_ERR_ARG, "num_heads (%lld) must be a positive multiple of num_heads_k (%lld)", (long long)hq,
+                    (long long)hkv);
+    if (head_size <= 0) return fail(PA_ERR_ARG, "head_dim must be positive");
+    if (out->ndim != 3 || out->shape[0] != total_q || out->shape[1] != hq || out->shape[2] != head_size)
+        return fail(PA_ERR_ARG, "out must have q's shape %s, got %s", dims(q).c_str(), dims(out).c_str());
+    if (out->stride[2] != 1)
+        return fail(PA_ERR_NONCONTIG, "the last dim of out must be contiguous %s", strides(out).c_str());
+    if (lse->ndim != 2 || lse->shape[0] != hq || lse->shape[1] != total_q || lse->stride[1] != 1)
+        return fail(PA_ERR_ARG, "softmax_lse must be (num_heads, total_q) = (%lld, %lld) with a contiguous last dim",
+                    (long long)hq, (long long)total_q);
+    if (cu_q->shape[0] < 1 || cu_q->shape[0] != cu_k->shape[0])
+        return fail(PA_ERR_ARG, "cu_seqlens_q and cu_seqlens_k must both have batch + 1 >= 1 entries (%lld, %lld)",
+                    (long long)cu_q->shape[0], (long long)cu_k->shape[0]);
+    const int64_t batch = cu_q->shape[0] - 1;
+    if (paged && bt->shape[0] != batch)
+        return fail(PA_ERR_ARG, "block_table has %lld rows for a batch of %lld", (long long)bt->shape[0],
+                    (long long)batch);
+    if (max_sq < 0 || max_sk < 0) return fail(PA_ERR_ARG, "max_seqlen_q and max_seqlen_k must be >= 0");
+    if (paged && (int64_t)max_sk > bt->shape[1] * page)
+        return fail(PA_ERR_ARG, "block_table holds %lld pages of %lld slots, too few for max_seqlen_k %d",
+                    (long long)bt->shape[1], (long long)page, max_sk);
+    if (!std::isfinite(softmax_scale)) return fail(PA_ERR_ARG, "softmax_scale must be finite");
+
+    // -- implementation limits (not page conditions)
+    if (head_size % 8 != 0)
+        return fail(PA_ERR_UNSUPPORTED, "head_dim %lld: kernels need a multiple of 8", (long long)head_size);
+    if (!paged && head_size > 512)
+        return fail(PA_ERR_UNSUPPORTED, "head_dim %lld: kernels support up to 512", (long long)head_size);
+    if (batch > 65535) return fail(PA_ERR_UNSUPPORTED, "batch %lld exceeds 65535", (long long)batch);
+    if (total_q >= (1ll << 31) || num_blocks >= (1ll << 31) || hq * total_q >= (1ll << 40))
+        return fail(PA_ERR_UNSUPPORTED, "sizes beyond 2^31 rows are not supported");
+    for (const pa_tensor* t : {q, k, v, out}) {
+        if (!aligned16(t->data))
+            return fail(PA_ERR_UNSUPPORTED, "q/k/v/out base addresses must be 16-byte aligned");
+        for (int d = 0; d < t->ndim - 1; ++d)
+            if (t->stride[d] % 8 != 0 || t->stride[d] <= 0)
+                return fail(PA_ERR_UNSUPPORTED, "strides %s: all but the last must be positive multiples of 8 elements",
+                            strides(t).c_str());
+    }
+
+    a->dtype = q->dtype;
+    a->q = q->data;
+    a->q_s0 = q->stride[0];
+    a->q_s1 = q->stride[1];
+    a->k = k->data;
+    a->v = v->data;
+    if (paged) {
+        if (k->stride[0] != v->stride[0] || k->stride[1] != v->stride[1] || k->stride[2] != v->stride[2])
+            return fail(PA_ERR_UNSUPPORTED, "k and v caches must share strides (k %s, v %s)", strides(k).c_str(),
+                        strides(v).c_str());
+        a->kv_s0 = k->stride[0];
+        a->kv_s1 = k->stride[1];
+        a->kv_s2 = k->stride[2];
+    } else {
+        if (k->stride[0] != v->stride[0] || k->stride[1] != v->stride[1])
+            return fail(PA_ERR_UNSUPPORTED, "k and v must share strides (k %s, v %s)", strides(k).c_str(),
+                        strides(v).c_str());
+        a->kv_s0 = k->stride[0];
+        a->kv_s1 = 0;
+        a->kv_s2 = k->stride[1];
+    }
+    a->paged = paged;
+    a->num_blocks = num_blocks;
+    a->page = paged ? (int)page : 0;
+    a->cu_q = static_cast<const int32_t*>(cu_q->data);
+    a->cu_k = static_cast<const int32_t*>(cu_k->data);
+    a->batch = (int)batch;
+    a->block_table = paged ? static_cast<const int32_t*>(bt->data) : nullptr;
+    a->bt_s0 = paged ? bt->stride[0] : 0;
+    a->bt_cols = paged ? (int)bt->shape[1] : 0;
+    a->max_sq = max_sq;
+    a->max_sk = max_sk;
+    a->H = (int)hq;
+    a->Hkv = (int)hkv;
+    a->D = (int)head_size;
+    a->scale = softmax_scale;
+    a->wl = wl < 0 ? -1 : wl;
+    a->wr = wr < 0 ? -1 : wr;
+    a->out = out->data;
+    a->o_s0 = out->stride[0];
+    a->o_s1 = out->stride[1];
+    a->lse = static_cast<float*>(lse->data);
+    a->lse_s0 = lse->stride[0];
+    a->total_q = total_q;
+    g_msg[0] = '\0';
+    return PA_OK;
+}
+
+// ---- per-(device, stream) split-KV workspace ------------------------------------------------
+std::mutex g_ws_mu;
+std::map<std::pair<int, cudaStream_t>, pa::Workspace> g_ws;
+
+int workspace_for(cudaStream_t stream, size_t bytes, void** ptr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(PA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    pa::Workspace& w = g_ws[{dev, stream}];
+    if (w.bytes < bytes) {
+        cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+        e = cudaStreamIsCapturing(stream, &st);
+        if (e != cudaSuccess) return fail(PA_ERR_CUDA, "cudaStreamIsCapturing: %s", cudaGetErrorString(e));
+        if (st != cudaStreamCaptureStatusNone)
+            return fail(PA_ERR_WORKSPACE,
+                        "split-KV workspace must grow to %zu bytes while the stream is capturing; run one call "
+                        "of the largest shape before capture",
+                        bytes);
+        if (w.ptr) {
+            e = cudaFree(w.ptr);  // synchronises the device: earlier calls are done with it
+            w.ptr = nullptr;
+            w.bytes = 0;
+            if (e != cudaSuccess) return fail(PA_ERR_CUDA, "cudaFree(workspace): %s", cudaGetErrorString(e));
+        }
+        size_t want = std::max(bytes + bytes / 4, (size_t)1 << 20);
+        e = cudaMalloc(&w.ptr, want);
+        if (e != cudaSuccess) {
+            w.ptr = nullptr;
+            return fail(PA_ERR_CUDA, "cudaMalloc(workspace, %zu): %s", want, cudaGetErrorString(e));
+        }
+        w.bytes = want;
+    }
+    *ptr = w.ptr;
+    return PA_OK;
+}
+
+int sm_count() {
+    static int cached[256] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return 148;
+    if (!cached[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult qres;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qres) ==
+                cudaSuccess &&
+            qres == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+}  // namespace
+
+namespace pa {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+int encode_tmap_4d(void* map, int dtype, const void* base, const uint64_t dims_[4], const uint64_t strides_bytes[3],
+                   const uint32_t box[4], int swizzle128, char* msg, size_t msg_len) {
+    auto fn = encode_fn();
+    if (!fn) {
+        snprintf(msg, msg_len, "cuTensorMapEncodeTiled is not available from the driver");
+        return PA_ERR_CUDA;
+    }
+    cuuint64_t gdim[4] = {dims_[0], dims_[1], dims_[2], dims_[3]};
+    cuuint64_t gstride[3] = {strides_bytes[0], strides_bytes[1], strides_bytes[2]};
+    cuuint32_t bdim[4] = {box[0], box[1], box[2], box[3]};
+    cuuint32_t estride[4] = {1, 1, 1, 1};
+    CUresult r = fn(reinterpret_cast<CUtensorMap*>(map),
+                    dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                    const_cast<void*>(base), gdim, gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(msg, msg_len,
+                 "cuTensorMapEncodeTiled failed (%d): dims [%llu %llu %llu %llu], strides [%llu %llu %llu] bytes", (int)r,
+                 (unsigned long long)gdim[0], (unsigned long long)gdim[1], (unsigned long long)gdim[2],
+                 (unsigned long long)gdim[3], (unsigned long long)gstride[0], (unsigned long long)gstride[1],
+                 (unsigned long long)gstride[2]);
+        return PA_ERR_UNSUPPORTED;
+    }
+    return PA_OK;
+}
+
+SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, int num_sms) {
+    SplitPlan pl{};
+    pl.dp = a.D <= 64 ? 64 : a.D <= 128 ? 128 : a.D <= 256 ? 256 : 512;
+    pl.nt = pl.dp == 512 ? 32 : 64;
+    const int G = a.H / a.Hkv;
+    const int64_t rows_max = (int64_t)a.max_sq * G;
+    pl.rows_cap = prefill_takes_long_rows ? prefill_rows_threshold() : (1 << 30);
+    const int64_t rows_here = std::max<int64_t>(1, std::min<int64_t>(rows_max, pl.rows_cap));
+    pl.mt = rows_here <= 16 ? 1 : 2;
+    const int M = 16 * pl.mt;
+    pl.row_tiles = (int)((rows_here + M - 1) / M);
+    // keys one row tile can touch: its queries span at most M / G + 1 positions
+    int64_t kspan = a.max_sk;
+    if (a.wl >= 0) kspan = std::min<int64_t>(kspan, (int64_t)a.wl + M / G + 1 + std::max(a.wr, 0) + 1);
+    const int64_t tiles_max = std::max<int64_t>(1, kspan / pl.nt + 2);
+    int64_t split_tiles = tiles_max;
+    const int64_t units = (int64_t)a.batch * a.Hkv * pl.row_tiles;
+    if (const char* env = std::getenv("PA_SPLIT_TILES")) {
+        split_tiles = std::max<int64_t>(1, std::atoll(env));
+    } else if (pl.row_tiles == 1) {
+        // aim at about four CTAs of work per SM; a split never shorter than 4 tiles
+        const int64_t target = 4ll * num_sms;
+        int64_t splits = (target + units - 1) / units;
+        splits = std::max<int64_t>(1, std::min(splits, tiles_max));
+        split_tiles = std::max<int64_t>(4, (tiles_max + splits - 1) / splits);
+    }
+    split_tiles = std::min(split_tiles, tiles_max);
+    pl.split_tiles = (int)split_tiles;
+    pl.max_splits = (int)((tiles_max + split_tiles - 1) / split_tiles);
+    pl.ws_bytes = 0;
+    if (pl.max_splits > 1) {
+        const size_t rows = (size_t)a.total_q * a.H;
+        pl.ws_bytes = (size_t)pl.max_splits * rows * ((size_t)a.D + 1) * sizeof(float) + 256;
+    }
+    return pl;
+}
+
+int launch_splitkv(const Args& a, const SplitPlan& plan, void* workspace, unsigned int* err, char* msg,
+                   size_t msg_len) {
+    if (a.dtype == PA_BF16) return launch_splitkv_bf16(a, plan, workspace, err, msg, msg_len);
+    return launch_splitkv_f16(a, plan, workspace, err, msg, msg_len);
+}
+
+}  // namespace pa
+
+extern "C" {
+
+int pa_varlen_check(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                    const pa_tensor* cu_seqlens_q, const pa_tensor* cu_seqlens_k, const pa_tensor* block_table,
+                    int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_heads, int32_t num_heads_k,
+                    int32_t head_dim, int32_t page_block_size, float softmax_scale, int32_t window_left,
+                    int32_t window_right, const pa_tensor* out, const pa_tensor* softmax_lse) {
+    pa::Args a{};
+    return validate(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, max_seqlen_q, max_seqlen_k,
+                    num_heads, num_heads_k, head_dim, page_block_size, softmax_scale, window_left, window_right, out,
+                    softmax_lse, false, &a);
+}
+
+int pa_varlen_fwd(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                  const pa_tensor* cu_seqlens_q, const pa_tensor* cu_seqlens_k, const pa_tensor* block_table,
+                  int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_heads, int32_t num_heads_k,
+                  int32_t head_dim, int32_t page_block_size, float softmax_scale, int32_t window_left,
+                  int32_t window_right, const pa_tensor* out, const pa_tensor* softmax_lse, void* stream) {
+    pa::Args a{};
+    int rc = validate(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, max_seqlen_q, max_seqlen_k,
+                      num_heads, num_heads_k, head_dim, page_block_size, softmax_scale, window_left, window_right,
+                      out, softmax_lse, true, &a);
+    if (rc != PA_OK) return rc;
+    a.stream = static_cast<cudaStream_t>(stream);
+    if (a.total_q == 0 || a.batch == 0) return PA_OK;
+
+    unsigned int* err = nullptr;
+    int ce = pa::error_word(&err);
+    if (ce != cudaSuccess) return fail(PA_ERR_CUDA, "error word: %s", cudaGetErrorString((cudaError_t)ce));
+
+    const bool use_prefill = pa::prefill_supported(a);
+    const pa::SplitPlan plan = pa::plan_splitkv(a, use_prefill, sm_count());
+    void* ws = nullptr;
+    if (plan.ws_bytes) {
+        rc = workspace_for(a.stream, plan.ws_bytes, &ws);
+        if (rc != PA_OK) return rc;
+    }
+    if (use_prefill) {
+        rc = pa::launch_prefill(a, err, g_msg, sizeof g_msg);
+        if (rc != PA_OK) return rc;
+    }
+    rc = pa::launch_splitkv(a, plan, ws, err, g_msg, sizeof g_msg);
+    if (rc != PA_OK) return rc;
+    g_msg[0] = '\0';
+    return PA_OK;
+}
+
+const char* pa_last_error(void) { return g_msg; }
+
+int pa_device_status(void* stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(PA_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+    unsigned int* word = nullptr;
+    int ce = pa::error_word(&word);
+    if (ce != cudaSuccess) return fail(PA_ERR_CUDA, "error word: %s", cudaGetErrorString((cudaError_t)ce));
+    unsigned int v = 0;
+    e = cudaMemcpy(&v, word, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(PA_ERR_CUDA, "reading the error word: %s", cudaGetErrorString(e));
+    if (!v) {
+        g_msg[0] = '\0';
+        return PA_OK;
+    }
+    e = cudaMemset(word, 0, sizeof v);
+    if (e != cudaSuccess) return fail(PA_ERR_CUDA, "clearing the error word: %s", cudaGetErrorString(e));
+    const int code = (int)(v & 0xffu);
+    if (code == PA_ERR_DEVICE_TIMEOUT)
+        return fail(code, "a kernel gave up a bounded wait (its output is undefined)");
+    return fail(code, "a kernel met out-of-range metadata (block id, page, cu_seqlens or max_seqlen); "
+                      "that work was skipped and its output is undefined");
+}
+
+int pa_version(void) { return 100; }
+
+uint64_t pa_kernel_launches(void) { return pa::g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

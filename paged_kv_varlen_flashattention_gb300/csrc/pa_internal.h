@@ -1,0 +1,89 @@
+// Internal interface between the C-ABI front end (api.cpp) and the kernel
+// translation units.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pa_varlen.h"
+
+#ifndef PA_WAIT_LIMIT_NS
+#define PA_WAIT_LIMIT_NS 2000000000ull  // a bounded wait gives up after 2 s of wall time
+#endif
+
+namespace pa {
+
+// Validated, flattened arguments of one pa_varlen_fwd call (element strides).
+struct Args {
+    int dtype;  // PA_F16 or PA_BF16
+    const void* q;
+    int64_t q_s0, q_s1;
+    const void* k;
+    const void* v;
+    // paged: strides of (block, slot, head); non-paged: (token, unused, head)
+    int64_t kv_s0, kv_s1, kv_s2;
+    bool paged;
+    int64_t num_blocks;  // paged: k_cache.shape[0]; non-paged: total_k
+    int page;            // page_block_size (0 when non-paged)
+    const int32_t* cu_q;
+    const int32_t* cu_k;
+    int batch;
+    const int32_t* block_table;
+    int64_t bt_s0;
+    int bt_cols;
+    int max_sq, max_sk;
+    int H, Hkv, D;
+    float scale;
+    int wl, wr;
+    void* out;
+    int64_t o_s0, o_s1;
+    float* lse;
+    int64_t lse_s0;
+    int64_t total_q;
+    cudaStream_t stream;
+};
+
+// Scratch the split-KV path needs for a call (bytes), and where to put it.
+struct Workspace {
+    void* ptr;
+    size_t bytes;
+};
+
+// Launch plan of the split-KV kernel (host-chosen; device recomputes the per-tile view).
+struct SplitPlan {
+    int dp;           // padded head dim: 64, 128, 256, 512
+    int mt;           // 16-row groups per CTA (1 or 2)
+    int nt;           // keys per tile (64 or 32)
+    int row_tiles;    // row tiles per (sequence, kv head)
+    int rows_cap;     // sequences with sq*G above this belong to the tensor-core prefill kernel
+    int split_tiles;  // key tiles per split
+    int max_splits;   // grid.x
+    size_t ws_bytes;  // partial-result scratch needed (0 when max_splits == 1)
+};
+
+// Dense-prefill (tcgen05) launch availability for these arguments.
+bool prefill_supported(const Args& a);
+int prefill_rows_threshold();  // sequences with sq*G > this go to the prefill kernel
+int launch_prefill(const Args& a, unsigned int* err, char* msg, size_t msg_len);
+
+SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, int num_sms);
+int launch_splitkv(const Args& a, const SplitPlan& plan, void* workspace, unsigned int* err, char* msg,
+                   size_t msg_len);
+int launch_splitkv_bf16(const Args& a, const SplitPlan& plan, void* workspace, unsigned int* err, char* msg,
+                        size_t msg_len);
+int launch_splitkv_f16(const Args& a, const SplitPlan& plan, void* workspace, unsigned int* err, char* msg,
+                       size_t msg_len);
+
+// Device address (current device) of the library's error word, which kernels set
+// with the first PA_ERR_DEVICE_* code they meet (bit 31 = set).  Returns a cudaError_t.
+int error_word(unsigned int** ptr);
+
+// Counts successful kernel launches (pa_kernel_launches).
+void count_launches(int n);
+
+// Tensor-map encoding through the driver entry point (no libcuda link needed).
+// Rank-4 bf16/f16 map over (d0 fastest .. d3), strides in bytes for dims 1..3.
+int encode_tmap_4d(void* map, int dtype, const void* base, const uint64_t dims[4], const uint64_t strides_bytes[3],
+                   const uint32_t box[4], int swizzle128, char* msg, size_t msg_len);
+
+}  // namespace pa

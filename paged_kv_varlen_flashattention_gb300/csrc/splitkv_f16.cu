@@ -1,0 +1,9 @@
+// fp16 instantiations of the split-KV and combine kernels.
+#include "splitkv_launch.cuh"
+
+namespace pa {
+int launch_splitkv_f16(const Args& a, const SplitPlan& plan, void* workspace, unsigned int* err, char* msg,
+                       size_t msg_len) {
+    return launch_splitkv_t<__half>(a, plan, workspace, err, msg, msg_len);
+}
+}  // namespace pa

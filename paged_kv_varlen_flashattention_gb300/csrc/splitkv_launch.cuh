@@ -1,0 +1,158 @@
+// Host-side launch of the split-KV kernel and the combine kernel for one element
+// type.  Included by one translation unit per type so the instantiations compile
+// in parallel.
+#pragma once
+
+#include <cstdio>
+
+#include "splitkv_kernel.cuh"
+
+namespace pa {
+
+template <int DP>
+struct SplitShape;  // tile width and pipeline depth per padded head dim
+template <>
+struct SplitShape<64> {
+    static constexpr int NT = 64, STAGES = 4;
+};
+template <>
+struct SplitShape<128> {
+    static constexpr int NT = 64, STAGES = 3;
+};
+template <>
+struct SplitShape<256> {
+    static constexpr int NT = 64, STAGES = 3;
+};
+template <>
+struct SplitShape<512> {
+    static constexpr int NT = 32, STAGES = 2;  // 3 stages would exceed 227 KB with a 32-row Q tile
+};
+
+template <typename T, int DP, int MT>
+static int run_splitkv(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& sp, const SplitPlan& plan,
+                       cudaStream_t stream, char* msg, size_t msg_len) {
+    constexpr int NT = SplitShape<DP>::NT, STAGES = SplitShape<DP>::STAGES;
+    using C = SplitCfg<DP, MT, NT, STAGES>;
+    auto kern = splitkv_kernel<T, DP, MT, NT, STAGES>;
+    static bool configured = false;  // attribute set once per process (per instantiation)
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) {
+            snprintf(msg, msg_len, "cudaFuncSetAttribute(split-KV, %d bytes): %s", C::SMEM, cudaGetErrorString(e));
+            return PA_ERR_CUDA;
+        }
+        configured = true;
+    }
+    dim3 grid(plan.max_splits, sp.Hkv * plan.row_tiles, sp.batch);
+    kern<<<grid, 128, C::SMEM, stream>>>(tk, tv, sp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        snprintf(msg, msg_len, "split-KV launch: %s", cudaGetErrorString(e));
+        return PA_ERR_CUDA;
+    }
+    count_launches(1);
+    if (plan.max_splits > 1) {
+        dim3 g2(1, sp.Hkv * plan.row_tiles, sp.batch);
+        combine_kernel<T, C::M, NT><<<g2, 128, 0, stream>>>(sp);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) {
+            snprintf(msg, msg_len, "split-KV combine launch: %s", cudaGetErrorString(e));
+            return PA_ERR_CUDA;
+        }
+        count_launches(1);
+    }
+    return PA_OK;
+}
+
+template <typename T>
+static int launch_splitkv_t(const Args& a, const SplitPlan& plan, void* workspace, unsigned int* err, char* msg,
+                            size_t msg_len) {
+    const int NT = plan.dp == 512 ? 32 : 64;
+    // Box rows: the largest of {NT, 32} that divides the page, so that a box never
+    // straddles two pages (page sizes are multiples of 32).
+    int box_rows = NT;
+    if (a.paged && (a.page % NT) != 0) box_rows = 32;
+    CUtensorMap tk, tv;
+    uint64_t dims[4];
+    uint64_t strides[3];
+    if (a.paged) {
+        dims[0] = (uint64_t)a.D;
+        dims[1] = (uint64_t)a.Hkv;
+        dims[2] = (uint64_t)a.page;
+        dims[3] = (uint64_t)a.num_blocks;
+        strides[0] = (uint64_t)a.kv_s2 * 2;
+        strides[1] = (uint64_t)a.kv_s1 * 2;
+        strides[2] = (uint64_t)a.kv_s0 * 2;
+    } else {
+        dims[0] = (uint64_t)a.D;
+        dims[1] = (uint64_t)a.Hkv;
+        dims[2] = (uint64_t)(a.num_blocks > 0 ? a.num_blocks : 1);
+        dims[3] = 1;
+        strides[0] = (uint64_t)a.kv_s2 * 2;
+        strides[1] = (uint64_t)a.kv_s0 * 2;
+        strides[2] = (uint64_t)a.kv_s0 * 2 * dims[2];
+    }
+    const uint32_t box[4] = {64u, 1u, (uint32_t)box_rows, 1u};
+    int rc = encode_tmap_4d(&tk, a.dtype, a.k, dims, strides, box, 1, msg, msg_len);
+    if (rc != PA_OK) return rc;
+    rc = encode_tmap_4d(&tv, a.dtype, a.v, dims, strides, box, 1, msg, msg_len);
+    if (rc != PA_OK) return rc;
+
+    SplitParams sp{};
+    sp.q = a.q;
+    sp.q_s0 = a.q_s0;
+    sp.q_s1 = a.q_s1;
+    sp.out = a.out;
+    sp.o_s0 = a.o_s0;
+    sp.o_s1 = a.o_s1;
+    sp.lse = a.lse;
+    sp.lse_s0 = a.lse_s0;
+    sp.cu_q = a.cu_q;
+    sp.cu_k = a.cu_k;
+    sp.bt = a.block_table;
+    sp.bt_s0 = a.bt_s0;
+    sp.bt_cols = a.bt_cols;
+    sp.batch = a.batch;
+    sp.H = a.H;
+    sp.Hkv = a.Hkv;
+    sp.G = a.H / a.Hkv;
+    sp.D = a.D;
+    sp.P = a.paged ? a.page : 1;
+    sp.num_blocks = a.num_blocks;
+    sp.total_q = a.total_q;
+    sp.paged = a.paged ? 1 : 0;
+    sp.box_rows = box_rows;
+    sp.boxes_per_tile = NT / box_rows;
+    sp.max_sq = a.max_sq;
+    sp.max_sk = a.max_sk;
+    sp.scale_log2 = a.scale * 1.4426950408889634f;
+    sp.wl = a.wl;
+    sp.wr = a.wr;
+    sp.rows_cap = plan.rows_cap;
+    sp.row_tiles = plan.row_tiles;
+    sp.split_tiles = plan.split_tiles;
+    sp.max_splits = plan.max_splits;
+    sp.part_stride = a.total_q * a.H;
+    if (plan.max_splits > 1) {
+        sp.part_o = static_cast<float*>(workspace);
+        sp.part_lse = sp.part_o + (size_t)plan.max_splits * sp.part_stride * a.D;
+    }
+    sp.err = err;
+
+#define PA_SPLIT_CASE(DPV, MTV)                                                        \
+    if (plan.dp == DPV && plan.mt == MTV)                                              \
+        return run_splitkv<T, DPV, MTV>(tk, tv, sp, plan, a.stream, msg, msg_len);
+    PA_SPLIT_CASE(64, 1)
+    PA_SPLIT_CASE(64, 2)
+    PA_SPLIT_CASE(128, 1)
+    PA_SPLIT_CASE(128, 2)
+    PA_SPLIT_CASE(256, 1)
+    PA_SPLIT_CASE(256, 2)
+    PA_SPLIT_CASE(512, 1)
+    PA_SPLIT_CASE(512, 2)
+#undef PA_SPLIT_CASE
+    snprintf(msg, msg_len, "no split-KV kernel for head_dim tile %d, row groups %d", plan.dp, plan.mt);
+    return PA_ERR_UNSUPPORTED;
+}
+
+}  // namespace pa

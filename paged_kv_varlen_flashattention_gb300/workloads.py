@@ -225,7 +225,7 @@ class Inputs:
     block_table: "object"
 
     def to(self, device):
-        return Inputs(self.layout, *(t.to(device) for t in (
+        return Inputs(self.layout, *(None if t is None else t.to(device) for t in (
             self.q, self.k_cache, self.v_cache, self.cu_seqlens_q, self.cu_seqlens_k,
             self.block_table)))
 

@@ -1,0 +1,137 @@
+"""CUDA path vs the oracle on the same seeded inputs (GPU)."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_varlen_flashattention_gb300 import binding, workloads
+from tests import _gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def test_tiny_fp16_all_rows():
+    _gpu.check_layout(workloads.tiny_fp16(), gen_device="cpu")
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill", "mixed", "long", "d512"])
+def test_reduced_workloads_all_rows(name):
+    _gpu.check_layout(workloads.small(name))
+
+
+@pytest.mark.parametrize("name,limit", [("decode_bf16", 1024), ("prefill_bf16", 768), ("mixed_bf16", 768),
+                                        ("long_bf16", 96), ("long_d512_bf16", 256)])
+def test_full_size_sampled_rows(name, limit):
+    _gpu.check_layout(workloads.CONFIGS[name](), limit=limit)
+
+
+def _custom(sq, sk, H=4, Hkv=2, D=64, P=32, dtype="bf16", wl=-1, wr=0, seed=21, **kw):
+    return workloads.make_layout("custom", dtype, sq, sk, num_heads=H, num_heads_k=Hkv, head_dim=D,
+                                 page_block_size=P, seed=seed, spare=0.2, window_left=wl, window_right=wr, **kw)
+
+
+def test_empty_sequences():
+    _gpu.check_layout(_custom([0, 3, 2, 1], [5, 0, 40, 70]))
+
+
+def test_more_queries_than_keys_fully_masked_rows():
+    _gpu.check_layout(_custom([10, 7], [4, 7]))
+
+
+@pytest.mark.parametrize("wl,wr", [(-1, -1), (3, 2), (0, 0), (17, -1), (-1, 5)])
+def test_windows(wl, wr):
+    _gpu.check_layout(_custom([1, 9, 40, 3], [100, 64, 200, 33], wl=wl, wr=wr))
+
+
+@pytest.mark.parametrize("D", [8, 80, 96, 192, 256, 320, 512])
+def test_head_dims(D):
+    _gpu.check_layout(_custom([1, 5, 12], [77, 150, 12], H=4, Hkv=1, D=D))
+
+
+@pytest.mark.parametrize("P", [32, 96, 160, 256])
+def test_page_sizes(P):
+    _gpu.check_layout(_custom([2, 33, 1], [300, 99, 520], P=P, H=8, Hkv=2, D=128))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_decode_dtypes(dtype):
+    lay = workloads.small("decode")
+    lay.dtype = dtype
+    _gpu.check_layout(lay)
+
+
+@pytest.mark.parametrize("tiles", ["1", "2", "5"])
+def test_forced_split_counts(tiles, monkeypatch):
+    monkeypatch.setenv("PA_SPLIT_TILES", tiles)
+    _gpu.check_layout(workloads.small("decode"))
+    _gpu.check_layout(workloads.small("long"))
+
+
+def test_non_paged_mode():
+    lay = _custom([3, 1, 20], [50, 129, 20], H=8, Hkv=2, D=128)
+    lay.paged = False
+    _gpu.check_layout(lay)
+
+
+def test_strided_q_and_out():
+    lay = _custom([3, 4], [40, 70], H=4, Hkv=2, D=64)
+    inp = workloads.materialize(lay, device="cuda")
+    big = torch.zeros((lay.total_q, 8, 72), dtype=inp.q.dtype, device="cuda")
+    big[:, 2:6, :64] = inp.q
+    q_view = big[:, 2:6, :64]
+    out_big = torch.zeros((lay.total_q, 6, 72), dtype=inp.q.dtype, device="cuda")
+    out_view = out_big[:, 1:5, :64]
+    inp2 = workloads.Inputs(lay, q_view, inp.k_cache, inp.v_cache, inp.cu_seqlens_q, inp.cu_seqlens_k,
+                            inp.block_table)
+    out, lse = _gpu.run_cuda(inp2, out=out_view)
+    assert out.data_ptr() == out_view.data_ptr()
+    ref_o, ref_l = _gpu.oracle_for(inp.to("cpu"))
+    _gpu.compare(lay, out.contiguous(), lse, ref_o, ref_l)
+    assert torch.all(out_big[:, 0] == 0) and torch.all(out_big[:, 5] == 0)
+
+
+def test_block_permutation_bit_identical():
+    lay = workloads.small("mixed")
+    inp = workloads.materialize(lay, device="cuda")
+    out1, lse1 = _gpu.run_cuda(inp)
+    inp2 = workloads.with_block_permutation(inp, seed=5)
+    out2, lse2 = _gpu.run_cuda(inp2)
+    assert torch.equal(out1, out2)
+    assert torch.equal(lse1, lse2)
+
+
+def test_bad_block_id_is_reported_not_faulted():
+    lay = _custom([1, 1], [100, 64], H=4, Hkv=2, D=64)
+    inp = workloads.materialize(lay, device="cuda")
+    inp.block_table[0, 1] = lay.num_blocks + 1000
+    inp.block_table[1, 0] = -7
+    binding.varlen_fwd(inp.q, inp.k_cache, inp.v_cache, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.block_table,
+                       max_seqlen_q=1, max_seqlen_k=100)
+    st = binding.device_status()
+    assert binding.STATUS[st] == "PA_ERR_DEVICE_BOUNDS", binding.last_error()
+    assert binding.device_status() == 0  # cleared
+
+
+def test_sequence_longer_than_max_seqlen_k_is_reported():
+    lay = _custom([1, 1], [300, 64], H=4, Hkv=2, D=64)
+    inp = workloads.materialize(lay, device="cuda")
+    binding.varlen_fwd(inp.q, inp.k_cache, inp.v_cache, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.block_table,
+                       max_seqlen_q=1, max_seqlen_k=64)
+    assert binding.STATUS[binding.device_status()] == "PA_ERR_DEVICE_BOUNDS"
+
+
+def test_host_memory_is_rejected():
+    lay = workloads.tiny_fp16()
+    inp = workloads.materialize(lay, device="cuda")
+    with pytest.raises(binding.PaError) as ei:
+        binding.varlen_fwd(inp.q, inp.k_cache, inp.v_cache, inp.cu_seqlens_q, inp.cu_seqlens_k,
+                           inp.block_table.cpu(), max_seqlen_q=5, max_seqlen_k=70)
+    assert ei.value.name == "PA_ERR_NOT_DEVICE" and "block_table must be a cuda tensor" in str(ei.value)
+
+
+def test_zero_queries_is_a_no_op():
+    lay = _custom([0, 0], [5, 7])
+    inp = workloads.materialize(lay, device="cuda")
+    out, lse = _gpu.run_cuda(inp)
+    assert out.numel() == 0 and lse.numel() == 0

@@ -1,0 +1,161 @@
+"""Host-side validation through pa_varlen_check (no GPU, no CUDA call).
+
+The cases come from the candle error-explanation pages (tests/golden/validation_cases.json,
+each with its citation); the descriptors point at fake, 16-byte aligned addresses because
+the check never dereferences them."""
+import json
+import os
+
+import pytest
+
+from paged_kv_varlen_flashattention_gb300 import binding
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "validation_cases.json")
+CASES = json.load(open(GOLDEN))["cases"]
+CODES = {v: k for k, v in binding.STATUS.items()}
+
+
+def contiguous(shape):
+    st, acc = [], 1
+    for s in reversed(shape):
+        st.append(acc)
+        acc *= s
+    return list(reversed(st))
+
+
+def desc(shape, dtype, stride=None, addr=0x100000):
+    d = binding.PaTensor()
+    d.data = addr
+    d.dtype = dtype
+    d.ndim = len(shape)
+    for i, s in enumerate(shape):
+        d.shape[i] = s
+    for i, s in enumerate(stride or contiguous(shape)):
+        d.stride[i] = s
+    return d
+
+
+def build(case):
+    q = case.get("q", [8, 4, 64])
+    k = case.get("k", [6, 32, 2, 64])
+    v = case.get("v", [6, 32, 2, 64])
+    out = case.get("out", q if len(q) == 3 else [8, 4, 64])
+    bt = case.get("block_table", [2, 3])
+    H = q[-2] if len(q) >= 2 else 4
+    D = case.get("head_dim", q[-1])
+    Hkv = k[-2]
+    P = case.get("page_block_size", 32)
+    ds = [
+        desc(q, binding.PA_BF16, case.get("q_stride")),
+        desc(k, binding.PA_BF16, case.get("k_stride")),
+        desc(v, binding.PA_BF16, case.get("v_stride")),
+        desc([3], binding.PA_I32, case.get("cu_q_stride")),
+        desc([3], binding.PA_I32, case.get("cu_k_stride")),
+        None if bt is None else desc(bt, binding.PA_I32, case.get("bt_stride")),
+        desc(out, binding.PA_BF16),
+        desc([4, 8], binding.PA_F32),
+    ]
+    return ds, H, Hkv, D, (P if bt is not None else 0)
+
+
+def run_check(ds, H, Hkv, D, P, max_sq=5, max_sk=64, wl=-1, wr=0, scale=0.125):
+    lib = binding.load()
+    r = lambda d: None if d is None else binding.ctypes.byref(d)  # noqa: E731
+    rc = lib.pa_varlen_check(r(ds[0]), r(ds[1]), r(ds[2]), r(ds[3]), r(ds[4]), r(ds[5]), max_sq, max_sk, H, Hkv,
+                             D, P, scale, wl, wr, r(ds[6]), r(ds[7]))
+    return rc, lib.pa_last_error().decode()
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c["name"] for c in CASES])
+def test_page_case(case):
+    ds, H, Hkv, D, P = build(case)
+    rc, msg = run_check(ds, H, Hkv, D, P)
+    assert binding.STATUS[rc] == case["expect"], (msg, case["citation"])
+    if "message" in case:
+        assert case["message"] in msg, msg
+    if rc == 0:
+        assert msg == ""
+
+
+def _base():
+    return build({})
+
+
+def test_scalar_disagreement_is_an_argument_error():
+    ds, H, Hkv, D, P = _base()
+    assert run_check(ds, H + 1, Hkv, D, P)[0] == CODES["PA_ERR_ARG"]
+    assert run_check(ds, H, Hkv, D + 8, P)[0] == CODES["PA_ERR_ARG"]
+    assert run_check(ds, H, Hkv + 1, D, P)[0] == CODES["PA_ERR_ARG"]
+
+
+def test_gqa_divisibility():
+    ds, _, _, D, P = build({"q": [8, 3, 64], "out": [8, 3, 64]})
+    ds[7] = desc([3, 8], binding.PA_F32)
+    rc, msg = run_check(ds, 3, 2, D, P)
+    assert rc == CODES["PA_ERR_ARG"] and "multiple of num_heads_k" in msg
+
+
+def test_dtype_rules():
+    ds, H, Hkv, D, P = _base()
+    ds[1] = desc([6, 32, 2, 64], binding.PA_F16)
+    assert run_check(ds, H, Hkv, D, P)[0] == CODES["PA_ERR_ARG"]
+    ds, H, Hkv, D, P = _base()
+    ds[7] = desc([4, 8], binding.PA_BF16)
+    assert run_check(ds, H, Hkv, D, P)[0] == CODES["PA_ERR_ARG"]
+    ds, H, Hkv, D, P = _base()
+    ds[3] = desc([3], binding.PA_F32)
+    assert run_check(ds, H, Hkv, D, P)[0] == CODES["PA_ERR_ARG"]
+    ds, H, Hkv, D, P = _base()
+    for i in (0, 1, 2, 6):
+        ds[i].dtype = binding.PA_F32
+    assert run_check(ds, H, Hkv, D, P)[0] == CODES["PA_ERR_UNSUPPORTED"]
+
+
+def test_out_and_lse_shapes():
+    ds, H, Hkv, D, P = _base()
+    ds[6] = desc([8, 4, 32], binding.PA_BF16)
+    assert run_check(ds, H, Hkv, D, P)[0] == CODES["PA_ERR_ARG"]
+    ds, H, Hkv, D, P = _base()
+    ds[7] = desc([8, 4], binding.PA_F32)
+    assert run_check(ds, H, Hkv, D, P)[0] == CODES["PA_ERR_ARG"]
+
+
+def test_block_table_rows_and_width():
+    ds, H, Hkv, D, P = _base()
+    ds[5] = desc([3, 3], binding.PA_I32)
+    assert run_check(ds, H, Hkv, D, P)[0] == CODES["PA_ERR_ARG"]
+    ds, H, Hkv, D, P = _base()
+    rc, msg = run_check(ds, H, Hkv, D, P, max_sk=97)  # 3 pages of 32 hold 96 keys
+    assert rc == CODES["PA_ERR_ARG"] and "too few for max_seqlen_k" in msg
+    assert run_check(ds, H, Hkv, D, P, max_sk=96)[0] == 0
+
+
+def test_implementation_limits():
+    ds, H, Hkv, D, P = build({"q": [8, 4, 60], "k": [6, 32, 2, 60], "v": [6, 32, 2, 60], "out": [8, 4, 60]})
+    rc, msg = run_check(ds, H, Hkv, 60, P)
+    assert rc == CODES["PA_ERR_UNSUPPORTED"] and "multiple of 8" in msg
+    ds, H, Hkv, D, P = _base()
+    ds[0].data = 0x100008  # not 16-byte aligned
+    assert run_check(ds, H, Hkv, D, P)[0] == CODES["PA_ERR_UNSUPPORTED"]
+    ds, H, Hkv, D, P = _base()
+    ds[0].stride[0] = 260  # not a multiple of 8 elements
+    assert run_check(ds, H, Hkv, D, P)[0] == CODES["PA_ERR_UNSUPPORTED"]
+
+
+def test_non_finite_scale():
+    ds, H, Hkv, D, P = _base()
+    assert run_check(ds, H, Hkv, D, P, scale=float("nan"))[0] == CODES["PA_ERR_ARG"]
+
+
+def test_check_order_follows_the_pages():
+    """Several faults at once: the rank fault is reported before contiguity, contiguity
+    before shapes, shapes before the page size, the page size before the head size."""
+    ds, H, Hkv, D, P = build({"k": [192, 2, 64], "v": [192, 2, 64], "q_stride": [512, 128, 2]})
+    assert run_check(ds, H, Hkv, D, P)[0] == CODES["PA_ERR_RANK_PAGED"]
+    ds, H, Hkv, D, P = build({"q_stride": [512, 128, 2], "v": [6, 32, 1, 64]})
+    assert run_check(ds, H, Hkv, D, P)[0] == CODES["PA_ERR_NONCONTIG"]
+    ds, H, Hkv, D, P = build({"v": [6, 32, 1, 64], "page_block_size": 0})
+    assert run_check(ds, H, Hkv, D, P)[0] == CODES["PA_ERR_SHAPE"]
+    ds, H, Hkv, D, P = build({"q": [8, 4, 576], "k": [6, 16, 2, 576], "v": [6, 16, 2, 576], "out": [8, 4, 576],
+                              "head_dim": 576, "page_block_size": 16})
+    assert run_check(ds, H, Hkv, D, P)[0] == CODES["PA_ERR_PAGE_MULT32"]
