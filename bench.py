@@ -276,9 +276,11 @@ def run_ours(args):
     hbm, bf16, bf16_sus, peak_kind = peaks()
 
     # a sustained run of the same step while the clock sampler warms up
+    if args.profile:
+        args.no_e2e = args.no_secondary = args.no_cpu_baseline = True
     sampler = ClockSampler(torch.cuda.current_device() if world == 1 else local)
     sampler.start()
-    t_end = time.time() + 1.0
+    t_end = time.time() + (0.0 if args.profile else 1.0)
     out = torch.empty_like(g.q)
     lse = torch.empty((lay.num_heads, lay.total_q), dtype=torch.float32, device="cuda")
     while time.time() < t_end:
@@ -401,6 +403,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-sequences", type=int, default=16)
+    ap.add_argument("--profile", action="store_true",
+                    help="only warm-up + timed steps (no clock warm-up loop, e2e, secondary or CPU legs): "
+                         "the command the ncu summaries are taken with")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

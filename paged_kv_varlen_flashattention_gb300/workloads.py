@@ -234,6 +234,8 @@ def _randn(shape, std, dtype, gen, device, chunk_rows=1 << 14):
     """N(0, std^2) in fp32, rounded to ``dtype``; drawn in slabs to bound temporaries."""
     import torch
     out = torch.empty(shape, dtype=dtype, device=device)
+    if out.numel() == 0:
+        return out
     flat = out.view(shape[0], -1)
     for r0 in range(0, shape[0], chunk_rows):
         r1 = min(shape[0], r0 + chunk_rows)
