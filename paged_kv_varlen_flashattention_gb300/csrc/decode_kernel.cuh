@@ -1,0 +1,378 @@
+// Decode-class paged attention kernel with warp-private key slices.
+//
+// One CTA owns one (sequence, kv head, key split) with at most 32 query rows (the
+// (query, head) pairs of the GQA group, ordered i * G + g).  Warp 4 is the producer:
+// it walks the block table and issues TMA loads of K/V tiles into a ring of
+// shared-memory stages (full/empty mbarriers).  Warps 0..3 consume: warp w takes row
+// group w / KW and the w % KW-th slice of every tile's keys, computes its scores with
+// mma.sync, runs the online softmax inside the warp (quad shuffles only), feeds P from
+// registers straight into the P.V mma, and releases the stage.  No CTA-wide barrier
+// runs inside the key loop; the per-warp (max, sum, O) triples are merged once at the
+// end through shared memory.
+#pragma once
+
+#include "splitkv_kernel.cuh"
+
+namespace pa {
+
+template <int DP, int MG, int NT, int STAGES>
+struct DecCfg {
+    static constexpr int M = 16 * MG;        // rows per CTA
+    static constexpr int KW = 4 / MG;        // warps sharing one row group (key-slice ways)
+    static constexpr int KPW = NT / KW;      // keys per warp per tile
+    static constexpr int CH = DP / 64;
+    static constexpr int TILE_BYTES = CH * NT * 128;
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    static constexpr int Q_BYTES = CH * M * 128;
+    static constexpr int OFF_Q = STAGES * STAGE_BYTES;
+    static constexpr int OFF_ROW = OFF_Q + Q_BYTES;            // row_lo[M], row_hi[M]
+    static constexpr int OFF_ML = OFF_ROW + 2 * M * 4;         // m[4][16], l[4][16] of the merge
+    static constexpr int OFF_BAR = (OFF_ML + 2 * 4 * 16 * 4 + 15) & ~15;
+    static constexpr int OFF_FLAG = OFF_BAR + 2 * STAGES * 8;
+    static constexpr int SMEM = OFF_FLAG + 16 + 1024;
+    static constexpr int MERGE_BYTES = 4 * 16 * DP * 4;        // O of every warp, reuses the stages
+    static constexpr bool Q_IN_REGS = DP <= 128;
+    static_assert(KPW % 16 == 0, "keys per warp");
+    static_assert(MERGE_BYTES <= STAGES * STAGE_BYTES, "merge scratch");
+    static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
+};
+
+__device__ __forceinline__ bool dec_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                         unsigned int* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > PA_WAIT_LIMIT_NS) {
+            *abort_flag = 1u;
+            flag_error(err, PA_ERR_DEVICE_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+template <typename T, int DP, int MG, int NT, int STAGES>
+__global__ void __launch_bounds__(160) decode_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                     const __grid_constant__ CUtensorMap tm_v,
+                                                     const SplitParams p) {
+    using C = DecCfg<DP, MG, NT, STAGES>;
+    constexpr int M = C::M;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.z, hk = blockIdx.y % p.Hkv, split = blockIdx.x;
+
+    TileView tv;
+    if (!tile_view<M, NT>(p, b, 0, tv, split == 0)) return;
+    if (split >= max(tv.nsplit, 1)) return;
+    const bool single = tv.nsplit <= 1;
+    const int t_begin = split * p.split_tiles;
+    const int n_iter = max(0, min(tv.ntiles, t_begin + p.split_tiles) - t_begin);
+
+    int* row_lo = reinterpret_cast<int*>(smem + C::OFF_ROW);
+    int* row_hi = row_lo + M;
+    float* m_sm = reinterpret_cast<float*>(smem + C::OFF_ML);
+    float* l_sm = m_sm + 4 * 16;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* empty = full + STAGES;
+    volatile uint32_t* abort_flag = reinterpret_cast<uint32_t*>(smem + C::OFF_FLAG);
+
+    if (tid < M) {
+        int lo = 0, hi = -1;  // padding rows attend nothing
+        if (tid < tv.rows) {
+            const int64_t i = (tv.row0 + tid) / p.G;
+            const int64_t diag = i + tv.sk - tv.sq;
+            lo = p.wl >= 0 ? (int)max64(0, diag - p.wl) : 0;
+            hi = p.wr >= 0 ? (int)max64(-1, min64(tv.sk - 1, diag + p.wr)) : tv.sk - 1;
+        }
+        row_lo[tid] = lo;
+        row_hi[tid] = hi;
+    }
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 4);
+        }
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (tid < 128) {  // q rows -> shared memory (128-byte swizzled rows, zero padded)
+        const T* q = static_cast<const T*>(p.q);
+        constexpr int UNITS = DP / 8;
+        uint8_t* qs = smem + C::OFF_Q;
+        for (int idx = tid; idx < M * UNITS; idx += 128) {
+            const int r = idx / UNITS, u = idx - r * UNITS;
+            int4 val = make_int4(0, 0, 0, 0);
+            if (r < tv.rows && u * 8 < p.D) {
+                const int rho = tv.row0 + r;
+                const int i = rho / p.G, g = rho - i * p.G;
+                val = __ldg(reinterpret_cast<const int4*>(q + (int64_t)(tv.q0 + i) * p.q_s0 +
+                                                          (int64_t)(hk * p.G + g) * p.q_s1 + u * 8));
+            }
+            *reinterpret_cast<int4*>(qs + (u >> 3) * (M * 128) + swz128(r, u & 7)) = val;
+        }
+    }
+    __syncthreads();
+
+    if (warp == 4) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            const uint64_t policy = l2_policy_evict_first();
+            for (int it = 0; it < n_iter; ++it) {
+                const int stage = it % STAGES;
+                if (it >= STAGES && !dec_wait(&empty[stage], ((it / STAGES) - 1) & 1, abort_flag, p.err)) break;
+                const int kt = tv.kt0 + (t_begin + it) * NT;
+                uint8_t* kst = smem + stage * C::STAGE_BYTES;
+                uint8_t* vst = kst + C::TILE_BYTES;
+                int cs[4], cb[4];
+                bool live[4];
+                uint32_t bytes = 0;
+                for (int j = 0; j < p.boxes_per_tile; ++j) {
+                    live[j] = false;
+                    const int key = kt + j * p.box_rows;
+                    if (key >= tv.sk) continue;
+                    if (p.paged) {
+                        const int page = key / p.P;
+                        if (page >= p.bt_cols) {
+                            flag_error(p.err, PA_ERR_DEVICE_BOUNDS);
+                            continue;
+                        }
+                        const int blk = __ldg(p.bt + (int64_t)b * p.bt_s0 + page);
+                        if (blk < 0 || blk >= p.num_blocks) {
+                            flag_error(p.err, PA_ERR_DEVICE_BOUNDS);
+                            continue;
+                        }
+                        cs[j] = key - page * p.P;
+                        cb[j] = blk;
+                    } else {
+                        cs[j] = p.cu_k[b] + key;
+                        cb[j] = 0;
+                    }
+                    live[j] = true;
+                    bytes += 2u * C::CH * p.box_rows * 128u;
+                }
+                mbar_arrive_expect_tx(&full[stage], bytes);
+                for (int j = 0; j < p.boxes_per_tile; ++j) {
+                    if (!live[j]) continue;
+                    for (int c = 0; c < C::CH; ++c) {
+                        const int off = (c * NT + j * p.box_rows) * 128;
+                        tma_load_4d(kst + off, &tm_k, &full[stage], c * 64, hk, cs[j], cb[j], policy);
+                        tma_load_4d(vst + off, &tm_v, &full[stage], c * 64, hk, cs[j], cb[j], policy);
+                    }
+                }
+            }
+        }
+        return;  // the consumers synchronise among themselves with named barrier 1
+    }
+
+    // ---------------- consumers ----------------
+    const int rg = warp / C::KW, kq = warp % C::KW;
+    const int gq = lane >> 2, tq = lane & 3;
+    const int mi = lane >> 3, rr = lane & 7;
+    const int r0 = rg * 16 + gq, r1 = r0 + 8;  // the two rows this lane holds
+    const int lo0 = row_lo[r0], hi0 = row_hi[r0], lo1 = row_lo[r1], hi1 = row_hi[r1];
+    const uint32_t q_base = smem_addr(smem + C::OFF_Q);
+
+    uint32_t qf[C::Q_IN_REGS ? DP / 16 : 1][4];
+    if constexpr (C::Q_IN_REGS) {
+#pragma unroll
+        for (int ks = 0; ks < DP / 16; ++ks) {
+            const int row = rg * 16 + rr + ((mi & 1) << 3);
+            ldsm_x4(q_base + (ks >> 2) * (M * 128) + swz128(row, (ks & 3) * 2 + (mi >> 1)), qf[ks][0], qf[ks][1],
+                    qf[ks][2], qf[ks][3]);
+        }
+    }
+
+    float o[DP / 8][4];
+#pragma unroll
+    for (int n = 0; n < DP / 8; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[n][e] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    bool ok = true;
+
+    for (int it = 0; it < n_iter; ++it) {
+        const int stage = it % STAGES;
+        ok = __all_sync(0xffffffffu, dec_wait(&full[stage], (it / STAGES) & 1, abort_flag, p.err));
+        if (!ok) break;
+        const int kt = tv.kt0 + (t_begin + it) * NT;
+        uint8_t* kst = smem + stage * C::STAGE_BYTES;
+        uint8_t* vst = kst + C::TILE_BYTES;
+        const int key0 = kq * C::KPW;
+        // V rows of this warp's slice at or past sk -> 0 (NaN-safe P.V)
+        const int valid = tv.sk - kt;
+        const bool zeroed = valid < key0 + C::KPW;
+        if (zeroed) {
+            const int z0 = max(valid, key0), zr = key0 + C::KPW - z0;
+            for (int idx = lane; idx < C::CH * zr * 8; idx += 32) {
+                const int c = idx / (zr * 8), rem = idx - c * zr * 8;
+                *reinterpret_cast<int4*>(vst + (c * NT + z0 + (rem >> 3)) * 128 + ((rem & 7) << 4)) =
+                    make_int4(0, 0, 0, 0);
+            }
+            __syncwarp();
+        }
+        const uint32_t k_base = smem_addr(kst), v_base = smem_addr(vst);
+#pragma unroll
+        for (int kc = 0; kc < C::KPW / 16; ++kc) {
+            const int kk0 = key0 + kc * 16;
+            float s[2][4];
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[n][e] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < DP / 16; ++ks) {
+                uint32_t b00, b01, b10, b11;
+                const int key = kk0 + rr + ((mi >> 1) << 3);
+                ldsm_x4(k_base + (ks >> 2) * NT * 128 + swz128(key, (ks & 3) * 2 + (mi & 1)), b00, b01, b10, b11);
+                uint32_t af[4];
+                if constexpr (C::Q_IN_REGS) {
+                    af[0] = qf[ks][0];
+                    af[1] = qf[ks][1];
+                    af[2] = qf[ks][2];
+                    af[3] = qf[ks][3];
+                } else {
+                    const int row = rg * 16 + rr + ((mi & 1) << 3);
+                    ldsm_x4(q_base + (ks >> 2) * (M * 128) + swz128(row, (ks & 3) * 2 + (mi >> 1)), af[0], af[1], af[2],
+                            af[3]);
+                }
+                MmaOp<T>::run(s[0], af, b00, b01);
+                MmaOp<T>::run(s[1], af, b10, b11);
+            }
+            // scale into the log2 domain, mask by select, and take the row maxima
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int key = kt + kk0 + n * 8 + tq * 2 + (e & 1);
+                    const bool up = e < 2;
+                    const bool in = up ? (key >= lo0 && key <= hi0) : (key >= lo1 && key <= hi1);
+                    s[n][e] = in ? s[n][e] * p.scale_log2 : -INFINITY;
+                    if (up)
+                        mx0 = fmaxf(mx0, s[n][e]);
+                    else
+                        mx1 = fmaxf(mx1, s[n][e]);
+                }
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+            if (__any_sync(0xffffffffu, n0 > m0 || n1 > m1)) {  // a running max grew: rescale O and l
+                const float a0 = (n0 == -INFINITY) ? 1.f : fast_exp2(m0 - n0);
+                const float a1 = (n1 == -INFINITY) ? 1.f : fast_exp2(m1 - n1);
+#pragma unroll
+                for (int n = 0; n < DP / 8; ++n) {
+                    o[n][0] *= a0;
+                    o[n][1] *= a0;
+                    o[n][2] *= a1;
+                    o[n][3] *= a1;
+                }
+                l0 *= a0;
+                l1 *= a1;
+                m0 = n0;
+                m1 = n1;
+            }
+            const float u0 = m0 == -INFINITY ? 0.f : m0, u1 = m1 == -INFINITY ? 0.f : m1;
+            float pv[2][4];
+#pragma unroll
+            for (int n = 0; n < 2; ++n) {
+                pv[n][0] = fast_exp2(s[n][0] - u0);
+                pv[n][1] = fast_exp2(s[n][1] - u0);
+                pv[n][2] = fast_exp2(s[n][2] - u1);
+                pv[n][3] = fast_exp2(s[n][3] - u1);
+                l0 += pv[n][0] + pv[n][1];
+                l1 += pv[n][2] + pv[n][3];
+            }
+            // the score fragment of two n8 tiles is the A fragment of a k16 step
+            uint32_t pa[4];
+            pa[0] = pack2<T>(pv[0][0], pv[0][1]);
+            pa[1] = pack2<T>(pv[0][2], pv[0][3]);
+            pa[2] = pack2<T>(pv[1][0], pv[1][1]);
+            pa[3] = pack2<T>(pv[1][2], pv[1][3]);
+#pragma unroll
+            for (int np = 0; np < DP / 16; ++np) {
+                const int d0 = np * 16;
+                const int key = kk0 + rr + ((mi & 1) << 3);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(v_base + (d0 >> 6) * NT * 128 + swz128(key, ((d0 & 63) >> 3) + (mi >> 1)), b0, b1, b2, b3);
+                MmaOp<T>::run(o[2 * np], pa, b0, b1);
+                MmaOp<T>::run(o[2 * np + 1], pa, b2, b3);
+            }
+        }
+        if (zeroed) fence_proxy_async_smem();  // the stage is rewritten by TMA later
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
+    }
+
+    // ---- merge the KW key slices of each row group, then write ----
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    named_barrier_sync(1, 128);  // every consumer is done with the stages (reused below)
+    if (*abort_flag) return;     // set before the barrier by whichever role gave up
+    float* o_sm = reinterpret_cast<float*>(smem);  // [warp][16][DP]
+    if (tq == 0) {
+        m_sm[warp * 16 + gq] = m0;
+        m_sm[warp * 16 + gq + 8] = m1;
+        l_sm[warp * 16 + gq] = l0;
+        l_sm[warp * 16 + gq + 8] = l1;
+    }
+#pragma unroll
+    for (int n = 0; n < DP / 8; ++n) {
+        const int d = n * 8 + tq * 2;
+        *reinterpret_cast<float2*>(o_sm + (warp * 16 + gq) * DP + d) = make_float2(o[n][0], o[n][1]);
+        *reinterpret_cast<float2*>(o_sm + (warp * 16 + gq + 8) * DP + d) = make_float2(o[n][2], o[n][3]);
+    }
+    named_barrier_sync(1, 128);
+
+    T* out = static_cast<T*>(p.out);
+    // each thread: pairs of columns of one row
+    for (int idx = tid; idx < M * (DP / 2); idx += 128) {
+        const int row = idx / (DP / 2), d = (idx - row * (DP / 2)) * 2;
+        if (row >= tv.rows || d >= p.D) continue;
+        const int g16 = row >> 4, rw = row & 15;
+        float mm = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < C::KW; ++k) mm = fmaxf(mm, m_sm[(g16 * C::KW + k) * 16 + rw]);
+        const float mu = mm == -INFINITY ? 0.f : mm;
+        float L = 0.f, x0 = 0.f, x1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < C::KW; ++k) {
+            const int w = g16 * C::KW + k;
+            const float f = fast_exp2(m_sm[w * 16 + rw] - mu);
+            L += f * l_sm[w * 16 + rw];
+            const float2 ov = *reinterpret_cast<const float2*>(o_sm + (w * 16 + rw) * DP + d);
+            x0 += f * ov.x;
+            x1 += f * ov.y;
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const int rho = tv.row0 + row;
+        const int i = rho / p.G, g = rho - i * p.G;
+        const int64_t t = tv.q0 + i;
+        const int h = hk * p.G + g;
+        if (single)
+            *reinterpret_cast<uint32_t*>(out + t * p.o_s0 + (int64_t)h * p.o_s1 + d) = pack2<T>(x0 * inv, x1 * inv);
+        else
+            *reinterpret_cast<float2*>(p.part_o + ((int64_t)split * p.part_stride + t * p.H + h) * p.D + d) =
+                make_float2(x0 * inv, x1 * inv);
+        if (d == 0) {
+            const float lse = L > 0.f ? (mm + log2f(L)) * 0.69314718055994531f : -INFINITY;
+            if (single)
+                p.lse[(int64_t)h * p.lse_s0 + t] = lse;
+            else
+                p.part_lse[(int64_t)split * p.part_stride + t * p.H + h] = lse;
+        }
+    }
+}
+
+}  // namespace pa

@@ -1,14 +1,555 @@
-// Tensor-core (tcgen05) prefill kernel -- not yet enabled: every sequence runs on the
-// split-KV kernel until this path is in place.
+// Tensor-core prefill / chunked-prefill kernel for paged varlen attention (sm_103a).
+//
+// One CTA owns 128 query rows of one (sequence, kv head): the rows are the (query i,
+// head g) pairs of the kv head's GQA group, ordered i * G + g, so each K/V tile feeds
+// all G query heads.  Roles (192 threads):
+//   warp 0      TMA producer: the q tile once, then K and V tiles of 128 keys through
+//               the block table (one box per page piece; the paged layout of
+//               "flash-attn-varlen paged expects k/v tensors of rank 4", What it means)
+//   warp 1      tensor-memory owner and MMA issuer (one elected lane):
+//               S_j = Q K_j^T   (tcgen05.mma, A and B from shared memory, S in TMEM)
+//               O  += P_j V_j   (tcgen05.mma, A = P from TMEM, B = V from shared memory)
+//   warps 2..5  softmax: thread r owns row r (TMEM lane r); reads S_j from TMEM, masks,
+//               keeps the running max and sum, writes P_j (16-bit) back to TMEM, and
+//               rescales O in TMEM only when the running max grew by more than 2^8
+//               (otherwise the stale max stays: exact after the final division).
+// S is double-buffered in TMEM so Q K_{j+1}^T overlaps the softmax of tile j.
+// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+DP), P0, P1 (64 columns each).
+//
+// Mask (bottom-right aligned): query i of a sequence with sq queries and sk keys attends
+// key j iff 0 <= j < sk, j >= i + sk - sq - window_left (window_left >= 0), and
+// j <= i + sk - sq + window_right (window_right >= 0).
 #include <cstdio>
+#include <cstdlib>
+#include <type_traits>
 
-#include "pa_internal.h"
+#include "tc_common.cuh"
 
 namespace pa {
-bool prefill_supported(const Args&) { return false; }
-int prefill_rows_threshold() { return 32; }
-int launch_prefill(const Args&, unsigned int*, char* msg, size_t msg_len) {
-    snprintf(msg, msg_len, "tensor-core prefill kernel not built");
-    return PA_ERR_UNSUPPORTED;
+namespace {
+
+constexpr int kPrefillThreads = 192;
+
+struct PrefillParams {
+    void* out;
+    int64_t o_s0, o_s1;
+    float* lse;
+    int64_t lse_s0;
+    const int32_t* cu_q;
+    const int32_t* cu_k;
+    const int32_t* bt;
+    int64_t bt_s0;
+    int bt_cols;
+    int batch, H, Hkv, G, D, P;
+    int64_t num_blocks, total_q;
+    int paged;
+    int box_rows, boxes_per_tile;
+    int max_sq, max_sk;
+    float scale_log2;
+    int wl, wr;
+    int rows_cap;
+    int q_tiles;
+    unsigned int* err;
+};
+
+template <int DP>
+struct PfCfg {
+    static constexpr int CH = DP / 64;                 // 64-column (128-byte) chunks
+    static constexpr int Q_BYTES = CH * 128 * 128;
+    static constexpr int KV_TILE = CH * 128 * 128;     // 128 keys x DP
+    static constexpr int KS = DP == 64 ? 3 : 2;        // K stages
+    static constexpr int VS = DP == 64 ? 3 : 2;        // V stages
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = Q_BYTES;
+    static constexpr int OFF_V = OFF_K + KS * KV_TILE;
+    static constexpr int OFF_BAR = OFF_V + VS * KV_TILE;
+    // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2], p_full[2], pv_done[2], drain
+    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 7;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM_USED = OFF_MISC + 16 + 1024;
+    // at least 120 KB so that one CTA (and its 512 TMEM columns) owns an SM
+    static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
+    static constexpr uint32_t T_S0 = 0, T_S1 = 128, T_O = 256, T_P0 = 256 + DP, T_P1 = 256 + DP + 64;
+    static_assert(T_P1 + 64 <= 512, "TMEM columns");
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+// Bounded wait that also gives up as soon as another role of the CTA has aborted.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                         unsigned int* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > PA_WAIT_LIMIT_NS) {
+            *abort_flag = 1u;
+            flag_error(err, PA_ERR_DEVICE_TIMEOUT);
+            return false;
+        }
+    }
 }
+
+// Issues the K (or V) boxes of the 128-key tile starting at key `kt` into `dst`.
+__device__ __forceinline__ void issue_kv_tile(const PrefillParams& p, const CUtensorMap* map, uint8_t* dst,
+                                              uint64_t* bar, int b, int hk, int kt, int sk, int kbase, int CH) {
+    int cs[4], cb[4];
+    bool live[4];
+    uint32_t bytes = 0;
+    for (int j = 0; j < p.boxes_per_tile; ++j) {
+        live[j] = false;
+        const int key = kt + j * p.box_rows;
+        if (key >= sk) continue;
+        if (p.paged) {
+            const int page = key / p.P;
+            if (page >= p.bt_cols) {
+                flag_error(p.err, PA_ERR_DEVICE_BOUNDS);
+                continue;
+            }
+            const int blk = __ldg(p.bt + (int64_t)b * p.bt_s0 + page);
+            if (blk < 0 || blk >= p.num_blocks) {
+                flag_error(p.err, PA_ERR_DEVICE_BOUNDS);
+                continue;
+            }
+            cs[j] = key - page * p.P;
+            cb[j] = blk;
+        } else {
+            cs[j] = kbase + key;
+            cb[j] = 0;
+        }
+        live[j] = true;
+        bytes += (uint32_t)(CH * p.box_rows * 128);
+    }
+    mbar_arrive_expect_tx(bar, bytes);
+    for (int j = 0; j < p.boxes_per_tile; ++j) {
+        if (!live[j]) continue;
+        for (int c = 0; c < CH; ++c)
+            tma_load_4d(dst + (c * 128 + j * p.box_rows) * 128, map, bar, c * 64, hk, cs[j], cb[j], 0ull);
+    }
+}
+
+template <typename T, int DP>
+__global__ void __launch_bounds__(kPrefillThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+    using C = PfCfg<DP>;
+    constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.z, hk = blockIdx.y;
+    const int rt = p.q_tiles - 1 - (int)blockIdx.x;  // longest row tiles (causal) start first
+
+    // ---- this CTA's work (uniform over the CTA) ----
+    const int q0 = p.cu_q[b], q1 = p.cu_q[b + 1];
+    const int k0 = p.cu_k[b], k1 = p.cu_k[b + 1];
+    const int sq = q1 - q0, sk = k1 - k0;
+    if (sq < 0 || sk < 0 || sq > p.max_sq || sk > p.max_sk || q0 < 0 || q1 > p.total_q ||
+        (!p.paged && (k0 < 0 || k1 > p.num_blocks))) {
+        if (tid == 0 && blockIdx.x == 0) flag_error(p.err, PA_ERR_DEVICE_BOUNDS);
+        return;
+    }
+    const int64_t rows_total = (int64_t)sq * p.G;
+    if (rows_total <= p.rows_cap) return;  // decode class: owned by the split-KV kernel
+    const int row0 = rt * 128;
+    if (row0 >= rows_total) return;
+    const int qpt = 128 / p.G;
+    const int i0 = row0 / p.G;
+    const int i_last = min(sq - 1, i0 + qpt - 1);
+    const int64_t cdiag = (int64_t)sk - sq;
+    const int64_t lo = p.wl >= 0 ? max64(0, i0 + cdiag - p.wl) : 0;
+    const int64_t hi = p.wr >= 0 ? min64((int64_t)sk - 1, i_last + cdiag + p.wr) : (int64_t)sk - 1;
+    const int kt0 = hi >= lo ? (int)(lo & ~int64_t(127)) : 0;
+    const int n_tiles = hi >= lo ? (int)((hi - kt0) / 128 + 1) : 0;
+
+    T* out = static_cast<T*>(p.out);
+    if (n_tiles == 0) {  // no row of this tile attends any key: out = 0, lse = -inf
+        if (warp >= 2) {
+            const int r = (warp & 3) * 32 + lane;
+            const int64_t rho = row0 + r;
+            if (rho < rows_total) {
+                const int i = (int)(rho / p.G), g = (int)(rho - (int64_t)i * p.G);
+                const int64_t t = q0 + i;
+                const int h = hk * p.G + g;
+                for (int d = 0; d < p.D; d += 8)
+                    *reinterpret_cast<int4*>(out + t * p.o_s0 + (int64_t)h * p.o_s1 + d) = make_int4(0, 0, 0, 0);
+                p.lse[(int64_t)h * p.lse_s0 + t] = -INFINITY;
+            }
+        }
+        return;
+    }
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* q_full = bars;
+    uint64_t* k_full = bars + 1;
+    uint64_t* k_empty = k_full + C::KS;
+    uint64_t* v_full = k_empty + C::KS;
+    uint64_t* v_empty = v_full + C::VS;
+    uint64_t* s_full = v_empty + C::VS;
+    uint64_t* p_full = s_full + 2;
+    uint64_t* pv_done = p_full + 2;
+    uint64_t* drain = pv_done + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    if (tid == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < C::KS; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+        }
+        for (int s = 0; s < C::VS; ++s) {
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&s_full[s], 1);
+            mbar_init(&p_full[s], 4);  // one arrive per softmax warp
+            mbar_init(&pv_done[s], 1);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+            for (int c = 0; c < C::CH; ++c)
+                tma_load_4d(smem + C::OFF_Q + c * 128 * 128, &tm_q, q_full, c * 64, hk * p.G, q0 + i0, 0, 0ull);
+            for (int j = 0; j < n_tiles; ++j) {
+                const int kt = kt0 + j * 128;
+                int s = j % C::KS;
+                if (j >= C::KS && !wait_bar(&k_empty[s], ((j / C::KS) - 1) & 1, abort_flag, p.err)) break;
+                issue_kv_tile(p, &tm_k, smem + C::OFF_K + s * C::KV_TILE, &k_full[s], b, hk, kt, sk, k0, C::CH);
+                s = j % C::VS;
+                if (j >= C::VS && !wait_bar(&v_empty[s], ((j / C::VS) - 1) & 1, abort_flag, p.err)) break;
+                issue_kv_tile(p, &tm_v, smem + C::OFF_V + s * C::KV_TILE, &v_full[s], b, hk, kt, sk, k0, C::CH);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        constexpr uint32_t IDESC_S = tc::idesc_f16(128, 128, kBF16, false, false);
+        constexpr uint32_t IDESC_O = tc::idesc_f16(128, DP, kBF16, false, true);
+        const uint32_t q_addr = smem_addr(smem + C::OFF_Q);
+        bool ok = __all_sync(0xffffffffu, wait_bar(q_full, 0, abort_flag, p.err));
+        for (int j = 0; ok && j <= n_tiles; ++j) {
+            if (j < n_tiles) {
+                const int s = j % C::KS;
+                ok = __all_sync(0xffffffffu, wait_bar(&k_full[s], (j / C::KS) & 1, abort_flag, p.err));
+                if (!ok) break;
+                tc::fence_after_sync();
+                if (lane == 0) {
+                    const uint32_t d = tmem + ((j & 1) ? C::T_S1 : C::T_S0);
+                    const uint32_t k_addr = smem_addr(smem + C::OFF_K + s * C::KV_TILE);
+#pragma unroll
+                    for (int kk = 0; kk < DP / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+                        tc::mma_ss(d, tc::smem_desc_sw128(q_addr + off, 16, 1024),
+                                   tc::smem_desc_sw128(k_addr + off, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+                    }
+                    tc::commit(&s_full[j & 1]);
+                    tc::commit(&k_empty[s]);
+                }
+                __syncwarp();
+            }
+            if (j >= 1) {
+                const int t = j - 1;
+                const int s = t % C::VS;
+                ok = __all_sync(0xffffffffu, wait_bar(&p_full[t & 1], (t >> 1) & 1, abort_flag, p.err));
+                if (!ok) break;
+                ok = __all_sync(0xffffffffu, wait_bar(&v_full[s], (t / C::VS) & 1, abort_flag, p.err));
+                if (!ok) break;
+                uint8_t* vst = smem + C::OFF_V + s * C::KV_TILE;
+                const int valid = min(128, sk - (kt0 + t * 128));
+                if (valid < 128) {  // keys at or past sk: zero V rows so P = 0 never meets NaN
+                    const int zr = 128 - valid;
+                    for (int idx = lane; idx < C::CH * zr * 8; idx += 32) {
+                        const int c = idx / (zr * 8), rem = idx - c * zr * 8;
+                        *reinterpret_cast<int4*>(vst + (c * 128 + valid + (rem >> 3)) * 128 + ((rem & 7) << 4)) =
+                            make_int4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                tc::fence_after_sync();
+                if (lane == 0) {
+                    const uint32_t pt = tmem + ((t & 1) ? C::T_P1 : C::T_P0);
+                    const uint32_t v_addr = smem_addr(vst);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc::mma_ts(tmem + C::T_O, pt + kk * 8, tc::smem_desc_sw128(v_addr + kk * 2048, 128 * 128, 1024),
+                                   IDESC_O, (t > 0 || kk > 0) ? 1u : 0u);
+                    tc::commit(&pv_done[t & 1]);
+                    tc::commit(&v_empty[s]);
+                }
+                __syncwarp();
+            }
+        }
+        // every MMA issued above has completed before tensor memory is released
+        if (lane == 0) {
+            tc::commit(drain);
+            wait_bar(drain, 0, abort_flag, p.err);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- softmax warpgroup ----------------
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;
+        const int64_t rho = row0 + r;
+        const bool row_valid = rho < rows_total;
+        const int i = (int)(rho / p.G), g = (int)(rho - (int64_t)i * p.G);
+        int lo_r = 0, hi_r = -1;
+        if (row_valid) {
+            const int64_t diag = i + cdiag;
+            lo_r = p.wl >= 0 ? (int)max64(0, diag - p.wl) : 0;
+            hi_r = p.wr >= 0 ? (int)max64(-1, min64((int64_t)sk - 1, diag + p.wr)) : sk - 1;
+        }
+        const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int kt = kt0 + j * 128;
+            ok = __all_sync(0xffffffffu, wait_bar(&s_full[j & 1], (j >> 1) & 1, abort_flag, p.err));
+            if (!ok) break;
+            tc::fence_after_sync();
+            float sv[128];
+            const uint32_t s_col = tmem + lane_base + ((j & 1) ? C::T_S1 : C::T_S0);
+            tc::ld_32cols(s_col + 0, *reinterpret_cast<float(*)[32]>(&sv[0]));
+            tc::ld_32cols(s_col + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
+            tc::ld_32cols(s_col + 64, *reinterpret_cast<float(*)[32]>(&sv[64]));
+            tc::ld_32cols(s_col + 96, *reinterpret_cast<float(*)[32]>(&sv[96]));
+            tc::wait_ld();
+            if (!(kt >= lo_r && kt + 127 <= hi_r)) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    const int key = kt + c;
+                    sv[c] = (key >= lo_r && key <= hi_r) ? sv[c] : -INFINITY;
+                }
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 128; ++c) mx = fmaxf(mx, sv[c]);
+            const float m_cand = mx * p.scale_log2;  // softmax_scale > 0 on this path
+            float alpha = 1.f;
+            bool resc = false;
+            if (m_cand > m_run + 8.f) {
+                alpha = fast_exp2(m_run - m_cand);
+                m_run = m_cand;
+                resc = true;
+            }
+            const float m_use = m_run == -INFINITY ? 0.f : m_run;
+            float sum = 0.f;
+            uint32_t pk[64];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const float p0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, -m_use));
+                const float p1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, -m_use));
+                sum += p0 + p1;
+                pk[c] = pack2<T>(p0, p1);
+            }
+            l_run = l_run * alpha + sum;
+            if (j > 0 && __any_sync(0xffffffffu, resc)) {
+                // O was accumulated with the old maximum: rescale it once PV_{j-1} is done
+                ok = __all_sync(0xffffffffu, wait_bar(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.err));
+                if (!ok) break;
+                tc::fence_after_sync();
+#pragma unroll 1
+                for (int cc = 0; cc < DP / 32; ++cc) {
+                    float o[32];
+                    tc::ld_32cols(tmem + lane_base + C::T_O + cc * 32, o);
+                    tc::wait_ld();
+                    uint32_t ob[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) ob[e] = __float_as_uint(o[e] * alpha);
+                    tc::st_32cols(tmem + lane_base + C::T_O + cc * 32, ob);
+                }
+                tc::wait_st();
+            }
+            if (j >= 2) {  // P buffer (j & 1) was read by PV_{j-2}
+                ok = __all_sync(0xffffffffu, wait_bar(&pv_done[j & 1], ((j - 2) >> 1) & 1, abort_flag, p.err));
+                if (!ok) break;
+                tc::fence_after_sync();
+            }
+            const uint32_t p_col = tmem + lane_base + ((j & 1) ? C::T_P1 : C::T_P0);
+            tc::st_32cols(p_col, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+            tc::st_32cols(p_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+            tc::wait_st();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[j & 1]);
+        }
+        if (ok) {
+            const int t_last = n_tiles - 1;
+            ok = __all_sync(0xffffffffu, wait_bar(&pv_done[t_last & 1], (t_last >> 1) & 1, abort_flag, p.err));
+        }
+        if (ok) {
+            tc::fence_after_sync();
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            const int64_t t = q0 + i;
+            const int h = hk * p.G + g;
+            T* orow = out + t * p.o_s0 + (int64_t)h * p.o_s1;
+#pragma unroll 1
+            for (int cc = 0; cc < DP / 32; ++cc) {
+                float o[32];
+                tc::ld_32cols(tmem + lane_base + C::T_O + cc * 32, o);
+                tc::wait_ld();
+                if (row_valid) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        const int d = cc * 32 + e;
+                        if (d < p.D) {
+                            int4 v;
+                            v.x = (int)pack2<T>(o[e] * inv, o[e + 1] * inv);
+                            v.y = (int)pack2<T>(o[e + 2] * inv, o[e + 3] * inv);
+                            v.z = (int)pack2<T>(o[e + 4] * inv, o[e + 5] * inv);
+                            v.w = (int)pack2<T>(o[e + 6] * inv, o[e + 7] * inv);
+                            *reinterpret_cast<int4*>(orow + d) = v;
+                        }
+                    }
+                }
+            }
+            if (row_valid)
+                p.lse[(int64_t)h * p.lse_s0 + t] =
+                    l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+        }
+        tc::fence_before_sync();
+    }
+    __syncwarp();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+template <typename T, int DP>
+int run_prefill(const Args& a, const PrefillParams& pp, cudaStream_t stream, char* msg, size_t msg_len) {
+    using C = PfCfg<DP>;
+    // tensor maps: q as (D, H, total_q, 1), box (64, G, 128 / G, 1); K/V as in the split-KV path
+    CUtensorMap tq, tk, tv;
+    {
+        const uint64_t dims[4] = {(uint64_t)a.D, (uint64_t)a.H, (uint64_t)a.total_q, 1};
+        const uint64_t strides[3] = {(uint64_t)a.q_s1 * 2, (uint64_t)a.q_s0 * 2, (uint64_t)a.q_s0 * 2 * a.total_q};
+        const uint32_t box[4] = {64u, (uint32_t)pp.G, (uint32_t)(128 / pp.G), 1u};
+        int rc = encode_tmap_4d(&tq, a.dtype, a.q, dims, strides, box, 1, msg, msg_len);
+        if (rc != PA_OK) return rc;
+    }
+    {
+        uint64_t dims[4], strides[3];
+        if (a.paged) {
+            dims[0] = (uint64_t)a.D;
+            dims[1] = (uint64_t)a.Hkv;
+            dims[2] = (uint64_t)a.page;
+            dims[3] = (uint64_t)a.num_blocks;
+            strides[0] = (uint64_t)a.kv_s2 * 2;
+            strides[1] = (uint64_t)a.kv_s1 * 2;
+            strides[2] = (uint64_t)a.kv_s0 * 2;
+        } else {
+            dims[0] = (uint64_t)a.D;
+            dims[1] = (uint64_t)a.Hkv;
+            dims[2] = (uint64_t)(a.num_blocks > 0 ? a.num_blocks : 1);
+            dims[3] = 1;
+            strides[0] = (uint64_t)a.kv_s2 * 2;
+            strides[1] = (uint64_t)a.kv_s0 * 2;
+            strides[2] = (uint64_t)a.kv_s0 * 2 * dims[2];
+        }
+        const uint32_t box[4] = {64u, 1u, (uint32_t)pp.box_rows, 1u};
+        int rc = encode_tmap_4d(&tk, a.dtype, a.k, dims, strides, box, 1, msg, msg_len);
+        if (rc != PA_OK) return rc;
+        rc = encode_tmap_4d(&tv, a.dtype, a.v, dims, strides, box, 1, msg, msg_len);
+        if (rc != PA_OK) return rc;
+    }
+    auto kern = prefill_kernel<T, DP>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) {
+            snprintf(msg, msg_len, "cudaFuncSetAttribute(prefill, %d bytes): %s", C::SMEM, cudaGetErrorString(e));
+            return PA_ERR_CUDA;
+        }
+        configured = true;
+    }
+    dim3 grid(pp.q_tiles, a.Hkv, a.batch);
+    kern<<<grid, kPrefillThreads, C::SMEM, stream>>>(tq, tk, tv, pp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        snprintf(msg, msg_len, "prefill launch: %s", cudaGetErrorString(e));
+        return PA_ERR_CUDA;
+    }
+    count_launches(1);
+    return PA_OK;
+}
+
+}  // namespace
+
+int prefill_rows_threshold() { return 32; }
+
+bool prefill_supported(const Args& a) {
+    static const bool disabled = std::getenv("PA_DISABLE_TC_PREFILL") != nullptr;
+    if (disabled) return false;
+    const int G = a.H / a.Hkv;
+    if (a.D > 128 || 128 % G != 0) return false;
+    if (!(a.scale > 0.f)) return false;
+    if ((int64_t)a.max_sq * G <= prefill_rows_threshold()) return false;  // nothing for it to do
+    if (a.total_q <= 0 || a.q_s1 * 2 % 16 != 0 || a.q_s0 * 2 % 16 != 0) return false;
+    return true;
+}
+
+int launch_prefill(const Args& a, unsigned int* err, char* msg, size_t msg_len) {
+    PrefillParams pp{};
+    pp.out = a.out;
+    pp.o_s0 = a.o_s0;
+    pp.o_s1 = a.o_s1;
+    pp.lse = a.lse;
+    pp.lse_s0 = a.lse_s0;
+    pp.cu_q = a.cu_q;
+    pp.cu_k = a.cu_k;
+    pp.bt = a.block_table;
+    pp.bt_s0 = a.bt_s0;
+    pp.bt_cols = a.bt_cols;
+    pp.batch = a.batch;
+    pp.H = a.H;
+    pp.Hkv = a.Hkv;
+    pp.G = a.H / a.Hkv;
+    pp.D = a.D;
+    pp.P = a.paged ? a.page : 1;
+    pp.num_blocks = a.num_blocks;
+    pp.total_q = a.total_q;
+    pp.paged = a.paged ? 1 : 0;
+    if (a.paged) {
+        pp.box_rows = (a.page % 128 == 0) ? 128 : (a.page % 64 == 0) ? 64 : 32;
+    } else {
+        pp.box_rows = 128;
+    }
+    pp.boxes_per_tile = 128 / pp.box_rows;
+    pp.max_sq = a.max_sq;
+    pp.max_sk = a.max_sk;
+    pp.scale_log2 = a.scale * 1.4426950408889634f;
+    pp.wl = a.wl;
+    pp.wr = a.wr;
+    pp.rows_cap = prefill_rows_threshold();
+    pp.q_tiles = (int)(((int64_t)a.max_sq * pp.G + 127) / 128);
+    pp.err = err;
+    const int dp = a.D <= 64 ? 64 : 128;
+    if (a.dtype == PA_BF16) {
+        return dp == 64 ? run_prefill<__nv_bfloat16, 64>(a, pp, a.stream, msg, msg_len)
+                        : run_prefill<__nv_bfloat16, 128>(a, pp, a.stream, msg, msg_len);
+    }
+    return dp == 64 ? run_prefill<__half, 64>(a, pp, a.stream, msg, msg_len)
+                    : run_prefill<__half, 128>(a, pp, a.stream, msg, msg_len);
+}
+
 }  // namespace pa

@@ -5,7 +5,9 @@
 
 #include <cstdio>
 
-#include "splitkv_kernel.cuh"
+#include <cstdlib>
+
+#include "decode_kernel.cuh"
 
 namespace pa {
 
@@ -57,6 +59,57 @@ static int run_splitkv(const CUtensorMap& tk, const CUtensorMap& tv, const Split
         e = cudaGetLastError();
         if (e != cudaSuccess) {
             snprintf(msg, msg_len, "split-KV combine launch: %s", cudaGetErrorString(e));
+            return PA_ERR_CUDA;
+        }
+        count_launches(1);
+    }
+    return PA_OK;
+}
+
+template <int DP>
+struct DecShape;  // pipeline depth of the warp-sliced decode kernel per padded head dim
+template <>
+struct DecShape<64> {
+    static constexpr int STAGES = 4;
+};
+template <>
+struct DecShape<128> {
+    static constexpr int STAGES = 3;
+};
+template <>
+struct DecShape<256> {
+    static constexpr int STAGES = 3;
+};
+
+template <typename T, int DP, int MG>
+static int run_decode(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& sp, const SplitPlan& plan,
+                      cudaStream_t stream, char* msg, size_t msg_len) {
+    constexpr int NT = 64, STAGES = DecShape<DP>::STAGES;
+    using C = DecCfg<DP, MG, NT, STAGES>;
+    auto kern = decode_kernel<T, DP, MG, NT, STAGES>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) {
+            snprintf(msg, msg_len, "cudaFuncSetAttribute(decode, %d bytes): %s", C::SMEM, cudaGetErrorString(e));
+            return PA_ERR_CUDA;
+        }
+        configured = true;
+    }
+    dim3 grid(plan.max_splits, sp.Hkv, sp.batch);
+    kern<<<grid, 160, C::SMEM, stream>>>(tk, tv, sp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        snprintf(msg, msg_len, "decode launch: %s", cudaGetErrorString(e));
+        return PA_ERR_CUDA;
+    }
+    count_launches(1);
+    if (plan.max_splits > 1) {
+        dim3 g2(1, sp.Hkv, sp.batch);
+        combine_kernel<T, C::M, NT><<<g2, 128, 0, stream>>>(sp);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) {
+            snprintf(msg, msg_len, "decode combine launch: %s", cudaGetErrorString(e));
             return PA_ERR_CUDA;
         }
         count_launches(1);
@@ -138,6 +191,17 @@ static int launch_splitkv_t(const Args& a, const SplitPlan& plan, void* workspac
         sp.part_lse = sp.part_o + (size_t)plan.max_splits * sp.part_stride * a.D;
     }
     sp.err = err;
+
+    // decode class (one row tile of at most 32 rows, head dim <= 256): warp-sliced kernel
+    static const bool force_generic = std::getenv("PA_FORCE_GENERIC") != nullptr;
+    if (plan.row_tiles == 1 && plan.dp <= 256 && !force_generic) {
+        if (plan.dp == 64) return plan.mt == 1 ? run_decode<T, 64, 1>(tk, tv, sp, plan, a.stream, msg, msg_len)
+                                               : run_decode<T, 64, 2>(tk, tv, sp, plan, a.stream, msg, msg_len);
+        if (plan.dp == 128) return plan.mt == 1 ? run_decode<T, 128, 1>(tk, tv, sp, plan, a.stream, msg, msg_len)
+                                                : run_decode<T, 128, 2>(tk, tv, sp, plan, a.stream, msg, msg_len);
+        return plan.mt == 1 ? run_decode<T, 256, 1>(tk, tv, sp, plan, a.stream, msg, msg_len)
+                            : run_decode<T, 256, 2>(tk, tv, sp, plan, a.stream, msg, msg_len);
+    }
 
 #define PA_SPLIT_CASE(DPV, MTV)                                                        \
     if (plan.dp == DPV && plan.mt == MTV)                                              \
