@@ -60,6 +60,12 @@ bool same_shape(const pa_tensor* a, const pa_tensor* b) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+int64_t numel(const pa_tensor* t) {
+    int64_t n = 1;
+    for (int i = 0; i < t->ndim && i < 4; ++i) n *= t->shape[i];
+    return n;
+}
+
 bool is_device_memory(const void* p) {
     cudaPointerAttributes attr{};
     cudaError_t e = cudaPointerGetAttributes(&attr, p);
@@ -135,15 +141,16 @@ int validate(const pa_tensor* q, const pa_tensor* k, const pa_tensor* v, const p
         if (bt->ndim != 2) return fail(PA_ERR_ARG, "block_table must be rank 2, got rank %d", bt->ndim);
         if (bt->stride[1] != 1) return fail(PA_ERR_NONCONTIG, "block_table last dimension must be contiguous");
     }
-    if (check_device) {
-        if (paged && !is_device_memory(bt->data)) return fail(PA_ERR_NOT_DEVICE, "block_table must be a cuda tensor");
-        if (!is_device_memory(cu_q->data)) return fail(PA_ERR_NOT_DEVICE, "seqlens_q must be a cuda tensor");
-        if (!is_device_memory(cu_k->data)) return fail(PA_ERR_NOT_DEVICE, "seqlens_k must be a cuda tensor");
-        if (!is_device_memory(q->data)) return fail(PA_ERR_NOT_DEVICE, "q must be a cuda tensor");
-        if (!is_device_memory(k->data)) return fail(PA_ERR_NOT_DEVICE, "k must be a cuda tensor");
-        if (!is_device_memory(v->data)) return fail(PA_ERR_NOT_DEVICE, "v must be a cuda tensor");
-        if (!is_device_memory(out->data)) return fail(PA_ERR_NOT_DEVICE, "out must be a cuda tensor");
-        if (!is_device_memory(lse->data)) return fail(PA_ERR_NOT_DEVICE, "softmax_lse must be a cuda tensor");
+    if (check_device) {  // tensors with no elements are never read or written
+        auto on_device = [](const pa_tensor* t) { return numel(t) == 0 || is_device_memory(t->data); };
+        if (paged && !on_device(bt)) return fail(PA_ERR_NOT_DEVICE, "block_table must be a cuda tensor");
+        if (!on_device(cu_q)) return fail(PA_ERR_NOT_DEVICE, "seqlens_q must be a cuda tensor");
+        if (!on_device(cu_k)) return fail(PA_ERR_NOT_DEVICE, "seqlens_k must be a cuda tensor");
+        if (!on_device(q)) return fail(PA_ERR_NOT_DEVICE, "q must be a cuda tensor");
+        if (!on_device(k)) return fail(PA_ERR_NOT_DEVICE, "k must be a cuda tensor");
+        if (!on_device(v)) return fail(PA_ERR_NOT_DEVICE, "v must be a cuda tensor");
+        if (!on_device(out)) return fail(PA_ERR_NOT_DEVICE, "out must be a cuda tensor");
+        if (!on_device(lse)) return fail(PA_ERR_NOT_DEVICE, "softmax_lse must be a cuda tensor");
     }
 
     // -- this library's own argument checks
@@ -193,6 +200,7 @@ int validate(const pa_tensor* q, const pa_tensor* k, const pa_tensor* v, const p
     if (total_q >= (1ll << 31) || num_blocks >= (1ll << 31) || hq * total_q >= (1ll << 40))
         return fail(PA_ERR_UNSUPPORTED, "sizes beyond 2^31 rows are not supported");
     for (const pa_tensor* t : {q, k, v, out}) {
+        if (numel(t) == 0) continue;
         if (!aligned16(t->data))
             return fail(PA_ERR_UNSUPPORTED, "q/k/v/out base addresses must be 16-byte aligned");
         for (int d = 0; d < t->ndim - 1; ++d)
