@@ -148,6 +148,18 @@ int pa_device_status(void* stream);
 /* Library version, major * 10000 + minor * 100 + patch. */
 int pa_version(void);
 
+/* Upper bound, in nanoseconds of wall time, on every wait inside the kernels (for
+ * pipeline stages that never complete).  Default 2e9; 0 restores the default.  A wait
+ * that runs out makes its CTA leave and pa_device_status() report PA_ERR_DEVICE_TIMEOUT;
+ * the CUDA context stays usable.  Applies to calls made after it. */
+void pa_set_wait_limit_ns(uint64_t ns);
+
+/* Fault injection for tests of the bounded waits: while enabled (non-zero), the kernels'
+ * load producers issue no loads, so every consumer wait runs out after the wait limit
+ * and the call reports PA_ERR_DEVICE_TIMEOUT through pa_device_status().  Outputs of
+ * such calls are undefined.  No GPU fault is involved.  Applies to calls made after it. */
+void pa_set_withhold_loads(int enable);
+
 /* Number of kernels this library has launched in this process (all threads, all
  * devices), for profiling: a caller reads it before and after a region. */
 uint64_t pa_kernel_launches(void);

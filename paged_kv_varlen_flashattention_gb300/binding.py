@@ -70,6 +70,10 @@ def load():
         lib.pa_device_status.argtypes = [ctypes.c_void_p]
         lib.pa_version.restype = ctypes.c_int
         lib.pa_kernel_launches.restype = ctypes.c_uint64
+        lib.pa_set_wait_limit_ns.restype = None
+        lib.pa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        lib.pa_set_withhold_loads.restype = None
+        lib.pa_set_withhold_loads.argtypes = [ctypes.c_int]
         _lib = lib
     return _lib
 
@@ -100,6 +104,16 @@ def _ref(d):
 def kernel_launches() -> int:
     """Kernels the library has launched in this process so far."""
     return int(load().pa_kernel_launches())
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Bound, in ns of wall time, on every in-kernel wait (0 restores the 2 s default)."""
+    load().pa_set_wait_limit_ns(int(ns))
+
+
+def set_withhold_loads(enable: bool) -> None:
+    """Test hook: while enabled the kernels issue no loads and their waits run out."""
+    load().pa_set_withhold_loads(1 if enable else 0)
 
 
 def last_error() -> str:

@@ -325,6 +325,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 namespace pa {
 
 static std::atomic<uint64_t> g_launches{0};
+static std::atomic<uint64_t> g_wait_ns{PA_WAIT_LIMIT_NS};
+static std::atomic<int> g_withhold{0};
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
 int encode_tmap_4d(void* map, int dtype, const void* base, const uint64_t dims_[4], const uint64_t strides_bytes[3],
@@ -423,6 +425,8 @@ int pa_varlen_fwd(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor*
                       out, softmax_lse, true, &a);
     if (rc != PA_OK) return rc;
     a.stream = static_cast<cudaStream_t>(stream);
+    a.wait_ns = pa::g_wait_ns.load(std::memory_order_relaxed);
+    a.withhold_loads = pa::g_withhold.load(std::memory_order_relaxed);
     if (a.total_q == 0 || a.batch == 0) return PA_OK;
 
     unsigned int* err = nullptr;
@@ -471,6 +475,10 @@ int pa_device_status(void* stream) {
 }
 
 int pa_version(void) { return 100; }
+
+void pa_set_wait_limit_ns(uint64_t ns) { pa::g_wait_ns.store(ns ? ns : PA_WAIT_LIMIT_NS); }
+
+void pa_set_withhold_loads(int enable) { pa::g_withhold.store(enable ? 1 : 0); }
 
 uint64_t pa_kernel_launches(void) { return pa::g_launches.load(std::memory_order_relaxed); }
 

@@ -29,7 +29,9 @@ struct DecCfg {
     static constexpr int OFF_ML = OFF_ROW + 2 * M * 4;         // m[4][16], l[4][16] of the merge
     static constexpr int OFF_BAR = (OFF_ML + 2 * 4 * 16 * 4 + 15) & ~15;
     static constexpr int OFF_FLAG = OFF_BAR + 2 * STAGES * 8;
-    static constexpr int SMEM = OFF_FLAG + 16 + 1024;
+    static constexpr int OFF_IDS = OFF_FLAG + 16;              // block id of every TMA box of the split
+    static constexpr int MAX_BOXES = 512;
+    static constexpr int SMEM = OFF_IDS + MAX_BOXES * 4 + 1024;
     static constexpr int MERGE_BYTES = 4 * 16 * DP * 4;        // O of every warp, reuses the stages
     static constexpr bool Q_IN_REGS = DP <= 128;
     static_assert(KPW % 16 == 0, "keys per warp");
@@ -38,13 +40,13 @@ struct DecCfg {
 };
 
 __device__ __forceinline__ bool dec_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                         unsigned int* err) {
+                                         unsigned int* err, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (global_timer_ns() - t0 > PA_WAIT_LIMIT_NS) {
+        if (global_timer_ns() - t0 > limit_ns) {
             *abort_flag = 1u;
             flag_error(err, PA_ERR_DEVICE_TIMEOUT);
             return false;
@@ -121,50 +123,47 @@ __global__ void __launch_bounds__(160) decode_kernel(const __grid_constant__ CUt
 
     if (warp == 4) {
         // ---------------- producer ----------------
-        if (lane == 0) {
+        // physical block of every box of this split's key range, looked up once
+        int* ids = reinterpret_cast<int*>(smem + C::OFF_IDS);
+        const int kbeg = tv.kt0 + t_begin * NT;
+        const int n_boxes = min(n_iter * p.boxes_per_tile, C::MAX_BOXES);
+        const int32_t* bt_row = p.paged ? p.bt + (int64_t)b * p.bt_s0 : nullptr;
+        for (int bi = lane; bi < n_boxes; bi += 32) {
+            const int key = kbeg + bi * p.box_rows;
+            ids[bi] = p.paged ? box_block(bt_row, p.bt_cols, p.num_blocks, p.P, key, tv.sk, p.err)
+                              : (key < tv.sk ? 0 : -1);
+        }
+        __syncwarp();
+        if (lane == 0 && !p.withhold) {
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
             const uint64_t policy = l2_policy_evict_first();
             for (int it = 0; it < n_iter; ++it) {
                 const int stage = it % STAGES;
-                if (it >= STAGES && !dec_wait(&empty[stage], ((it / STAGES) - 1) & 1, abort_flag, p.err)) break;
-                const int kt = tv.kt0 + (t_begin + it) * NT;
+                if (it >= STAGES && !dec_wait(&empty[stage], ((it / STAGES) - 1) & 1, abort_flag, p.err, p.wait_ns)) break;
+                const int kt = kbeg + it * NT;
                 uint8_t* kst = smem + stage * C::STAGE_BYTES;
                 uint8_t* vst = kst + C::TILE_BYTES;
-                int cs[4], cb[4];
-                bool live[4];
+                int blk[4];
                 uint32_t bytes = 0;
                 for (int j = 0; j < p.boxes_per_tile; ++j) {
-                    live[j] = false;
+                    const int bi = it * p.boxes_per_tile + j;
                     const int key = kt + j * p.box_rows;
-                    if (key >= tv.sk) continue;
-                    if (p.paged) {
-                        const int page = key / p.P;
-                        if (page >= p.bt_cols) {
-                            flag_error(p.err, PA_ERR_DEVICE_BOUNDS);
-                            continue;
-                        }
-                        const int blk = __ldg(p.bt + (int64_t)b * p.bt_s0 + page);
-                        if (blk < 0 || blk >= p.num_blocks) {
-                            flag_error(p.err, PA_ERR_DEVICE_BOUNDS);
-                            continue;
-                        }
-                        cs[j] = key - page * p.P;
-                        cb[j] = blk;
-                    } else {
-                        cs[j] = p.cu_k[b] + key;
-                        cb[j] = 0;
-                    }
-                    live[j] = true;
-                    bytes += 2u * C::CH * p.box_rows * 128u;
+                    blk[j] = bi < C::MAX_BOXES ? ids[bi]
+                             : (p.paged ? box_block(bt_row, p.bt_cols, p.num_blocks, p.P, key, tv.sk, p.err)
+                                        : (key < tv.sk ? 0 : -1));
+                    if (blk[j] >= 0) bytes += 2u * C::CH * p.box_rows * 128u;
                 }
                 mbar_arrive_expect_tx(&full[stage], bytes);
                 for (int j = 0; j < p.boxes_per_tile; ++j) {
-                    if (!live[j]) continue;
+                    if (blk[j] < 0) continue;
+                    const int key = kt + j * p.box_rows;
+                    const int c2 = p.paged ? key - (key / p.P) * p.P : p.cu_k[b] + key;
+                    const int c3 = p.paged ? blk[j] : 0;
                     for (int c = 0; c < C::CH; ++c) {
                         const int off = (c * NT + j * p.box_rows) * 128;
-                        tma_load_4d(kst + off, &tm_k, &full[stage], c * 64, hk, cs[j], cb[j], policy);
-                        tma_load_4d(vst + off, &tm_v, &full[stage], c * 64, hk, cs[j], cb[j], policy);
+                        tma_load_4d(kst + off, &tm_k, &full[stage], c * 64, hk, c2, c3, policy);
+                        tma_load_4d(vst + off, &tm_v, &full[stage], c * 64, hk, c2, c3, policy);
                     }
                 }
             }
@@ -200,7 +199,7 @@ __global__ void __launch_bounds__(160) decode_kernel(const __grid_constant__ CUt
 
     for (int it = 0; it < n_iter; ++it) {
         const int stage = it % STAGES;
-        ok = __all_sync(0xffffffffu, dec_wait(&full[stage], (it / STAGES) & 1, abort_flag, p.err));
+        ok = __all_sync(0xffffffffu, dec_wait(&full[stage], (it / STAGES) & 1, abort_flag, p.err, p.wait_ns));
         if (!ok) break;
         const int kt = tv.kt0 + (t_begin + it) * NT;
         uint8_t* kst = smem + stage * C::STAGE_BYTES;

@@ -65,15 +65,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete.  Gives up after
-// PA_WAIT_LIMIT_NS of wall time and returns false (the caller flags a timeout and
-// leaves the kernel instead of hanging the GPU).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Waits for the phase with the given parity to complete.  Gives up after `limit_ns`
+// of wall time and returns false (the caller flags a timeout and leaves the kernel
+// instead of hanging the GPU).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (global_timer_ns() - t0 > PA_WAIT_LIMIT_NS) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
     }
 }
 
@@ -163,6 +163,25 @@ __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Physical block of the TMA box that starts at logical key `key` of a sequence, looked
+// up in that sequence's block-table row: -1 for a box past the sequence's sk keys (not
+// loaded), -2 for metadata out of range (flagged in the error word, not loaded).
+__device__ __forceinline__ int box_block(const int32_t* bt_row, int bt_cols, int64_t num_blocks, int page_size,
+                                         int key, int sk, unsigned int* err) {
+    if (key >= sk) return -1;
+    const int page = key / page_size;
+    if (page >= bt_cols) {
+        flag_error(err, PA_ERR_DEVICE_BOUNDS);
+        return -2;
+    }
+    const int blk = __ldg(bt_row + page);
+    if (blk < 0 || blk >= num_blocks) {
+        flag_error(err, PA_ERR_DEVICE_BOUNDS);
+        return -2;
+    }
+    return blk;
 }
 
 // Byte offset of 16-byte unit `u` (0..7) of row `r` in a tile whose rows are 128 bytes

@@ -41,6 +41,8 @@ struct Args {
     int64_t lse_s0;
     int64_t total_q;
     cudaStream_t stream;
+    uint64_t wait_ns;    // bound on every in-kernel wait
+    int withhold_loads;  // test hook: producers issue no loads
 };
 
 // Scratch the split-KV path needs for a call (bytes), and where to put it.

@@ -50,6 +50,8 @@ struct PrefillParams {
     int rows_cap;
     int q_tiles;
     unsigned int* err;
+    uint64_t wait_ns;  // bound on every wait
+    int withhold;      // test hook: issue no loads
 };
 
 template <int DP>
@@ -66,7 +68,9 @@ struct PfCfg {
     // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2], p_full[2], pv_done[2], drain
     static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 7;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr int SMEM_USED = OFF_MISC + 16 + 1024;
+    static constexpr int OFF_IDS = OFF_MISC + 16;         // block id of every TMA box of the CTA
+    static constexpr int MAX_BOXES = 1024;
+    static constexpr int SMEM_USED = OFF_IDS + MAX_BOXES * 4 + 1024;
     // at least 120 KB so that one CTA (and its 512 TMEM columns) owns an SM
     static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
     static constexpr uint32_t T_S0 = 0, T_S1 = 128, T_O = 256, T_P0 = 256 + DP, T_P1 = 256 + DP + 64;
@@ -76,13 +80,13 @@ struct PfCfg {
 
 // Bounded wait that also gives up as soon as another role of the CTA has aborted.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                         unsigned int* err) {
+                                         unsigned int* err, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (global_timer_ns() - t0 > PA_WAIT_LIMIT_NS) {
+        if (global_timer_ns() - t0 > limit_ns) {
             *abort_flag = 1u;
             flag_error(err, PA_ERR_DEVICE_TIMEOUT);
             return false;
@@ -90,41 +94,25 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
     }
 }
 
-// Issues the K (or V) boxes of the 128-key tile starting at key `kt` into `dst`.
+// Issues the K (or V) boxes of the CTA's 128-key tile number `j` (first key kt0 + 128 j)
+// into `dst`.  ids[j * boxes_per_tile + jj] holds the physical block of box jj, or a
+// negative value for a box that is not loaded.
 __device__ __forceinline__ void issue_kv_tile(const PrefillParams& p, const CUtensorMap* map, uint8_t* dst,
-                                              uint64_t* bar, int b, int hk, int kt, int sk, int kbase, int CH) {
-    int cs[4], cb[4];
-    bool live[4];
+                                              uint64_t* bar, const int* ids, int j, int hk, int kt0, int k0,
+                                              int CH) {
+    const int kt = kt0 + j * 128;
     uint32_t bytes = 0;
-    for (int j = 0; j < p.boxes_per_tile; ++j) {
-        live[j] = false;
-        const int key = kt + j * p.box_rows;
-        if (key >= sk) continue;
-        if (p.paged) {
-            const int page = key / p.P;
-            if (page >= p.bt_cols) {
-                flag_error(p.err, PA_ERR_DEVICE_BOUNDS);
-                continue;
-            }
-            const int blk = __ldg(p.bt + (int64_t)b * p.bt_s0 + page);
-            if (blk < 0 || blk >= p.num_blocks) {
-                flag_error(p.err, PA_ERR_DEVICE_BOUNDS);
-                continue;
-            }
-            cs[j] = key - page * p.P;
-            cb[j] = blk;
-        } else {
-            cs[j] = kbase + key;
-            cb[j] = 0;
-        }
-        live[j] = true;
-        bytes += (uint32_t)(CH * p.box_rows * 128);
-    }
+    for (int jj = 0; jj < p.boxes_per_tile; ++jj)
+        if (ids[j * p.boxes_per_tile + jj] >= 0) bytes += (uint32_t)(CH * p.box_rows * 128);
     mbar_arrive_expect_tx(bar, bytes);
-    for (int j = 0; j < p.boxes_per_tile; ++j) {
-        if (!live[j]) continue;
+    for (int jj = 0; jj < p.boxes_per_tile; ++jj) {
+        const int blk = ids[j * p.boxes_per_tile + jj];
+        if (blk < 0) continue;
+        const int key = kt + jj * p.box_rows;
+        const int c2 = p.paged ? key - (key / p.P) * p.P : k0 + key;
+        const int c3 = p.paged ? blk : 0;
         for (int c = 0; c < CH; ++c)
-            tma_load_4d(dst + (c * 128 + j * p.box_rows) * 128, map, bar, c * 64, hk, cs[j], cb[j], 0ull);
+            tma_load_4d(dst + (c * 128 + jj * p.box_rows) * 128, map, bar, c * 64, hk, c2, c3, 0ull);
     }
 }
 
@@ -222,21 +210,43 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
-        if (lane == 0) {
+        // physical block of every box of this CTA's key range, looked up once
+        int* ids = reinterpret_cast<int*>(smem + C::OFF_IDS);
+        const int n_boxes = min(n_tiles * p.boxes_per_tile, C::MAX_BOXES);
+        const int32_t* bt_row = p.paged ? p.bt + (int64_t)b * p.bt_s0 : nullptr;
+        for (int bi = lane; bi < n_boxes; bi += 32) {
+            const int key = kt0 + bi * p.box_rows;
+            ids[bi] = p.paged ? box_block(bt_row, p.bt_cols, p.num_blocks, p.P, key, sk, p.err) : (key < sk ? 0 : -1);
+        }
+        __syncwarp();
+        if (lane == 0 && !p.withhold) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
             mbar_arrive_expect_tx(q_full, C::Q_BYTES);
             for (int c = 0; c < C::CH; ++c)
                 tma_load_4d(smem + C::OFF_Q + c * 128 * 128, &tm_q, q_full, c * 64, hk * p.G, q0 + i0, 0, 0ull);
+            int spill[4];  // block ids of one tile when the range exceeds the staged table
             for (int j = 0; j < n_tiles; ++j) {
-                const int kt = kt0 + j * 128;
+                const int* tile_ids = ids;
+                int jt = j;
+                if ((j + 1) * p.boxes_per_tile > C::MAX_BOXES) {
+                    for (int jj = 0; jj < p.boxes_per_tile; ++jj) {
+                        const int key = kt0 + j * 128 + jj * p.box_rows;
+                        spill[jj] = p.paged ? box_block(bt_row, p.bt_cols, p.num_blocks, p.P, key, sk, p.err)
+                                            : (key < sk ? 0 : -1);
+                    }
+                    tile_ids = spill;
+                    jt = 0;
+                }
                 int s = j % C::KS;
-                if (j >= C::KS && !wait_bar(&k_empty[s], ((j / C::KS) - 1) & 1, abort_flag, p.err)) break;
-                issue_kv_tile(p, &tm_k, smem + C::OFF_K + s * C::KV_TILE, &k_full[s], b, hk, kt, sk, k0, C::CH);
+                if (j >= C::KS && !wait_bar(&k_empty[s], ((j / C::KS) - 1) & 1, abort_flag, p.err, p.wait_ns)) break;
+                issue_kv_tile(p, &tm_k, smem + C::OFF_K + s * C::KV_TILE, &k_full[s], tile_ids, jt, hk,
+                              kt0 + (j - jt) * 128, k0, C::CH);
                 s = j % C::VS;
-                if (j >= C::VS && !wait_bar(&v_empty[s], ((j / C::VS) - 1) & 1, abort_flag, p.err)) break;
-                issue_kv_tile(p, &tm_v, smem + C::OFF_V + s * C::KV_TILE, &v_full[s], b, hk, kt, sk, k0, C::CH);
+                if (j >= C::VS && !wait_bar(&v_empty[s], ((j / C::VS) - 1) & 1, abort_flag, p.err, p.wait_ns)) break;
+                issue_kv_tile(p, &tm_v, smem + C::OFF_V + s * C::KV_TILE, &v_full[s], tile_ids, jt, hk,
+                              kt0 + (j - jt) * 128, k0, C::CH);
             }
         }
     } else if (warp == 1) {
@@ -244,11 +254,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         constexpr uint32_t IDESC_S = tc::idesc_f16(128, 128, kBF16, false, false);
         constexpr uint32_t IDESC_O = tc::idesc_f16(128, DP, kBF16, false, true);
         const uint32_t q_addr = smem_addr(smem + C::OFF_Q);
-        bool ok = __all_sync(0xffffffffu, wait_bar(q_full, 0, abort_flag, p.err));
+        bool ok = __all_sync(0xffffffffu, wait_bar(q_full, 0, abort_flag, p.err, p.wait_ns));
         for (int j = 0; ok && j <= n_tiles; ++j) {
             if (j < n_tiles) {
                 const int s = j % C::KS;
-                ok = __all_sync(0xffffffffu, wait_bar(&k_full[s], (j / C::KS) & 1, abort_flag, p.err));
+                ok = __all_sync(0xffffffffu, wait_bar(&k_full[s], (j / C::KS) & 1, abort_flag, p.err, p.wait_ns));
                 if (!ok) break;
                 tc::fence_after_sync();
                 if (lane == 0) {
@@ -268,9 +278,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             if (j >= 1) {
                 const int t = j - 1;
                 const int s = t % C::VS;
-                ok = __all_sync(0xffffffffu, wait_bar(&p_full[t & 1], (t >> 1) & 1, abort_flag, p.err));
+                ok = __all_sync(0xffffffffu, wait_bar(&p_full[t & 1], (t >> 1) & 1, abort_flag, p.err, p.wait_ns));
                 if (!ok) break;
-                ok = __all_sync(0xffffffffu, wait_bar(&v_full[s], (t / C::VS) & 1, abort_flag, p.err));
+                ok = __all_sync(0xffffffffu, wait_bar(&v_full[s], (t / C::VS) & 1, abort_flag, p.err, p.wait_ns));
                 if (!ok) break;
                 uint8_t* vst = smem + C::OFF_V + s * C::KV_TILE;
                 const int valid = min(128, sk - (kt0 + t * 128));
@@ -301,7 +311,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         // every MMA issued above has completed before tensor memory is released
         if (lane == 0) {
             tc::commit(drain);
-            wait_bar(drain, 0, abort_flag, p.err);
+            mbar_wait(drain, 0, p.wait_ns);  // not cut short by an abort: MMAs may be in flight
         }
         __syncwarp();
     } else {
@@ -322,7 +332,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
             const int kt = kt0 + j * 128;
-            ok = __all_sync(0xffffffffu, wait_bar(&s_full[j & 1], (j >> 1) & 1, abort_flag, p.err));
+            ok = __all_sync(0xffffffffu, wait_bar(&s_full[j & 1], (j >> 1) & 1, abort_flag, p.err, p.wait_ns));
             if (!ok) break;
             tc::fence_after_sync();
             float sv[128];
@@ -363,7 +373,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             l_run = l_run * alpha + sum;
             if (j > 0 && __any_sync(0xffffffffu, resc)) {
                 // O was accumulated with the old maximum: rescale it once PV_{j-1} is done
-                ok = __all_sync(0xffffffffu, wait_bar(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.err));
+                ok = __all_sync(0xffffffffu, wait_bar(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.err, p.wait_ns));
                 if (!ok) break;
                 tc::fence_after_sync();
 #pragma unroll 1
@@ -379,7 +389,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 tc::wait_st();
             }
             if (j >= 2) {  // P buffer (j & 1) was read by PV_{j-2}
-                ok = __all_sync(0xffffffffu, wait_bar(&pv_done[j & 1], ((j - 2) >> 1) & 1, abort_flag, p.err));
+                ok = __all_sync(0xffffffffu, wait_bar(&pv_done[j & 1], ((j - 2) >> 1) & 1, abort_flag, p.err, p.wait_ns));
                 if (!ok) break;
                 tc::fence_after_sync();
             }
@@ -393,7 +403,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
         if (ok) {
             const int t_last = n_tiles - 1;
-            ok = __all_sync(0xffffffffu, wait_bar(&pv_done[t_last & 1], (t_last >> 1) & 1, abort_flag, p.err));
+            ok = __all_sync(0xffffffffu, wait_bar(&pv_done[t_last & 1], (t_last >> 1) & 1, abort_flag, p.err, p.wait_ns));
         }
         if (ok) {
             tc::fence_after_sync();
@@ -543,6 +553,8 @@ int launch_prefill(const Args& a, unsigned int* err, char* msg, size_t msg_len) 
     pp.rows_cap = prefill_rows_threshold();
     pp.q_tiles = (int)(((int64_t)a.max_sq * pp.G + 127) / 128);
     pp.err = err;
+    pp.wait_ns = a.wait_ns;
+    pp.withhold = a.withhold_loads;
     const int dp = a.D <= 64 ? 64 : 128;
     if (a.dtype == PA_BF16) {
         return dp == 64 ? run_prefill<__nv_bfloat16, 64>(a, pp, a.stream, msg, msg_len)

@@ -46,6 +46,8 @@ struct SplitParams {
     float* part_lse;
     int64_t part_stride;  // rows per split slab (total_q * H)
     unsigned int* err;
+    uint64_t wait_ns;    // bound on every wait
+    int withhold;        // test hook: issue no loads
 };
 
 // The work of one (sequence, kv head, row tile), computed identically by the split
@@ -231,7 +233,7 @@ __global__ void __launch_bounds__(128) splitkv_kernel(const __grid_constant__ CU
             }
         }
     };
-    if (tid == 0) {
+    if (tid == 0 && !p.withhold) {
         for (int it = 0; it < min(STAGES - 1, n_iter); ++it) issue(it);
     }
 
@@ -258,7 +260,7 @@ __global__ void __launch_bounds__(128) splitkv_kernel(const __grid_constant__ CU
         const int kt = tv.kt0 + (t_begin + it) * NT;
         uint8_t* kst = smem + stage * C::STAGE_BYTES;
         uint8_t* vst = kst + C::TILE_BYTES;
-        const bool ok = mbar_wait(&full[stage], (it / STAGES) & 1);
+        const bool ok = mbar_wait(&full[stage], (it / STAGES) & 1, p.wait_ns);
 
         // V rows at or past sk (tail of the last page, or pages not loaded) -> 0, so that
         // P = 0 never meets NaN or stale values in P.V.
@@ -323,7 +325,7 @@ __global__ void __launch_bounds__(128) splitkv_kernel(const __grid_constant__ CU
             return;
         }
         // the stage used by the previous iteration is free: refill it
-        if (tid == 0 && it + STAGES - 1 < n_iter) {
+        if (tid == 0 && it + STAGES - 1 < n_iter && !p.withhold) {
             fence_proxy_async_smem();
             issue(it + STAGES - 1);
         }

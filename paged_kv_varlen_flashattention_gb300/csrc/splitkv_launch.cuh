@@ -191,6 +191,8 @@ static int launch_splitkv_t(const Args& a, const SplitPlan& plan, void* workspac
         sp.part_lse = sp.part_o + (size_t)plan.max_splits * sp.part_stride * a.D;
     }
     sp.err = err;
+    sp.wait_ns = a.wait_ns;
+    sp.withhold = a.withhold_loads;
 
     // decode class (one row tile of at most 32 rows, head dim <= 256): warp-sliced kernel
     static const bool force_generic = std::getenv("PA_FORCE_GENERIC") != nullptr;
