@@ -144,18 +144,21 @@ __global__ void __launch_bounds__(160) decode_kernel(const __grid_constant__ CUt
                 const int kt = kbeg + it * NT;
                 uint8_t* kst = smem + stage * C::STAGE_BYTES;
                 uint8_t* vst = kst + C::TILE_BYTES;
-                int blk[4];
+                int blk[2];  // a 64-key tile is at most two 32-row boxes
                 uint32_t bytes = 0;
-                for (int j = 0; j < p.boxes_per_tile; ++j) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
                     const int bi = it * p.boxes_per_tile + j;
                     const int key = kt + j * p.box_rows;
-                    blk[j] = bi < C::MAX_BOXES ? ids[bi]
+                    blk[j] = j >= p.boxes_per_tile ? -1
+                             : bi < C::MAX_BOXES ? ids[bi]
                              : (p.paged ? box_block(bt_row, p.bt_cols, p.num_blocks, p.P, key, tv.sk, p.err)
                                         : (key < tv.sk ? 0 : -1));
                     if (blk[j] >= 0) bytes += 2u * C::CH * p.box_rows * 128u;
                 }
                 mbar_arrive_expect_tx(&full[stage], bytes);
-                for (int j = 0; j < p.boxes_per_tile; ++j) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
                     if (blk[j] < 0) continue;
                     const int key = kt + j * p.box_rows;
                     const int c2 = p.paged ? key - (key / p.P) * p.P : p.cu_k[b] + key;

@@ -19,6 +19,7 @@
 // Mask (bottom-right aligned): query i of a sequence with sq queries and sk keys attends
 // key j iff 0 <= j < sk, j >= i + sk - sq - window_left (window_left >= 0), and
 // j <= i + sk - sq + window_right (window_right >= 0).
+#include <algorithm>
 #include <cstdio>
 #include <cstdlib>
 #include <type_traits>
@@ -48,7 +49,7 @@ struct PrefillParams {
     float scale_log2;
     int wl, wr;
     int rows_cap;
-    int q_tiles;
+    int q_tiles;  // grid.x: an upper bound of the number of 128-row tiles
     unsigned int* err;
     uint64_t wait_ns;  // bound on every wait
     int withhold;      // test hook: issue no loads
@@ -59,8 +60,8 @@ struct PfCfg {
     static constexpr int CH = DP / 64;                 // 64-column (128-byte) chunks
     static constexpr int Q_BYTES = CH * 128 * 128;
     static constexpr int KV_TILE = CH * 128 * 128;     // 128 keys x DP
-    static constexpr int KS = DP == 64 ? 3 : 2;        // K stages
-    static constexpr int VS = DP == 64 ? 3 : 2;        // V stages
+    static constexpr int KS = DP == 64 ? 4 : 3;        // K stages
+    static constexpr int VS = DP == 64 ? 4 : 3;        // V stages
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = Q_BYTES;
     static constexpr int OFF_V = OFF_K + KS * KV_TILE;
@@ -69,8 +70,8 @@ struct PfCfg {
     static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 7;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int OFF_IDS = OFF_MISC + 16;         // block id of every TMA box of the CTA
-    static constexpr int MAX_BOXES = 1024;
-    static constexpr int SMEM_USED = OFF_IDS + MAX_BOXES * 4 + 1024;
+    static constexpr int MAX_BOXES = 256;
+    static constexpr int SMEM_USED = OFF_IDS + (MAX_BOXES + 4) * 4 + 1024;
     // at least 120 KB so that one CTA (and its 512 TMEM columns) owns an SM
     static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
     static constexpr uint32_t T_S0 = 0, T_S1 = 128, T_O = 256, T_P0 = 256 + DP, T_P1 = 256 + DP + 64;
@@ -101,16 +102,20 @@ __device__ __forceinline__ void issue_kv_tile(const PrefillParams& p, const CUte
                                               uint64_t* bar, const int* ids, int j, int hk, int kt0, int k0,
                                               int CH) {
     const int kt = kt0 + j * 128;
+    int blk[4];
     uint32_t bytes = 0;
-    for (int jj = 0; jj < p.boxes_per_tile; ++jj)
-        if (ids[j * p.boxes_per_tile + jj] >= 0) bytes += (uint32_t)(CH * p.box_rows * 128);
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+        blk[jj] = jj < p.boxes_per_tile ? ids[j * p.boxes_per_tile + jj] : -1;
+        if (blk[jj] >= 0) bytes += (uint32_t)(CH * p.box_rows * 128);
+    }
     mbar_arrive_expect_tx(bar, bytes);
-    for (int jj = 0; jj < p.boxes_per_tile; ++jj) {
-        const int blk = ids[j * p.boxes_per_tile + jj];
-        if (blk < 0) continue;
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+        if (blk[jj] < 0) continue;
         const int key = kt + jj * p.box_rows;
         const int c2 = p.paged ? key - (key / p.P) * p.P : k0 + key;
-        const int c3 = p.paged ? blk : 0;
+        const int c3 = p.paged ? blk[jj] : 0;
         for (int c = 0; c < CH; ++c)
             tma_load_4d(dst + (c * 128 + jj * p.box_rows) * 128, map, bar, c * 64, hk, c2, c3, 0ull);
     }
@@ -125,8 +130,47 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int b = blockIdx.z, hk = blockIdx.y;
-    const int rt = p.q_tiles - 1 - (int)blockIdx.x;  // longest row tiles (causal) start first
+    const int hk = blockIdx.y;
+
+    // ---- which (sequence, row tile) this CTA owns: the blockIdx.x-th tile of the list of
+    // all 128-row tiles of prefill-class sequences, sequence by sequence, each sequence's
+    // last (longest, under a causal mask) tile first.  Warp 0 scans cu_seqlens_q 32
+    // sequences at a time with a prefix sum of tile counts.
+    int* pick = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
+    if (warp == 0) {
+        int remaining = (int)blockIdx.x, found_b = -1, found_rt = 0;
+        for (int base = 0; base < p.batch && found_b < 0; base += 32) {
+            const int bb = base + lane;
+            int tiles = 0;
+            if (bb < p.batch) {
+                const int64_t rows = (int64_t)(p.cu_q[bb + 1] - p.cu_q[bb]) * p.G;
+                tiles = rows > p.rows_cap ? (int)((rows + 127) / 128) : 0;
+            }
+            int incl = tiles;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += v;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, remaining < incl);
+            if (hit) {
+                const int src = __ffs(hit) - 1;
+                const int excl = __shfl_sync(0xffffffffu, incl - tiles, src);
+                const int cnt = __shfl_sync(0xffffffffu, tiles, src);
+                found_b = base + src;
+                found_rt = cnt - 1 - (remaining - excl);
+            } else {
+                remaining -= __shfl_sync(0xffffffffu, incl, 31);
+            }
+        }
+        if (lane == 0) {
+            pick[0] = found_b;
+            pick[1] = found_rt;
+        }
+    }
+    __syncthreads();
+    const int b = pick[0], rt = pick[1];
+    if (b < 0) return;  // past the last tile
 
     // ---- this CTA's work (uniform over the CTA) ----
     const int q0 = p.cu_q[b], q1 = p.cu_q[b + 1];
@@ -134,7 +178,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const int sq = q1 - q0, sk = k1 - k0;
     if (sq < 0 || sk < 0 || sq > p.max_sq || sk > p.max_sk || q0 < 0 || q1 > p.total_q ||
         (!p.paged && (k0 < 0 || k1 > p.num_blocks))) {
-        if (tid == 0 && blockIdx.x == 0) flag_error(p.err, PA_ERR_DEVICE_BOUNDS);
+        if (tid == 0) flag_error(p.err, PA_ERR_DEVICE_BOUNDS);
         return;
     }
     const int64_t rows_total = (int64_t)sq * p.G;
@@ -226,7 +270,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             mbar_arrive_expect_tx(q_full, C::Q_BYTES);
             for (int c = 0; c < C::CH; ++c)
                 tma_load_4d(smem + C::OFF_Q + c * 128 * 128, &tm_q, q_full, c * 64, hk * p.G, q0 + i0, 0, 0ull);
-            int spill[4];  // block ids of one tile when the range exceeds the staged table
+            int* spill = ids + C::MAX_BOXES;  // block ids of one tile past the staged range
             for (int j = 0; j < n_tiles; ++j) {
                 const int* tile_ids = ids;
                 int jt = j;
@@ -349,9 +393,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     sv[c] = (key >= lo_r && key <= hi_r) ? sv[c] : -INFINITY;
                 }
             }
-            float mx = -INFINITY;
+            float mxs[8];
 #pragma unroll
-            for (int c = 0; c < 128; ++c) mx = fmaxf(mx, sv[c]);
+            for (int u = 0; u < 8; ++u) mxs[u] = sv[u];
+#pragma unroll
+            for (int c = 8; c < 128; ++c) mxs[c & 7] = fmaxf(mxs[c & 7], sv[c]);
+            const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
+                                   fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
             const float m_cand = mx * p.scale_log2;  // softmax_scale > 0 on this path
             float alpha = 1.f;
             bool resc = false;
@@ -361,15 +409,16 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 resc = true;
             }
             const float m_use = m_run == -INFINITY ? 0.f : m_run;
-            float sum = 0.f;
+            float sums[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             uint32_t pk[64];
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
                 const float p0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, -m_use));
                 const float p1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, -m_use));
-                sum += p0 + p1;
+                sums[c & 7] += p0 + p1;
                 pk[c] = pack2<T>(p0, p1);
             }
+            const float sum = ((sums[0] + sums[1]) + (sums[2] + sums[3])) + ((sums[4] + sums[5]) + (sums[6] + sums[7]));
             l_run = l_run * alpha + sum;
             if (j > 0 && __any_sync(0xffffffffu, resc)) {
                 // O was accumulated with the old maximum: rescale it once PV_{j-1} is done
@@ -492,7 +541,7 @@ int run_prefill(const Args& a, const PrefillParams& pp, cudaStream_t stream, cha
         }
         configured = true;
     }
-    dim3 grid(pp.q_tiles, a.Hkv, a.batch);
+    dim3 grid(pp.q_tiles, a.Hkv, 1);
     kern<<<grid, kPrefillThreads, C::SMEM, stream>>>(tq, tk, tv, pp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
@@ -551,7 +600,9 @@ int launch_prefill(const Args& a, unsigned int* err, char* msg, size_t msg_len) 
     pp.wl = a.wl;
     pp.wr = a.wr;
     pp.rows_cap = prefill_rows_threshold();
-    pp.q_tiles = (int)(((int64_t)a.max_sq * pp.G + 127) / 128);
+    // upper bound of the number of 128-row tiles: sum_b ceil(sq_b G / 128) <= ceil(total_q G / 128) + batch
+    pp.q_tiles = (int)std::min<int64_t>(((int64_t)a.total_q * pp.G + 127) / 128 + a.batch,
+                                        (int64_t)a.batch * (((int64_t)a.max_sq * pp.G + 127) / 128));
     pp.err = err;
     pp.wait_ns = a.wait_ns;
     pp.withhold = a.withhold_loads;
