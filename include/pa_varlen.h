@@ -125,6 +125,35 @@ int pa_varlen_fwd(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor*
                   void* stream);
 
 /*
+ * pa_varlen_fwd_noalloc -- pa_varlen_fwd without any device allocation.  (The pages have
+ * no counterpart: this is a deployment variant of the same call.)
+ *
+ * For callers that cannot call cudaMalloc: inference runtimes that hand all device memory
+ * to their own arena at start-up, code that runs where an allocation could synchronise the
+ * device or fail at the worst moment (latency-critical serving loops), and hosts that only
+ * let a plug-in use the buffers they pass in.  Same arguments, checks and results as
+ * pa_varlen_fwd; the caller still provides every input and output.
+ *
+ * Scratch: split-KV partial results go to one fixed 32 MiB array compiled into the library
+ * (a static device array: every GPU that loads the library holds it until the process
+ * exits) instead of the library's growable workspace.  A call whose split plan needs more
+ * than 32 MiB is rejected with PA_ERR_WORKSPACE and a message giving both sizes.  The
+ * array keeps the last call's contents; nothing in it needs to start at zero.  All calls,
+ * on every stream and host thread, share this one array: calls that overlap on the GPU
+ * race and give undefined results, so serialise them (one stream, or events).
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, which allocates nothing); make that first call before any stream
+ * capture.  It calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+int pa_varlen_fwd_noalloc(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                          const pa_tensor* cu_seqlens_q, const pa_tensor* cu_seqlens_k,
+                          const pa_tensor* block_table, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                          int32_t num_heads, int32_t num_heads_k, int32_t head_dim,
+                          int32_t page_block_size, float softmax_scale, int32_t window_left,
+                          int32_t window_right, const pa_tensor* out, const pa_tensor* softmax_lse,
+                          void* stream);
+
+/*
  * pa_varlen_check -- the host-side checks of pa_varlen_fwd alone: no device-residency
  * check, no CUDA call, no launch.  Same arguments (no stream), same status codes.
  * Lets a caller (or a test without a GPU) validate descriptors ahead of time.

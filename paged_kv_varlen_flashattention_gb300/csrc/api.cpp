@@ -294,6 +294,11 @@ int workspace_for(cudaStream_t stream, size_t bytes, void** ptr) {
     return PA_OK;
 }
 
+// Scratch provider of pa_varlen_fwd: the library's own grow-only workspace.
+int library_workspace(void*, cudaStream_t stream, size_t bytes, void** ptr, char*, size_t) {
+    return workspace_for(stream, bytes, ptr);
+}
+
 int sm_count() {
     static int cached[256] = {};
     int dev = 0;
@@ -401,24 +406,14 @@ int launch_splitkv(const Args& a, const SplitPlan& plan, void* workspace, unsign
 
 }  // namespace pa
 
-extern "C" {
+namespace pa {
 
-int pa_varlen_check(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
-                    const pa_tensor* cu_seqlens_q, const pa_tensor* cu_seqlens_k, const pa_tensor* block_table,
-                    int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_heads, int32_t num_heads_k,
-                    int32_t head_dim, int32_t page_block_size, float softmax_scale, int32_t window_left,
-                    int32_t window_right, const pa_tensor* out, const pa_tensor* softmax_lse) {
-    pa::Args a{};
-    return validate(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, max_seqlen_q, max_seqlen_k,
-                    num_heads, num_heads_k, head_dim, page_block_size, softmax_scale, window_left, window_right, out,
-                    softmax_lse, false, &a);
-}
-
-int pa_varlen_fwd(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
-                  const pa_tensor* cu_seqlens_q, const pa_tensor* cu_seqlens_k, const pa_tensor* block_table,
-                  int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_heads, int32_t num_heads_k,
-                  int32_t head_dim, int32_t page_block_size, float softmax_scale, int32_t window_left,
-                  int32_t window_right, const pa_tensor* out, const pa_tensor* softmax_lse, void* stream) {
+int forward_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                 const pa_tensor* cu_seqlens_q, const pa_tensor* cu_seqlens_k, const pa_tensor* block_table,
+                 int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_heads, int32_t num_heads_k,
+                 int32_t head_dim, int32_t page_block_size, float softmax_scale, int32_t window_left,
+                 int32_t window_right, const pa_tensor* out, const pa_tensor* softmax_lse, void* stream,
+                 ScratchFn scratch, void* scratch_ctx) {
     pa::Args a{};
     int rc = validate(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, max_seqlen_q, max_seqlen_k,
                       num_heads, num_heads_k, head_dim, page_block_size, softmax_scale, window_left, window_right,
@@ -437,7 +432,7 @@ int pa_varlen_fwd(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor*
     const pa::SplitPlan plan = pa::plan_splitkv(a, use_prefill, sm_count());
     void* ws = nullptr;
     if (plan.ws_bytes) {
-        rc = workspace_for(a.stream, plan.ws_bytes, &ws);
+        rc = scratch(scratch_ctx, a.stream, plan.ws_bytes, &ws, g_msg, sizeof g_msg);
         if (rc != PA_OK) return rc;
     }
     if (use_prefill) {
@@ -448,6 +443,31 @@ int pa_varlen_fwd(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor*
     if (rc != PA_OK) return rc;
     g_msg[0] = '\0';
     return PA_OK;
+}
+
+}  // namespace pa
+
+extern "C" {
+
+int pa_varlen_check(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                    const pa_tensor* cu_seqlens_q, const pa_tensor* cu_seqlens_k, const pa_tensor* block_table,
+                    int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_heads, int32_t num_heads_k,
+                    int32_t head_dim, int32_t page_block_size, float softmax_scale, int32_t window_left,
+                    int32_t window_right, const pa_tensor* out, const pa_tensor* softmax_lse) {
+    pa::Args a{};
+    return validate(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, max_seqlen_q, max_seqlen_k,
+                    num_heads, num_heads_k, head_dim, page_block_size, softmax_scale, window_left, window_right, out,
+                    softmax_lse, false, &a);
+}
+
+int pa_varlen_fwd(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                  const pa_tensor* cu_seqlens_q, const pa_tensor* cu_seqlens_k, const pa_tensor* block_table,
+                  int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_heads, int32_t num_heads_k,
+                  int32_t head_dim, int32_t page_block_size, float softmax_scale, int32_t window_left,
+                  int32_t window_right, const pa_tensor* out, const pa_tensor* softmax_lse, void* stream) {
+    return pa::forward_impl(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, max_seqlen_q,
+                            max_seqlen_k, num_heads, num_heads_k, head_dim, page_block_size, softmax_scale,
+                            window_left, window_right, out, softmax_lse, stream, library_workspace, nullptr);
 }
 
 const char* pa_last_error(void) { return g_msg; }

@@ -83,6 +83,18 @@ int error_word(unsigned int** ptr);
 // Counts successful kernel launches (pa_kernel_launches).
 void count_launches(int n);
 
+// Supplier of the split-KV scratch for one call: sets *ptr to at least `bytes` bytes of
+// device memory usable on `stream`, or returns a status with a message in msg.
+using ScratchFn = int (*)(void* ctx, cudaStream_t stream, size_t bytes, void** ptr, char* msg, size_t msg_len);
+
+// Validation and dispatch shared by the C entry points (api.cpp).
+int forward_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                 const pa_tensor* cu_seqlens_q, const pa_tensor* cu_seqlens_k, const pa_tensor* block_table,
+                 int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_heads, int32_t num_heads_k,
+                 int32_t head_dim, int32_t page_block_size, float softmax_scale, int32_t window_left,
+                 int32_t window_right, const pa_tensor* out, const pa_tensor* softmax_lse, void* stream,
+                 ScratchFn scratch, void* scratch_ctx);
+
 // Tensor-map encoding through the driver entry point (no libcuda link needed).
 // Rank-4 bf16/f16 map over (d0 fastest .. d3), strides in bytes for dims 1..3.
 int encode_tmap_4d(void* map, int dtype, const void* base, const uint64_t dims[4], const uint64_t strides_bytes[3],
