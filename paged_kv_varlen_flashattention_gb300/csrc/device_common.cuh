@@ -65,6 +65,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the same condition (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Gives up after `limit_ns`
 // of wall time and returns false (the caller flags a timeout and leaves the kernel
 // instead of hanging the GPU).
@@ -182,6 +195,24 @@ __device__ __forceinline__ int box_block(const int32_t* bt_row, int bt_cols, int
         return -2;
     }
     return blk;
+}
+
+// 2^x on the FMA/ALU pipes, to take part of the softmax exponentials off MUFU.
+// Cody-Waite style range reduction x = n + f with n = round(x) (by adding and removing
+// 1.5 * 2^23, which leaves n in the low mantissa bits) and f in [-1/2, 1/2]; 2^f by a
+// degree-3 polynomial whose coefficients were fitted by the Remez exchange algorithm to
+// minimise the relative error on [-1/2, 1/2] (max 7.5e-5, below the rounding of the
+// 16-bit P it feeds); 2^n by adding n to the exponent field.  x is clamped below at -126
+// (the result is then ~0); x = -inf gives ~0 as well.
+__device__ __forceinline__ float poly_exp2(float x) {
+    x = fmaxf(x, -126.f);
+    const float t = x + 12582912.f;
+    const float n = t - 12582912.f;
+    const float f = x - n;
+    float p = fmaf(0.0551716685f, f, 0.242611125f);
+    p = fmaf(p, f, 0.693260968f);
+    p = fmaf(p, f, 0.999928057f);
+    return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
 }
 
 // Byte offset of 16-byte unit `u` (0..7) of row `r` in a tile whose rows are 128 bytes

@@ -1,20 +1,25 @@
 // Tensor-core prefill / chunked-prefill kernel for paged varlen attention (sm_103a).
 //
-// One CTA owns 128 query rows of one (sequence, kv head): the rows are the (query i,
-// head g) pairs of the kv head's GQA group, ordered i * G + g, so each K/V tile feeds
-// all G query heads.  Roles (192 threads):
-//   warp 0      TMA producer: the q tile once, then K and V tiles of 128 keys through
+// One CTA owns two 128-row query tiles (A and B, consecutive) of one (sequence, kv head);
+// a tile's rows are the (query i, head g) pairs of the kv head's GQA group, ordered
+// i * G + g, so each K/V tile feeds all G query heads and both query tiles.
+// Roles (384 threads, three warpgroups):
+//   warp 0      TMA producer: both q tiles once, then K and V tiles of 128 keys through
 //               the block table (one box per page piece; the paged layout of
-//               "flash-attn-varlen paged expects k/v tensors of rank 4", What it means)
+//               "flash-attn-varlen paged expects k/v tensors of rank 4", What it means),
+//               with independent K and V rings
 //   warp 1      tensor-memory owner and MMA issuer (one elected lane):
-//               S_j = Q K_j^T   (tcgen05.mma, A and B from shared memory, S in TMEM)
-//               O  += P_j V_j   (tcgen05.mma, A = P from TMEM, B = V from shared memory)
-//   warps 2..5  softmax: thread r owns row r (TMEM lane r); reads S_j from TMEM, masks,
-//               keeps the running max and sum, writes P_j (16-bit) back to TMEM, and
-//               rescales O in TMEM only when the running max grew by more than 2^8
-//               (otherwise the stale max stays: exact after the final division).
-// S is double-buffered in TMEM so Q K_{j+1}^T overlaps the softmax of tile j.
-// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+DP), P0, P1 (64 columns each).
+//               S_X = Q_X K_j^T  (tcgen05.mma, A and B from shared memory, S in TMEM)
+//               O_X += P_X V_j   (tcgen05.mma, A = P from TMEM, B = V from shared memory)
+//   warps 2, 3  idle (they complete warpgroup 0 for the register split)
+//   warps 4..7  softmax of tile A, warps 8..11 softmax of tile B: thread r owns row r
+//               (TMEM lane r); reads S from TMEM, masks, keeps the running max and sum,
+//               writes P (16-bit) over the columns of S it came from, and rescales O in
+//               TMEM only when the running max grew by more than 2^8 (otherwise the stale
+//               max stays: exact after the final division).
+// The two tiles ping-pong: while one warpgroup runs its softmax, the tensor pipe runs the
+// other tile's P.V and next Q.K^T.  TMEM columns: S_A [0,128), S_B [128,256),
+// O_A [256, 256+DP), O_B [256+DP, 256+2 DP).
 //
 // Mask (bottom-right aligned): query i of a sequence with sq queries and sk keys attends
 // key j iff 0 <= j < sk, j >= i + sk - sq - window_left (window_left >= 0), and
@@ -29,7 +34,11 @@
 namespace pa {
 namespace {
 
-constexpr int kPrefillThreads = 192;
+constexpr int kPrefillThreads = 384;  // three warpgroups
+// Register split (setmaxnreg): the launch gives 384 x 168; warpgroup 0 (producer, MMA
+// issuer, two idle warps) drops to 72 and the two softmax warpgroups rise to 216:
+// 128 x 72 + 256 x 216 = 64,512, the launch total.
+constexpr int kRegsControl = 72, kRegsSoftmax = 216;
 
 struct PrefillParams {
     void* out;
@@ -49,7 +58,7 @@ struct PrefillParams {
     float scale_log2;
     int wl, wr;
     int rows_cap;
-    int q_tiles;  // grid.x: an upper bound of the number of 128-row tiles
+    int pairs;  // grid.x: an upper bound of the number of tile pairs
     unsigned int* err;
     uint64_t wait_ns;  // bound on every wait
     int withhold;      // test hook: issue no loads
@@ -57,25 +66,24 @@ struct PrefillParams {
 
 template <int DP>
 struct PfCfg {
-    static constexpr int CH = DP / 64;                 // 64-column (128-byte) chunks
-    static constexpr int Q_BYTES = CH * 128 * 128;
-    static constexpr int KV_TILE = CH * 128 * 128;     // 128 keys x DP
-    static constexpr int KS = DP == 64 ? 4 : 3;        // K stages
-    static constexpr int VS = DP == 64 ? 4 : 3;        // V stages
-    static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = Q_BYTES;
+    static constexpr int CH = DP / 64;              // 64-column (128-byte) chunks
+    static constexpr int Q_TILE = CH * 128 * 128;   // one 128-row q tile
+    static constexpr int KV_TILE = CH * 128 * 128;  // 128 keys x DP
+    static constexpr int KS = 3;                    // K stages
+    static constexpr int VS = DP == 64 ? 3 : 2;     // V stages
+    static constexpr int OFF_Q = 0;                 // q tile A, then q tile B
+    static constexpr int OFF_K = 2 * Q_TILE;
     static constexpr int OFF_V = OFF_K + KS * KV_TILE;
     static constexpr int OFF_BAR = OFF_V + VS * KV_TILE;
     // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2], p_full[2], pv_done[2], drain
     static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 7;
-    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag, picked pair
     static constexpr int OFF_IDS = OFF_MISC + 16;         // block id of every TMA box of the CTA
     static constexpr int MAX_BOXES = 256;
-    static constexpr int SMEM_USED = OFF_IDS + (MAX_BOXES + 4) * 4 + 1024;
-    // at least 120 KB so that one CTA (and its 512 TMEM columns) owns an SM
-    static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
-    static constexpr uint32_t T_S0 = 0, T_S1 = 128, T_O = 256, T_P0 = 256 + DP, T_P1 = 256 + DP + 64;
-    static_assert(T_P1 + 64 <= 512, "TMEM columns");
+    static constexpr int SMEM = OFF_IDS + (MAX_BOXES + 4) * 4 + 1024;
+    static constexpr uint32_t T_S0 = 0, T_S1 = 128;        // S (then P) of tiles A and B
+    static constexpr uint32_t T_O0 = 256, T_O1 = 256 + DP;  // O of tiles A and B
+    static_assert(256 + 2 * DP <= 512, "TMEM columns");
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
@@ -132,21 +140,21 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hk = blockIdx.y;
 
-    // ---- which (sequence, row tile) this CTA owns: the blockIdx.x-th tile of the list of
-    // all 128-row tiles of prefill-class sequences, sequence by sequence, each sequence's
-    // last (longest, under a causal mask) tile first.  Warp 0 scans cu_seqlens_q 32
-    // sequences at a time with a prefix sum of tile counts.
+    // ---- which (sequence, tile pair) this CTA owns: the blockIdx.x-th pair of the list of
+    // all pairs of 128-row tiles of prefill-class sequences, sequence by sequence, each
+    // sequence's last pair (the longest under a causal mask) first.  Warp 0 scans
+    // cu_seqlens_q 32 sequences at a time with a prefix sum of pair counts.
     int* pick = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
     if (warp == 0) {
-        int remaining = (int)blockIdx.x, found_b = -1, found_rt = 0;
+        int remaining = (int)blockIdx.x, found_b = -1, found_u = 0;
         for (int base = 0; base < p.batch && found_b < 0; base += 32) {
             const int bb = base + lane;
-            int tiles = 0;
+            int pairs = 0;
             if (bb < p.batch) {
                 const int64_t rows = (int64_t)(p.cu_q[bb + 1] - p.cu_q[bb]) * p.G;
-                tiles = rows > p.rows_cap ? (int)((rows + 127) / 128) : 0;
+                pairs = rows > p.rows_cap ? (int)((rows + 255) / 256) : 0;
             }
-            int incl = tiles;
+            int incl = pairs;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 const int v = __shfl_up_sync(0xffffffffu, incl, off);
@@ -155,22 +163,22 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             const unsigned hit = __ballot_sync(0xffffffffu, remaining < incl);
             if (hit) {
                 const int src = __ffs(hit) - 1;
-                const int excl = __shfl_sync(0xffffffffu, incl - tiles, src);
-                const int cnt = __shfl_sync(0xffffffffu, tiles, src);
+                const int excl = __shfl_sync(0xffffffffu, incl - pairs, src);
+                const int cnt = __shfl_sync(0xffffffffu, pairs, src);
                 found_b = base + src;
-                found_rt = cnt - 1 - (remaining - excl);
+                found_u = cnt - 1 - (remaining - excl);
             } else {
                 remaining -= __shfl_sync(0xffffffffu, incl, 31);
             }
         }
         if (lane == 0) {
             pick[0] = found_b;
-            pick[1] = found_rt;
+            pick[1] = found_u;
         }
     }
     __syncthreads();
-    const int b = pick[0], rt = pick[1];
-    if (b < 0) return;  // past the last tile
+    const int b = pick[0], u = pick[1];
+    if (b < 0) return;  // past the last pair
 
     // ---- this CTA's work (uniform over the CTA) ----
     const int q0 = p.cu_q[b], q1 = p.cu_q[b + 1];
@@ -182,12 +190,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         return;
     }
     const int64_t rows_total = (int64_t)sq * p.G;
-    if (rows_total <= p.rows_cap) return;  // decode class: owned by the split-KV kernel
-    const int row0 = rt * 128;
-    if (row0 >= rows_total) return;
-    const int qpt = 128 / p.G;
+    const int row0 = u * 256;                             // first row of tile A
+    const bool has_b = (int64_t)row0 + 128 < rows_total;  // tile B holds at least one row
+    const int qpt = 128 / p.G;                            // queries per tile
     const int i0 = row0 / p.G;
-    const int i_last = min(sq - 1, i0 + qpt - 1);
+    const int i_last = min(sq - 1, i0 + (has_b ? 2 : 1) * qpt - 1);
     const int64_t cdiag = (int64_t)sk - sq;
     const int64_t lo = p.wl >= 0 ? max64(0, i0 + cdiag - p.wl) : 0;
     const int64_t hi = p.wr >= 0 ? min64((int64_t)sk - 1, i_last + cdiag + p.wr) : (int64_t)sk - 1;
@@ -195,9 +202,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const int n_tiles = hi >= lo ? (int)((hi - kt0) / 128 + 1) : 0;
 
     T* out = static_cast<T*>(p.out);
-    if (n_tiles == 0) {  // no row of this tile attends any key: out = 0, lse = -inf
-        if (warp >= 2) {
-            const int r = (warp & 3) * 32 + lane;
+    if (n_tiles == 0) {  // no row of the pair attends any key: out = 0, lse = -inf
+        if (warp >= 4) {
+            const int r = ((warp - 4) >> 2) * 128 + (warp & 3) * 32 + lane;
             const int64_t rho = row0 + r;
             if (rho < rows_total) {
                 const int i = (int)(rho / p.G), g = (int)(rho - (int64_t)i * p.G);
@@ -217,9 +224,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     uint64_t* k_empty = k_full + C::KS;
     uint64_t* v_full = k_empty + C::KS;
     uint64_t* v_empty = v_full + C::VS;
-    uint64_t* s_full = v_empty + C::VS;
-    uint64_t* p_full = s_full + 2;
-    uint64_t* pv_done = p_full + 2;
+    uint64_t* s_full = v_empty + C::VS;  // [tile]
+    uint64_t* p_full = s_full + 2;       // [tile]
+    uint64_t* pv_done = p_full + 2;      // [tile]: the tile's last P.V has completed
     uint64_t* drain = pv_done + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile uint32_t* abort_flag = tmem_slot + 1;
@@ -234,10 +241,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&s_full[s], 1);
-            mbar_init(&p_full[s], 4);  // one arrive per softmax warp
-            mbar_init(&pv_done[s], 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&s_full[x], 1);
+            mbar_init(&p_full[x], 4);  // one arrive per softmax warp
+            mbar_init(&pv_done[x], 1);
         }
         mbar_init(drain, 1);
         *abort_flag = 0u;
@@ -252,6 +259,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
+    if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         // physical block of every box of this CTA's key range, looked up once
@@ -267,87 +276,146 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
-            mbar_arrive_expect_tx(q_full, C::Q_BYTES);
-            for (int c = 0; c < C::CH; ++c)
-                tma_load_4d(smem + C::OFF_Q + c * 128 * 128, &tm_q, q_full, c * 64, hk * p.G, q0 + i0, 0, 0ull);
+            mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::Q_TILE);
+            for (int x = 0; x < (has_b ? 2 : 1); ++x)
+                for (int c = 0; c < C::CH; ++c)
+                    tma_load_4d(smem + C::OFF_Q + x * C::Q_TILE + c * 128 * 128, &tm_q, q_full, c * 64, hk * p.G,
+                                q0 + i0 + x * qpt, 0, 0ull);
             int* spill = ids + C::MAX_BOXES;  // block ids of one tile past the staged range
-            for (int j = 0; j < n_tiles; ++j) {
-                const int* tile_ids = ids;
-                int jt = j;
-                if ((j + 1) * p.boxes_per_tile > C::MAX_BOXES) {
-                    for (int jj = 0; jj < p.boxes_per_tile; ++jj) {
-                        const int key = kt0 + j * 128 + jj * p.box_rows;
-                        spill[jj] = p.paged ? box_block(bt_row, p.bt_cols, p.num_blocks, p.P, key, sk, p.err)
-                                            : (key < sk ? 0 : -1);
-                    }
-                    tile_ids = spill;
-                    jt = 0;
+            auto tile_ids = [&](int j, int& jt, int& kbase_j) -> const int* {
+                jt = j;
+                kbase_j = kt0;
+                if ((j + 1) * p.boxes_per_tile <= C::MAX_BOXES) return ids;
+                for (int jj = 0; jj < p.boxes_per_tile; ++jj) {
+                    const int key = kt0 + j * 128 + jj * p.box_rows;
+                    spill[jj] = p.paged ? box_block(bt_row, p.bt_cols, p.num_blocks, p.P, key, sk, p.err)
+                                        : (key < sk ? 0 : -1);
                 }
-                int s = j % C::KS;
-                if (j >= C::KS && !wait_bar(&k_empty[s], ((j / C::KS) - 1) & 1, abort_flag, p.err, p.wait_ns)) break;
-                issue_kv_tile(p, &tm_k, smem + C::OFF_K + s * C::KV_TILE, &k_full[s], tile_ids, jt, hk,
-                              kt0 + (j - jt) * 128, k0, C::CH);
-                s = j % C::VS;
-                if (j >= C::VS && !wait_bar(&v_empty[s], ((j / C::VS) - 1) & 1, abort_flag, p.err, p.wait_ns)) break;
-                issue_kv_tile(p, &tm_v, smem + C::OFF_V + s * C::KV_TILE, &v_full[s], tile_ids, jt, hk,
-                              kt0 + (j - jt) * 128, k0, C::CH);
+                jt = 0;
+                kbase_j = kt0 + j * 128;
+                return spill;
+            };
+            // K and V advance independently: a K slot frees when the tile's Q K^T products
+            // complete, a V slot only when its P V products complete (after the softmax).
+            int jk = 0, jv = 0;
+            uint64_t t_last = global_timer_ns();
+            while (jk < n_tiles || jv < n_tiles) {
+                bool progressed = false;
+                if (jk < n_tiles) {
+                    const int s = jk % C::KS;
+                    if (jk < C::KS || mbar_test_wait(&k_empty[s], ((jk / C::KS) - 1) & 1)) {
+                        int jt, kb;
+                        const int* ti = tile_ids(jk, jt, kb);
+                        issue_kv_tile(p, &tm_k, smem + C::OFF_K + s * C::KV_TILE, &k_full[s], ti, jt, hk, kb, k0,
+                                      C::CH);
+                        ++jk;
+                        progressed = true;
+                    }
+                }
+                if (jv < jk) {
+                    const int s = jv % C::VS;
+                    if (jv < C::VS || mbar_test_wait(&v_empty[s], ((jv / C::VS) - 1) & 1)) {
+                        int jt, kb;
+                        const int* ti = tile_ids(jv, jt, kb);
+                        issue_kv_tile(p, &tm_v, smem + C::OFF_V + s * C::KV_TILE, &v_full[s], ti, jt, hk, kb, k0,
+                                      C::CH);
+                        ++jv;
+                        progressed = true;
+                    }
+                }
+                if (progressed) {
+                    t_last = global_timer_ns();
+                } else {
+                    __nanosleep(128);  // back off: this warp shares a scheduler with softmax warps
+                    if (*abort_flag) break;
+                    if (global_timer_ns() - t_last > p.wait_ns) {
+                        *abort_flag = 1u;
+                        flag_error(p.err, PA_ERR_DEVICE_TIMEOUT);
+                        break;
+                    }
+                }
             }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         constexpr uint32_t IDESC_S = tc::idesc_f16(128, 128, kBF16, false, false);
         constexpr uint32_t IDESC_O = tc::idesc_f16(128, DP, kBF16, false, true);
-        const uint32_t q_addr = smem_addr(smem + C::OFF_Q);
-        bool ok = __all_sync(0xffffffffu, wait_bar(q_full, 0, abort_flag, p.err, p.wait_ns));
-        for (int j = 0; ok && j <= n_tiles; ++j) {
-            if (j < n_tiles) {
-                const int s = j % C::KS;
-                ok = __all_sync(0xffffffffu, wait_bar(&k_full[s], (j / C::KS) & 1, abort_flag, p.err, p.wait_ns));
-                if (!ok) break;
-                tc::fence_after_sync();
-                if (lane == 0) {
-                    const uint32_t d = tmem + ((j & 1) ? C::T_S1 : C::T_S0);
-                    const uint32_t k_addr = smem_addr(smem + C::OFF_K + s * C::KV_TILE);
+        const int nx = has_b ? 2 : 1;
+        // S_x = Q_x K_j^T into S buffer x
+        auto issue_s = [&](int x, int j) {
+            if (lane == 0) {
+                const uint32_t q_addr = smem_addr(smem + C::OFF_Q + x * C::Q_TILE);
+                const uint32_t k_addr = smem_addr(smem + C::OFF_K + (j % C::KS) * C::KV_TILE);
+                const uint32_t d = tmem + (x ? C::T_S1 : C::T_S0);
 #pragma unroll
-                    for (int kk = 0; kk < DP / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
-                        tc::mma_ss(d, tc::smem_desc_sw128(q_addr + off, 16, 1024),
-                                   tc::smem_desc_sw128(k_addr + off, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
-                    }
-                    tc::commit(&s_full[j & 1]);
-                    tc::commit(&k_empty[s]);
+                for (int kk = 0; kk < DP / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+                    tc::mma_ss(d, tc::smem_desc_sw128(q_addr + off, 16, 1024),
+                               tc::smem_desc_sw128(k_addr + off, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
                 }
-                __syncwarp();
+                tc::commit(&s_full[x]);
             }
-            if (j >= 1) {
-                const int t = j - 1;
-                const int s = t % C::VS;
-                ok = __all_sync(0xffffffffu, wait_bar(&p_full[t & 1], (t >> 1) & 1, abort_flag, p.err, p.wait_ns));
+        };
+        // O_x += P_x V_j, P_x read from the columns of S buffer x
+        auto issue_pv = [&](int x, int j) {
+            if (lane == 0) {
+                const uint32_t v_addr = smem_addr(smem + C::OFF_V + (j % C::VS) * C::KV_TILE);
+                const uint32_t pt = tmem + (x ? C::T_S1 : C::T_S0);
+                const uint32_t d = tmem + (x ? C::T_O1 : C::T_O0);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    tc::mma_ts(d, pt + kk * 8, tc::smem_desc_sw128(v_addr + kk * 2048, 128 * 128, 1024), IDESC_O,
+                               (j > 0 || kk > 0) ? 1u : 0u);
+            }
+        };
+        auto wait_k = [&](int j) {
+            const bool r = __all_sync(0xffffffffu, wait_bar(&k_full[j % C::KS], (j / C::KS) & 1, abort_flag,
+                                                             p.err, p.wait_ns));
+            tc::fence_after_sync();
+            return r;
+        };
+        // Tensor-pipe order: S_A(0), S_B(0), then for each tile j:
+        //   PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
+        // S_x(j+1) overwrites the P_x(j) columns only after PV_x(j) in pipe order.
+        bool ok = __all_sync(0xffffffffu, wait_bar(q_full, 0, abort_flag, p.err, p.wait_ns));
+        if (ok) ok = wait_k(0);
+        if (ok) {
+            for (int x = 0; x < nx; ++x) issue_s(x, 0);
+            if (lane == 0) tc::commit(&k_empty[0]);
+            __syncwarp();
+        }
+        for (int j = 0; ok && j < n_tiles; ++j) {
+            const bool more = j + 1 < n_tiles;
+            for (int x = 0; ok && x < nx; ++x) {
+                ok = __all_sync(0xffffffffu, wait_bar(&p_full[x], j & 1, abort_flag, p.err, p.wait_ns));
                 if (!ok) break;
-                ok = __all_sync(0xffffffffu, wait_bar(&v_full[s], (t / C::VS) & 1, abort_flag, p.err, p.wait_ns));
-                if (!ok) break;
-                uint8_t* vst = smem + C::OFF_V + s * C::KV_TILE;
-                const int valid = min(128, sk - (kt0 + t * 128));
-                if (valid < 128) {  // keys at or past sk: zero V rows so P = 0 never meets NaN
-                    const int zr = 128 - valid;
-                    for (int idx = lane; idx < C::CH * zr * 8; idx += 32) {
-                        const int c = idx / (zr * 8), rem = idx - c * zr * 8;
-                        *reinterpret_cast<int4*>(vst + (c * 128 + valid + (rem >> 3)) * 128 + ((rem & 7) << 4)) =
-                            make_int4(0, 0, 0, 0);
+                if (x == 0) {
+                    ok = __all_sync(0xffffffffu, wait_bar(&v_full[j % C::VS], (j / C::VS) & 1, abort_flag,
+                                                          p.err, p.wait_ns));
+                    if (!ok) break;
+                    uint8_t* vst = smem + C::OFF_V + (j % C::VS) * C::KV_TILE;
+                    const int valid = min(128, sk - (kt0 + j * 128));
+                    if (valid < 128) {  // keys at or past sk: zero V rows so P = 0 never meets NaN
+                        const int zr = 128 - valid;
+                        for (int idx = lane; idx < C::CH * zr * 8; idx += 32) {
+                            const int c = idx / (zr * 8), rem = idx - c * zr * 8;
+                            *reinterpret_cast<int4*>(vst + (c * 128 + valid + (rem >> 3)) * 128 + ((rem & 7) << 4)) =
+                                make_int4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
                     }
-                    fence_proxy_async_smem();
-                    __syncwarp();
                 }
                 tc::fence_after_sync();
+                issue_pv(x, j);
                 if (lane == 0) {
-                    const uint32_t pt = tmem + ((t & 1) ? C::T_P1 : C::T_P0);
-                    const uint32_t v_addr = smem_addr(vst);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        tc::mma_ts(tmem + C::T_O, pt + kk * 8, tc::smem_desc_sw128(v_addr + kk * 2048, 128 * 128, 1024),
-                                   IDESC_O, (t > 0 || kk > 0) ? 1u : 0u);
-                    tc::commit(&pv_done[t & 1]);
-                    tc::commit(&v_empty[s]);
+                    if (x == nx - 1) tc::commit(&v_empty[j % C::VS]);
+                    if (!more) tc::commit(&pv_done[x]);
+                }
+                if (more) {
+                    if (x == 0 && !(ok = wait_k(j + 1))) break;
+                    issue_s(x, j + 1);
+                    if (lane == 0 && x == nx - 1) tc::commit(&k_empty[(j + 1) % C::KS]);
                 }
                 __syncwarp();
             }
@@ -358,11 +426,15 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             mbar_wait(drain, 0, p.wait_ns);  // not cut short by an abort: MMAs may be in flight
         }
         __syncwarp();
+    }
     } else {
-        // ---------------- softmax warpgroup ----------------
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    if (warp < 8 || has_b) {
+        // ---------------- softmax warpgroups ----------------
+        const int x = (warp - 4) >> 2;  // 0: tile A (warps 4..7), 1: tile B (warps 8..11)
         const int wq = warp & 3;
         const int r = wq * 32 + lane;
-        const int64_t rho = row0 + r;
+        const int64_t rho = row0 + x * 128 + r;
         const bool row_valid = rho < rows_total;
         const int i = (int)(rho / p.G), g = (int)(rho - (int64_t)i * p.G);
         int lo_r = 0, hi_r = -1;
@@ -372,15 +444,16 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             hi_r = p.wr >= 0 ? (int)max64(-1, min64((int64_t)sk - 1, diag + p.wr)) : sk - 1;
         }
         const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+        const uint32_t s_col = tmem + lane_base + (x ? C::T_S1 : C::T_S0);
+        const uint32_t o_col = tmem + lane_base + (x ? C::T_O1 : C::T_O0);
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
             const int kt = kt0 + j * 128;
-            ok = __all_sync(0xffffffffu, wait_bar(&s_full[j & 1], (j >> 1) & 1, abort_flag, p.err, p.wait_ns));
+            ok = __all_sync(0xffffffffu, wait_bar(&s_full[x], j & 1, abort_flag, p.err, p.wait_ns));
             if (!ok) break;
             tc::fence_after_sync();
             float sv[128];
-            const uint32_t s_col = tmem + lane_base + ((j & 1) ? C::T_S1 : C::T_S0);
             tc::ld_32cols(s_col + 0, *reinterpret_cast<float(*)[32]>(&sv[0]));
             tc::ld_32cols(s_col + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
             tc::ld_32cols(s_col + 64, *reinterpret_cast<float(*)[32]>(&sv[64]));
@@ -395,7 +468,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             }
             float mxs[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) mxs[u] = sv[u];
+            for (int w = 0; w < 8; ++w) mxs[w] = sv[w];
 #pragma unroll
             for (int c = 8; c < 128; ++c) mxs[c & 7] = fmaxf(mxs[c & 7], sv[c]);
             const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
@@ -407,6 +480,20 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 alpha = fast_exp2(m_run - m_cand);
                 m_run = m_cand;
                 resc = true;
+            }
+            // O_x was accumulated with the old maximum.  Its last P.V (PV_x(j-1)) precedes
+            // S_x(j) in the tensor pipe, so it is complete once S_x(j) is.
+            if (j > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+                for (int cc = 0; cc < DP / 32; ++cc) {
+                    float o[32];
+                    tc::ld_32cols(o_col + cc * 32, o);
+                    tc::wait_ld();
+                    uint32_t ob[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) ob[e] = __float_as_uint(o[e] * alpha);
+                    tc::st_32cols(o_col + cc * 32, ob);
+                }
             }
             const float m_use = m_run == -INFINITY ? 0.f : m_run;
             float sums[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -420,40 +507,15 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             }
             const float sum = ((sums[0] + sums[1]) + (sums[2] + sums[3])) + ((sums[4] + sums[5]) + (sums[6] + sums[7]));
             l_run = l_run * alpha + sum;
-            if (j > 0 && __any_sync(0xffffffffu, resc)) {
-                // O was accumulated with the old maximum: rescale it once PV_{j-1} is done
-                ok = __all_sync(0xffffffffu, wait_bar(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.err, p.wait_ns));
-                if (!ok) break;
-                tc::fence_after_sync();
-#pragma unroll 1
-                for (int cc = 0; cc < DP / 32; ++cc) {
-                    float o[32];
-                    tc::ld_32cols(tmem + lane_base + C::T_O + cc * 32, o);
-                    tc::wait_ld();
-                    uint32_t ob[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) ob[e] = __float_as_uint(o[e] * alpha);
-                    tc::st_32cols(tmem + lane_base + C::T_O + cc * 32, ob);
-                }
-                tc::wait_st();
-            }
-            if (j >= 2) {  // P buffer (j & 1) was read by PV_{j-2}
-                ok = __all_sync(0xffffffffu, wait_bar(&pv_done[j & 1], ((j - 2) >> 1) & 1, abort_flag, p.err, p.wait_ns));
-                if (!ok) break;
-                tc::fence_after_sync();
-            }
-            const uint32_t p_col = tmem + lane_base + ((j & 1) ? C::T_P1 : C::T_P0);
-            tc::st_32cols(p_col, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-            tc::st_32cols(p_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+            // P overwrites the first 64 columns of the S it came from
+            tc::st_32cols(s_col, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+            tc::st_32cols(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
             tc::wait_st();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[j & 1]);
+            if (lane == 0) mbar_arrive(&p_full[x]);
         }
-        if (ok) {
-            const int t_last = n_tiles - 1;
-            ok = __all_sync(0xffffffffu, wait_bar(&pv_done[t_last & 1], (t_last >> 1) & 1, abort_flag, p.err, p.wait_ns));
-        }
+        if (ok) ok = __all_sync(0xffffffffu, wait_bar(&pv_done[x], 0, abort_flag, p.err, p.wait_ns));
         if (ok) {
             tc::fence_after_sync();
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -463,7 +525,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll 1
             for (int cc = 0; cc < DP / 32; ++cc) {
                 float o[32];
-                tc::ld_32cols(tmem + lane_base + C::T_O + cc * 32, o);
+                tc::ld_32cols(o_col + cc * 32, o);
                 tc::wait_ld();
                 if (row_valid) {
 #pragma unroll
@@ -485,6 +547,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
         }
         tc::fence_before_sync();
+    }
     }
     __syncwarp();
     __syncthreads();
@@ -541,7 +604,7 @@ int run_prefill(const Args& a, const PrefillParams& pp, cudaStream_t stream, cha
         }
         configured = true;
     }
-    dim3 grid(pp.q_tiles, a.Hkv, 1);
+    dim3 grid(pp.pairs, a.Hkv, 1);
     kern<<<grid, kPrefillThreads, C::SMEM, stream>>>(tq, tk, tv, pp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
@@ -600,9 +663,9 @@ int launch_prefill(const Args& a, unsigned int* err, char* msg, size_t msg_len) 
     pp.wl = a.wl;
     pp.wr = a.wr;
     pp.rows_cap = prefill_rows_threshold();
-    // upper bound of the number of 128-row tiles: sum_b ceil(sq_b G / 128) <= ceil(total_q G / 128) + batch
-    pp.q_tiles = (int)std::min<int64_t>(((int64_t)a.total_q * pp.G + 127) / 128 + a.batch,
-                                        (int64_t)a.batch * (((int64_t)a.max_sq * pp.G + 127) / 128));
+    // upper bound of the number of 256-row pairs: sum_b ceil(sq_b G / 256) <= ceil(total_q G / 256) + batch
+    pp.pairs = (int)std::min<int64_t>(((int64_t)a.total_q * pp.G + 255) / 256 + a.batch,
+                                      (int64_t)a.batch * (((int64_t)a.max_sq * pp.G + 255) / 256));
     pp.err = err;
     pp.wait_ns = a.wait_ns;
     pp.withhold = a.withhold_loads;

@@ -135,3 +135,23 @@ def test_zero_queries_is_a_no_op():
     inp = workloads.materialize(lay, device="cuda")
     out, lse = _gpu.run_cuda(inp)
     assert out.numel() == 0 and lse.numel() == 0
+
+
+def test_prefill_fp16():
+    lay = workloads.small("prefill")
+    lay.dtype = "f16"
+    _gpu.check_layout(lay)
+
+
+@pytest.mark.parametrize("H,Hkv", [(6, 2), (12, 1), (8, 8)])
+def test_group_sizes(H, Hkv):
+    """G = 3 and 12 do not divide the 128-row tensor-core tile (general path); G = 1 does."""
+    _gpu.check_layout(_custom([70, 1, 150], [70, 300, 200], H=H, Hkv=Hkv, D=64))
+
+
+def test_long_prefill_spans_many_tiles_and_pages():
+    _gpu.check_layout(_custom([1000, 517], [1000, 900], H=4, Hkv=1, D=128, P=32), limit=4096)
+
+
+def test_non_causal_prefill_with_sq_below_sk():
+    _gpu.check_layout(_custom([200, 64], [1000, 64], H=8, Hkv=2, D=128, wl=-1, wr=-1))
