@@ -54,10 +54,6 @@ __device__ __forceinline__ bool dec_wait(uint64_t* bar, uint32_t parity, volatil
     }
 }
 
-__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 template <typename T, int DP, int MG, int NT, int STAGES>
 __global__ void __launch_bounds__(160) decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                      const __grid_constant__ CUtensorMap tm_v,

@@ -90,6 +90,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
     }
 }
 
+// Barrier among `nthreads` threads (whole warps) of the CTA on hardware barrier `id` (1..15).
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // ---- TMA ---------------------------------------------------------------------------------
 // Tiled 4-D tensor load into shared memory, completing on `bar` (complete_tx bytes).
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0,

@@ -4,14 +4,14 @@
 // a tile's rows are the (query i, head g) pairs of the kv head's GQA group, ordered
 // i * G + g, so each K/V tile feeds all G query heads and both query tiles.
 // Roles (384 threads, three warpgroups):
-//   warp 0      TMA producer: both q tiles once, then K and V tiles of 128 keys through
-//               the block table (one box per page piece; the paged layout of
-//               "flash-attn-varlen paged expects k/v tensors of rank 4", What it means),
-//               with independent K and V rings
+//   warps 0, 2  TMA producers (warp 0: both q tiles once, then K tiles; warp 2: V tiles),
+//               128 keys per tile through the block table (one box per page piece; the
+//               paged layout of "flash-attn-varlen paged expects k/v tensors of rank 4",
+//               What it means), each blocking on its own ring's empty barriers
 //   warp 1      tensor-memory owner and MMA issuer (one elected lane):
 //               S_X = Q_X K_j^T  (tcgen05.mma, A and B from shared memory, S in TMEM)
 //               O_X += P_X V_j   (tcgen05.mma, A = P from TMEM, B = V from shared memory)
-//   warps 2, 3  idle (they complete warpgroup 0 for the register split)
+//   warp 3      idle (it completes warpgroup 0 for the register split)
 //   warps 4..7  softmax of tile A, warps 8..11 softmax of tile B: thread r owns row r
 //               (TMEM lane r); reads S from TMEM, masks, keeps the running max and sum,
 //               writes P (16-bit) over the columns of S it came from, and rescales O in
@@ -36,9 +36,15 @@ namespace {
 
 constexpr int kPrefillThreads = 384;  // three warpgroups
 // Register split (setmaxnreg): the launch gives 384 x 168; warpgroup 0 (producer, MMA
-// issuer, two idle warps) drops to 72 and the two softmax warpgroups rise to 216:
+// issuer, V producer, one idle warp) drops to 72 and the two softmax warpgroups rise to 216:
 // 128 x 72 + 256 x 216 = 64,512, the launch total.
 constexpr int kRegsControl = 72, kRegsSoftmax = 216;
+#ifndef PA_POLY_EVERY
+#define PA_POLY_EVERY 0
+#endif
+// One softmax pair in kPolyEvery takes its exponentials on the FMA pipe (poly_exp2);
+// 0 (the default) keeps them all on MUFU, which measured faster.
+constexpr int kPolyEvery = PA_POLY_EVERY;
 
 struct PrefillParams {
     void* out;
@@ -261,79 +267,56 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
     if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
-    if (warp == 0) {
-        // ---------------- TMA producer ----------------
-        // physical block of every box of this CTA's key range, looked up once
+    if (warp == 0 || warp == 2) {
+        // ---------------- TMA producers: warp 0 loads q and K, warp 2 loads V ----------------
+        // Physical block of every box of this CTA's key range, staged once by warp 0.
         int* ids = reinterpret_cast<int*>(smem + C::OFF_IDS);
         const int n_boxes = min(n_tiles * p.boxes_per_tile, C::MAX_BOXES);
         const int32_t* bt_row = p.paged ? p.bt + (int64_t)b * p.bt_s0 : nullptr;
-        for (int bi = lane; bi < n_boxes; bi += 32) {
-            const int key = kt0 + bi * p.box_rows;
-            ids[bi] = p.paged ? box_block(bt_row, p.bt_cols, p.num_blocks, p.P, key, sk, p.err) : (key < sk ? 0 : -1);
+        if (warp == 0) {
+            for (int bi = lane; bi < n_boxes; bi += 32) {
+                const int key = kt0 + bi * p.box_rows;
+                ids[bi] = p.paged ? box_block(bt_row, p.bt_cols, p.num_blocks, p.P, key, sk, p.err)
+                                  : (key < sk ? 0 : -1);
+            }
         }
-        __syncwarp();
+        named_barrier_sync(2, 64);  // warps 0 and 2: the staged ids are visible
+        const bool is_k = warp == 0;
         if (lane == 0 && !p.withhold) {
-            prefetch_tmap(&tm_q);
-            prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v);
-            mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::Q_TILE);
-            for (int x = 0; x < (has_b ? 2 : 1); ++x)
-                for (int c = 0; c < C::CH; ++c)
-                    tma_load_4d(smem + C::OFF_Q + x * C::Q_TILE + c * 128 * 128, &tm_q, q_full, c * 64, hk * p.G,
-                                q0 + i0 + x * qpt, 0, 0ull);
-            int* spill = ids + C::MAX_BOXES;  // block ids of one tile past the staged range
-            auto tile_ids = [&](int j, int& jt, int& kbase_j) -> const int* {
-                jt = j;
-                kbase_j = kt0;
-                if ((j + 1) * p.boxes_per_tile <= C::MAX_BOXES) return ids;
-                for (int jj = 0; jj < p.boxes_per_tile; ++jj) {
-                    const int key = kt0 + j * 128 + jj * p.box_rows;
-                    spill[jj] = p.paged ? box_block(bt_row, p.bt_cols, p.num_blocks, p.P, key, sk, p.err)
-                                        : (key < sk ? 0 : -1);
-                }
-                jt = 0;
-                kbase_j = kt0 + j * 128;
-                return spill;
-            };
-            // K and V advance independently: a K slot frees when the tile's Q K^T products
-            // complete, a V slot only when its P V products complete (after the softmax).
-            int jk = 0, jv = 0;
-            uint64_t t_last = global_timer_ns();
-            while (jk < n_tiles || jv < n_tiles) {
-                bool progressed = false;
-                if (jk < n_tiles) {
-                    const int s = jk % C::KS;
-                    if (jk < C::KS || mbar_test_wait(&k_empty[s], ((jk / C::KS) - 1) & 1)) {
-                        int jt, kb;
-                        const int* ti = tile_ids(jk, jt, kb);
-                        issue_kv_tile(p, &tm_k, smem + C::OFF_K + s * C::KV_TILE, &k_full[s], ti, jt, hk, kb, k0,
-                                      C::CH);
-                        ++jk;
-                        progressed = true;
+            const CUtensorMap* map = is_k ? &tm_k : &tm_v;
+            prefetch_tmap(map);
+            if (is_k) {
+                prefetch_tmap(&tm_q);
+                mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::Q_TILE);
+                for (int x = 0; x < (has_b ? 2 : 1); ++x)
+                    for (int c = 0; c < C::CH; ++c)
+                        tma_load_4d(smem + C::OFF_Q + x * C::Q_TILE + c * 128 * 128, &tm_q, q_full, c * 64,
+                                    hk * p.G, q0 + i0 + x * qpt, 0, 0ull);
+            }
+            const int stages = is_k ? C::KS : C::VS;
+            uint64_t* fullb = is_k ? k_full : v_full;
+            uint64_t* emptyb = is_k ? k_empty : v_empty;
+            uint8_t* ring = smem + (is_k ? C::OFF_K : C::OFF_V);
+            int spill[4];  // block ids of one tile past the staged range
+            for (int j = 0; j < n_tiles; ++j) {
+                const int s = j % stages;
+                if (j >= stages && !wait_bar(&emptyb[s], ((j / stages) - 1) & 1, abort_flag, p.err, p.wait_ns))
+                    break;
+                const int* tile = ids;
+                int jt = j, kb = kt0;
+                if ((j + 1) * p.boxes_per_tile > C::MAX_BOXES) {
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const int key = kt0 + j * 128 + jj * p.box_rows;
+                        spill[jj] = jj >= p.boxes_per_tile ? -1
+                                    : p.paged ? box_block(bt_row, p.bt_cols, p.num_blocks, p.P, key, sk, p.err)
+                                              : (key < sk ? 0 : -1);
                     }
+                    tile = spill;
+                    jt = 0;
+                    kb = kt0 + j * 128;
                 }
-                if (jv < jk) {
-                    const int s = jv % C::VS;
-                    if (jv < C::VS || mbar_test_wait(&v_empty[s], ((jv / C::VS) - 1) & 1)) {
-                        int jt, kb;
-                        const int* ti = tile_ids(jv, jt, kb);
-                        issue_kv_tile(p, &tm_v, smem + C::OFF_V + s * C::KV_TILE, &v_full[s], ti, jt, hk, kb, k0,
-                                      C::CH);
-                        ++jv;
-                        progressed = true;
-                    }
-                }
-                if (progressed) {
-                    t_last = global_timer_ns();
-                } else {
-                    __nanosleep(128);  // back off: this warp shares a scheduler with softmax warps
-                    if (*abort_flag) break;
-                    if (global_timer_ns() - t_last > p.wait_ns) {
-                        *abort_flag = 1u;
-                        flag_error(p.err, PA_ERR_DEVICE_TIMEOUT);
-                        break;
-                    }
-                }
+                issue_kv_tile(p, map, ring + s * C::KV_TILE, &fullb[s], tile, jt, hk, kb, k0, C::CH);
             }
         }
     } else if (warp == 1) {
@@ -500,8 +483,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             uint32_t pk[64];
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
-                const float p0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, -m_use));
-                const float p1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, -m_use));
+                const float x0 = fmaf(sv[2 * c], p.scale_log2, -m_use);
+                const float x1 = fmaf(sv[2 * c + 1], p.scale_log2, -m_use);
+                const bool on_fma = kPolyEvery > 0 && (c % (kPolyEvery > 0 ? kPolyEvery : 1)) == kPolyEvery - 1;
+                const float p0 = on_fma ? poly_exp2(x0) : fast_exp2(x0);
+                const float p1 = on_fma ? poly_exp2(x1) : fast_exp2(x1);
                 sums[c & 7] += p0 + p1;
                 pk[c] = pack2<T>(p0, p1);
             }
