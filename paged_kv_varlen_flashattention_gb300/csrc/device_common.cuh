@@ -202,6 +202,31 @@ __device__ __forceinline__ int box_block(const int32_t* bt_row, int bt_cols, int
     return blk;
 }
 
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Packed fp32 pair arithmetic (one instruction per pair on sm_100 and later); each lane
+// rounds exactly like its scalar counterpart.
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                      float c1) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void fadd2_acc(float& d0, float& d1, float a0, float a1) {
+    asm("{\n\t.reg .b64 ra, rd;\n\t"
+        "mov.b64 rd, {%0, %1};\n\tmov.b64 ra, {%2, %3};\n\t"
+        "add.f32x2 rd, rd, ra;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1));
+}
+
 // 2^x on the FMA/ALU pipes, to take part of the softmax exponentials off MUFU.
 // Cody-Waite style range reduction x = n + f with n = round(x) (by adding and removing
 // 1.5 * 2^23, which leaves n in the low mantissa bits) and f in [-1/2, 1/2]; 2^f by a

@@ -324,17 +324,21 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         constexpr uint32_t IDESC_S = tc::idesc_f16(128, 128, kBF16, false, false);
         constexpr uint32_t IDESC_O = tc::idesc_f16(128, DP, kBF16, false, true);
         const int nx = has_b ? 2 : 1;
+        // Shared-memory descriptors are built once; the start-address field (address / 16,
+        // bits 0..13) then advances by a compile-time constant per MMA.
+        const uint64_t dq0 = tc::smem_desc_sw128(smem_addr(smem + C::OFF_Q), 16, 1024);
+        const uint64_t dk0 = tc::smem_desc_sw128(smem_addr(smem + C::OFF_K), 16, 1024);
+        const uint64_t dv0 = tc::smem_desc_sw128(smem_addr(smem + C::OFF_V), 128 * 128, 1024);
         // S_x = Q_x K_j^T into S buffer x
         auto issue_s = [&](int x, int j) {
             if (lane == 0) {
-                const uint32_t q_addr = smem_addr(smem + C::OFF_Q + x * C::Q_TILE);
-                const uint32_t k_addr = smem_addr(smem + C::OFF_K + (j % C::KS) * C::KV_TILE);
+                const uint64_t da = dq0 + (uint64_t)(x * (C::Q_TILE >> 4));
+                const uint64_t db = dk0 + (uint64_t)((j % C::KS) * (C::KV_TILE >> 4));
                 const uint32_t d = tmem + (x ? C::T_S1 : C::T_S0);
 #pragma unroll
                 for (int kk = 0; kk < DP / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
-                    tc::mma_ss(d, tc::smem_desc_sw128(q_addr + off, 16, 1024),
-                               tc::smem_desc_sw128(k_addr + off, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+                    const uint64_t off = (uint64_t)((kk >> 2) * (128 * 128 / 16) + (kk & 3) * 2);
+                    tc::mma_ss(d, da + off, db + off, IDESC_S, kk > 0 ? 1u : 0u);
                 }
                 tc::commit(&s_full[x]);
             }
@@ -342,13 +346,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         // O_x += P_x V_j, P_x read from the columns of S buffer x
         auto issue_pv = [&](int x, int j) {
             if (lane == 0) {
-                const uint32_t v_addr = smem_addr(smem + C::OFF_V + (j % C::VS) * C::KV_TILE);
+                const uint64_t db = dv0 + (uint64_t)((j % C::VS) * (C::KV_TILE >> 4));
                 const uint32_t pt = tmem + (x ? C::T_S1 : C::T_S0);
                 const uint32_t d = tmem + (x ? C::T_O1 : C::T_O0);
+                const uint32_t first = j > 0 ? 1u : 0u;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    tc::mma_ts(d, pt + kk * 8, tc::smem_desc_sw128(v_addr + kk * 2048, 128 * 128, 1024), IDESC_O,
-                               (j > 0 || kk > 0) ? 1u : 0u);
+                    tc::mma_ts(d, pt + kk * 8, db + (uint64_t)(kk * (2048 / 16)), IDESC_O, kk > 0 ? 1u : first);
             }
         };
         auto wait_k = [&](int j) {
@@ -449,13 +453,16 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     sv[c] = (key >= lo_r && key <= hi_r) ? sv[c] : -INFINITY;
                 }
             }
-            float mxs[8];
+            // row maximum: four independent chains of three-input max
+            float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
 #pragma unroll
-            for (int w = 0; w < 8; ++w) mxs[w] = sv[w];
-#pragma unroll
-            for (int c = 8; c < 128; ++c) mxs[c & 7] = fmaxf(mxs[c & 7], sv[c]);
-            const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
-                                   fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
+            for (int c = 4; c < 128; c += 8) {
+                mx0 = max3f(mx0, sv[c], sv[c + 1]);
+                mx1 = max3f(mx1, sv[c + 2], sv[c + 3]);
+                mx2 = max3f(mx2, sv[c + 4], sv[c + 5]);
+                mx3 = max3f(mx3, sv[c + 6], sv[c + 7]);
+            }
+            const float mx = max3f(mx0, mx1, fmaxf(mx2, mx3));
             const float m_cand = mx * p.scale_log2;  // softmax_scale > 0 on this path
             float alpha = 1.f;
             bool resc = false;
@@ -479,16 +486,17 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 }
             }
             const float m_use = m_run == -INFINITY ? 0.f : m_run;
+            const float sl = p.scale_log2, nm = -m_use;
             float sums[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             uint32_t pk[64];
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
-                const float x0 = fmaf(sv[2 * c], p.scale_log2, -m_use);
-                const float x1 = fmaf(sv[2 * c + 1], p.scale_log2, -m_use);
+                float x0, x1;
+                ffma2(x0, x1, sv[2 * c], sv[2 * c + 1], sl, sl, nm, nm);  // scores -> log2 domain
                 const bool on_fma = kPolyEvery > 0 && (c % (kPolyEvery > 0 ? kPolyEvery : 1)) == kPolyEvery - 1;
                 const float p0 = on_fma ? poly_exp2(x0) : fast_exp2(x0);
                 const float p1 = on_fma ? poly_exp2(x1) : fast_exp2(x1);
-                sums[c & 7] += p0 + p1;
+                fadd2_acc(sums[2 * (c & 3)], sums[2 * (c & 3) + 1], p0, p1);
                 pk[c] = pack2<T>(p0, p1);
             }
             const float sum = ((sums[0] + sums[1]) + (sums[2] + sums[3])) + ((sums[4] + sums[5]) + (sums[6] + sums[7]));
