@@ -381,15 +381,22 @@ SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, int num_sms)
     if (const char* env = std::getenv("PA_SPLIT_TILES")) {
         split_tiles = std::max<int64_t>(1, std::atoll(env));
     } else if (pl.row_tiles == 1) {
-        // aim at about four CTAs of work per SM; a split never shorter than 4 tiles
+        // Aim at about four CTAs of work per SM.  A split is never shorter than 4 tiles, nor
+        // than 8 M keys: its fp32 partial result (M rows x D x 4 bytes, written and read back)
+        // then costs at most ~1/8 of the K/V bytes it reads (8 M keys x 2 D x 2 bytes).
         const int64_t target = 4ll * num_sms;
         int64_t splits = (target + units - 1) / units;
         splits = std::max<int64_t>(1, std::min(splits, tiles_max));
-        split_tiles = std::max<int64_t>(4, (tiles_max + splits - 1) / splits);
+        const int64_t min_tiles = std::max<int64_t>(4, (8ll * M + pl.nt - 1) / pl.nt);
+        split_tiles = std::max<int64_t>(min_tiles, (tiles_max + splits - 1) / splits);
     }
     split_tiles = std::min(split_tiles, tiles_max);
     pl.split_tiles = (int)split_tiles;
     pl.max_splits = (int)((tiles_max + split_tiles - 1) / split_tiles);
+    if (pl.max_splits > 1024) {  // the combine keeps at most 1024 split weights per row
+        pl.split_tiles = (int)((tiles_max + 1023) / 1024);
+        pl.max_splits = (int)((tiles_max + pl.split_tiles - 1) / pl.split_tiles);
+    }
     pl.ws_bytes = 0;
     if (pl.max_splits > 1) {
         const size_t rows = (size_t)a.total_q * a.H;

@@ -146,6 +146,44 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hk = blockIdx.y;
 
+    // ---- set-up that does not depend on the work item, overlapped with the scan below:
+    // warp 1 allocates tensor memory, warp 2 initialises the barriers.
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* q_full = bars;
+    uint64_t* k_full = bars + 1;
+    uint64_t* k_empty = k_full + C::KS;
+    uint64_t* v_full = k_empty + C::KS;
+    uint64_t* v_empty = v_full + C::VS;
+    uint64_t* s_full = v_empty + C::VS;  // [tile]
+    uint64_t* p_full = s_full + 2;       // [tile]
+    uint64_t* pv_done = p_full + 2;      // [tile]: the tile's last P.V has completed
+    uint64_t* drain = pv_done + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+    if (tid == 64) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < C::KS; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+        }
+        for (int s = 0; s < C::VS; ++s) {
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&s_full[x], 1);
+            mbar_init(&p_full[x], 4);  // one arrive per softmax warp
+            mbar_init(&pv_done[x], 1);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::tmem_relinquish();
+    }
+
     // ---- which (sequence, tile pair) this CTA owns: the blockIdx.x-th pair of the list of
     // all pairs of 128-row tiles of prefill-class sequences, sequence by sequence, each
     // sequence's last pair (the longest under a causal mask) first.  Warp 0 scans
@@ -182,9 +220,19 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             pick[1] = found_u;
         }
     }
+    tc::fence_before_sync();
     __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
     const int b = pick[0], u = pick[1];
-    if (b < 0) return;  // past the last pair
+    // every early exit below is uniform over the CTA; warp 1 returns the tensor memory
+    auto leave = [&]() {
+        if (warp == 1) tc::tmem_dealloc(tmem, 512);
+    };
+    if (b < 0) {  // past the last pair
+        leave();
+        return;
+    }
 
     // ---- this CTA's work (uniform over the CTA) ----
     const int q0 = p.cu_q[b], q1 = p.cu_q[b + 1];
@@ -193,6 +241,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     if (sq < 0 || sk < 0 || sq > p.max_sq || sk > p.max_sk || q0 < 0 || q1 > p.total_q ||
         (!p.paged && (k0 < 0 || k1 > p.num_blocks))) {
         if (tid == 0) flag_error(p.err, PA_ERR_DEVICE_BOUNDS);
+        leave();
         return;
     }
     const int64_t rows_total = (int64_t)sq * p.G;
@@ -221,49 +270,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 p.lse[(int64_t)h * p.lse_s0 + t] = -INFINITY;
             }
         }
+        leave();
         return;
     }
-
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-    uint64_t* q_full = bars;
-    uint64_t* k_full = bars + 1;
-    uint64_t* k_empty = k_full + C::KS;
-    uint64_t* v_full = k_empty + C::KS;
-    uint64_t* v_empty = v_full + C::VS;
-    uint64_t* s_full = v_empty + C::VS;  // [tile]
-    uint64_t* p_full = s_full + 2;       // [tile]
-    uint64_t* pv_done = p_full + 2;      // [tile]: the tile's last P.V has completed
-    uint64_t* drain = pv_done + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
-    volatile uint32_t* abort_flag = tmem_slot + 1;
-
-    if (tid == 0) {
-        mbar_init(q_full, 1);
-        for (int s = 0; s < C::KS; ++s) {
-            mbar_init(&k_full[s], 1);
-            mbar_init(&k_empty[s], 1);
-        }
-        for (int s = 0; s < C::VS; ++s) {
-            mbar_init(&v_full[s], 1);
-            mbar_init(&v_empty[s], 1);
-        }
-        for (int x = 0; x < 2; ++x) {
-            mbar_init(&s_full[x], 1);
-            mbar_init(&p_full[x], 4);  // one arrive per softmax warp
-            mbar_init(&pv_done[x], 1);
-        }
-        mbar_init(drain, 1);
-        *abort_flag = 0u;
-        fence_mbar_init();
-    }
-    if (warp == 1) {
-        tc::tmem_alloc(tmem_slot, 512);
-        tc::tmem_relinquish();
-    }
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tmem = *tmem_slot;
 
     if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
@@ -274,6 +283,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const int n_boxes = min(n_tiles * p.boxes_per_tile, C::MAX_BOXES);
         const int32_t* bt_row = p.paged ? p.bt + (int64_t)b * p.bt_s0 : nullptr;
         if (warp == 0) {
+            if (lane == 0 && !p.withhold) {  // the q tiles first: their latency overlaps the id lookups
+                prefetch_tmap(&tm_q);
+                mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::Q_TILE);
+                for (int x = 0; x < (has_b ? 2 : 1); ++x)
+                    for (int c = 0; c < C::CH; ++c)
+                        tma_load_4d(smem + C::OFF_Q + x * C::Q_TILE + c * 128 * 128, &tm_q, q_full, c * 64,
+                                    hk * p.G, q0 + i0 + x * qpt, 0, 0ull);
+            }
             for (int bi = lane; bi < n_boxes; bi += 32) {
                 const int key = kt0 + bi * p.box_rows;
                 ids[bi] = p.paged ? box_block(bt_row, p.bt_cols, p.num_blocks, p.P, key, sk, p.err)
@@ -285,14 +302,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         if (lane == 0 && !p.withhold) {
             const CUtensorMap* map = is_k ? &tm_k : &tm_v;
             prefetch_tmap(map);
-            if (is_k) {
-                prefetch_tmap(&tm_q);
-                mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::Q_TILE);
-                for (int x = 0; x < (has_b ? 2 : 1); ++x)
-                    for (int c = 0; c < C::CH; ++c)
-                        tma_load_4d(smem + C::OFF_Q + x * C::Q_TILE + c * 128 * 128, &tm_q, q_full, c * 64,
-                                    hk * p.G, q0 + i0 + x * qpt, 0, 0ull);
-            }
             const int stages = is_k ? C::KS : C::VS;
             uint64_t* fullb = is_k ? k_full : v_full;
             uint64_t* emptyb = is_k ? k_empty : v_empty;

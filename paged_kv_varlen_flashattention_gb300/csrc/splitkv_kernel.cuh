@@ -444,46 +444,62 @@ __global__ void __launch_bounds__(128) splitkv_kernel(const __grid_constant__ CU
 }
 
 // lse = ln sum_s exp(lse_s); out = sum_s exp(lse_s - lse) * O_s, for the tiles that
-// were split.  Same grid as the split kernel without the split dimension.
+// were split.  Grid: (row groups of 4, kv head x row tile, sequence); one warp per output
+// row: the split weights are computed once per row into shared memory, then each lane
+// accumulates pairs of output columns over the splits (reads of the partials coalesce
+// along the head dimension).
+constexpr int kCombineRows = 4;
+constexpr int kCombineMaxSplits = 1024;  // weights kept in shared memory per warp
+
 template <typename T, int M, int NT>
 __global__ void __launch_bounds__(128) combine_kernel(const SplitParams p) {
+    __shared__ float wsm[kCombineRows][kCombineMaxSplits];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.z, hk = blockIdx.y % p.Hkv, rt = blockIdx.y / p.Hkv;
     TileView tv;
     if (!tile_view<M, NT>(p, b, rt, tv, false)) return;
     if (tv.nsplit <= 1) return;
-    const int ns = tv.nsplit;
+    const int ns = min(tv.nsplit, kCombineMaxSplits);
+    const int r = blockIdx.x * kCombineRows + warp;
+    if (r >= tv.rows) return;
     T* out = static_cast<T*>(p.out);
-    for (int r = warp; r < tv.rows; r += 4) {
-        const int rho = tv.row0 + r;
-        const int i = rho / p.G, g = rho - i * p.G;
-        const int64_t t = tv.q0 + i;
-        const int h = hk * p.G + g;
-        const int64_t row = t * p.H + h;
-        float mx = -INFINITY;
-        for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, p.part_lse[(int64_t)s * p.part_stride + row]);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        const float m_use = (mx == -INFINITY) ? 0.f : mx;
-        float sum = 0.f;
-        for (int s = lane; s < ns; s += 32)
-            sum += fast_exp2((p.part_lse[(int64_t)s * p.part_stride + row] - m_use) * 1.4426950408889634f);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-        const float inv = sum > 0.f ? 1.f / sum : 0.f;
-        for (int d = lane * 2; d < p.D; d += 64) {
-            float a0 = 0.f, a1 = 0.f;
-            for (int s = 0; s < ns; ++s) {
-                const float w =
-                    fast_exp2((p.part_lse[(int64_t)s * p.part_stride + row] - m_use) * 1.4426950408889634f) * inv;
-                const float2 o = *reinterpret_cast<const float2*>(p.part_o + ((int64_t)s * p.part_stride + row) * p.D + d);
-                a0 += w * o.x;
-                a1 += w * o.y;
-            }
-            *reinterpret_cast<uint32_t*>(out + t * p.o_s0 + (int64_t)h * p.o_s1 + d) = pack2<T>(a0, a1);
-        }
-        if (lane == 0) p.lse[(int64_t)h * p.lse_s0 + t] = sum > 0.f ? m_use + logf(sum) : -INFINITY;
+    const int rho = tv.row0 + r;
+    const int i = rho / p.G, g = rho - i * p.G;
+    const int64_t t = tv.q0 + i;
+    const int h = hk * p.G + g;
+    const int64_t row = t * p.H + h;
+    float* w = wsm[warp];
+    float mx = -INFINITY;
+    for (int s = lane; s < ns; s += 32) {
+        const float l = p.part_lse[(int64_t)s * p.part_stride + row];
+        w[s] = l;
+        mx = fmaxf(mx, l);
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    const float m_use = (mx == -INFINITY) ? 0.f : mx;
+    float sum = 0.f;
+    for (int s = lane; s < ns; s += 32) {
+        const float e = fast_exp2((w[s] - m_use) * 1.4426950408889634f);
+        w[s] = e;
+        sum += e;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    __syncwarp();
+    const float inv = sum > 0.f ? 1.f / sum : 0.f;
+    const float* po = p.part_o + row * p.D;
+    const int64_t split_stride = p.part_stride * p.D;
+    for (int d = lane * 2; d < p.D; d += 64) {
+        float a0 = 0.f, a1 = 0.f;
+        for (int s = 0; s < ns; ++s) {
+            const float2 o = *reinterpret_cast<const float2*>(po + s * split_stride + d);
+            a0 = fmaf(w[s], o.x, a0);
+            a1 = fmaf(w[s], o.y, a1);
+        }
+        *reinterpret_cast<uint32_t*>(out + t * p.o_s0 + (int64_t)h * p.o_s1 + d) = pack2<T>(a0 * inv, a1 * inv);
+    }
+    if (lane == 0) p.lse[(int64_t)h * p.lse_s0 + t] = sum > 0.f ? m_use + logf(sum) : -INFINITY;
 }
 
 }  // namespace pa
