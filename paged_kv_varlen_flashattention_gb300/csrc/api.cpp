@@ -294,6 +294,31 @@ int workspace_for(cudaStream_t stream, size_t bytes, void** ptr) {
     return PA_OK;
 }
 
+// A second stream per device on which the tensor-core prefill kernel runs beside the
+// split-KV kernel (forked from and joined back to the caller's stream with events, so
+// stream ordering and graph capture behave as for a single launch).
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;  // also orders the fork/launch/join sequence of concurrent callers
+SideStream g_side[256];
+
+int side_stream(SideStream** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 256) return fail(PA_ERR_CUDA, "cudaGetDevice failed");
+    SideStream& ss = g_side[dev];
+    if (!ss.stream) {
+        if ((e = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming)) != cudaSuccess)
+            return fail(PA_ERR_CUDA, "creating the prefill side stream: %s", cudaGetErrorString(e));
+    }
+    *out = &ss;
+    return PA_OK;
+}
+
 // Scratch provider of pa_varlen_fwd: the library's own grow-only workspace.
 int library_workspace(void*, cudaStream_t stream, size_t bytes, void** ptr, char*, size_t) {
     return workspace_for(stream, bytes, ptr);
@@ -372,6 +397,7 @@ SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, int num_sms)
     pl.mt = rows_here <= 16 ? 1 : 2;
     const int M = 16 * pl.mt;
     pl.row_tiles = (int)((rows_here + M - 1) / M);
+    pl.tile_rows = (int)std::min<int64_t>(M, rows_here);
     // keys one row tile can touch: its queries span at most M / G + 1 positions
     int64_t kspan = a.max_sk;
     if (a.wl >= 0) kspan = std::min<int64_t>(kspan, (int64_t)a.wl + M / G + 1 + std::max(a.wr, 0) + 1);
@@ -442,12 +468,28 @@ int forward_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
         rc = scratch(scratch_ctx, a.stream, plan.ws_bytes, &ws, g_msg, sizeof g_msg);
         if (rc != PA_OK) return rc;
     }
-    if (use_prefill) {
-        rc = pa::launch_prefill(a, err, g_msg, sizeof g_msg);
+    if (!use_prefill) {
+        rc = pa::launch_splitkv(a, plan, ws, err, g_msg, sizeof g_msg);
         if (rc != PA_OK) return rc;
+        g_msg[0] = '\0';
+        return PA_OK;
     }
-    rc = pa::launch_splitkv(a, plan, ws, err, g_msg, sizeof g_msg);
+    // prefill-class sequences on the side stream, decode-class ones on the caller's stream
+    std::lock_guard<std::mutex> lock(g_side_mu);
+    SideStream* ss = nullptr;
+    if ((rc = side_stream(&ss)) != PA_OK) return rc;
+    cudaError_t e = cudaEventRecord(ss->fork, a.stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->stream, ss->fork, 0);
+    if (e != cudaSuccess) return fail(PA_ERR_CUDA, "forking the prefill stream: %s", cudaGetErrorString(e));
+    pa::Args ap = a;
+    ap.stream = ss->stream;
+    rc = pa::launch_prefill(ap, err, g_msg, sizeof g_msg);
+    if (rc == PA_OK) rc = pa::launch_splitkv(a, plan, ws, err, g_msg, sizeof g_msg);
+    // join even after a failed launch, so the caller's stream never runs ahead of the side stream
+    e = cudaEventRecord(ss->join, ss->stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(a.stream, ss->join, 0);
     if (rc != PA_OK) return rc;
+    if (e != cudaSuccess) return fail(PA_ERR_CUDA, "joining the prefill stream: %s", cudaGetErrorString(e));
     g_msg[0] = '\0';
     return PA_OK;
 }

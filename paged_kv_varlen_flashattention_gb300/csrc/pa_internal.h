@@ -58,6 +58,7 @@ struct SplitPlan {
     int nt;           // keys per tile (64 or 32)
     int row_tiles;    // row tiles per (sequence, kv head)
     int rows_cap;     // sequences with sq*G above this belong to the tensor-core prefill kernel
+    int tile_rows;    // most rows a row tile can hold: min(16 * mt, max_seqlen_q * G)
     int split_tiles;  // key tiles per split
     int max_splits;   // grid.x
     size_t ws_bytes;  // partial-result scratch needed (0 when max_splits == 1)

@@ -54,7 +54,7 @@ static int run_splitkv(const CUtensorMap& tk, const CUtensorMap& tv, const Split
     }
     count_launches(1);
     if (plan.max_splits > 1) {
-        dim3 g2((C::M + kCombineRows - 1) / kCombineRows, sp.Hkv * plan.row_tiles, sp.batch);
+        dim3 g2((plan.tile_rows + kCombineRows - 1) / kCombineRows, sp.Hkv * plan.row_tiles, sp.batch);
         combine_kernel<T, C::M, NT><<<g2, 128, 0, stream>>>(sp);
         e = cudaGetLastError();
         if (e != cudaSuccess) {
@@ -105,7 +105,7 @@ static int run_decode(const CUtensorMap& tk, const CUtensorMap& tv, const SplitP
     }
     count_launches(1);
     if (plan.max_splits > 1) {
-        dim3 g2((C::M + kCombineRows - 1) / kCombineRows, sp.Hkv, sp.batch);
+        dim3 g2((plan.tile_rows + kCombineRows - 1) / kCombineRows, sp.Hkv, sp.batch);
         combine_kernel<T, C::M, NT><<<g2, 128, 0, stream>>>(sp);
         e = cudaGetLastError();
         if (e != cudaSuccess) {
