@@ -8,10 +8,10 @@
 //               128 keys per tile through the block table (one box per page piece; the
 //               paged layout of "flash-attn-varlen paged expects k/v tensors of rank 4",
 //               What it means), each blocking on its own ring's empty barriers
-//   warp 1      tensor-memory owner and MMA issuer (one elected lane):
+//   warps 1, 3  MMA issuers for tiles A and B (one elected lane each; warp 1 also owns the
+//               tensor memory):
 //               S_X = Q_X K_j^T  (tcgen05.mma, A and B from shared memory, S in TMEM)
 //               O_X += P_X V_j   (tcgen05.mma, A = P from TMEM, B = V from shared memory)
-//   warp 3      idle (it completes warpgroup 0 for the register split)
 //   warps 4..7  softmax of tile A, warps 8..11 softmax of tile B: thread r owns row r
 //               (TMEM lane r); reads S from TMEM, masks, keeps the running max and sum,
 //               writes P (16-bit) over the columns of S it came from, and rescales O in
@@ -36,7 +36,7 @@ namespace {
 
 constexpr int kPrefillThreads = 384;  // three warpgroups
 // Register split (setmaxnreg): the launch gives 384 x 168; warpgroup 0 (producer, MMA
-// issuer, V producer, one idle warp) drops to 72 and the two softmax warpgroups rise to 216:
+// issuers, V producer) drops to 72 and the two softmax warpgroups rise to 216:
 // 128 x 72 + 256 x 216 = 64,512, the launch total.
 constexpr int kRegsControl = 72, kRegsSoftmax = 216;
 #ifndef PA_POLY_EVERY
@@ -81,8 +81,8 @@ struct PfCfg {
     static constexpr int OFF_K = 2 * Q_TILE;
     static constexpr int OFF_V = OFF_K + KS * KV_TILE;
     static constexpr int OFF_BAR = OFF_V + VS * KV_TILE;
-    // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2], p_full[2], pv_done[2], drain
-    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 7;
+    // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2], p_full[2], pv_done[2], drain[2]
+    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 8;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag, picked pair
     static constexpr int OFF_IDS = OFF_MISC + 16;         // block id of every TMA box of the CTA
     static constexpr int MAX_BOXES = 256;
@@ -157,25 +157,26 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     uint64_t* s_full = v_empty + C::VS;  // [tile]
     uint64_t* p_full = s_full + 2;       // [tile]
     uint64_t* pv_done = p_full + 2;      // [tile]: the tile's last P.V has completed
-    uint64_t* drain = pv_done + 2;
+    uint64_t* drain = pv_done + 2;       // [issuer]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile uint32_t* abort_flag = tmem_slot + 1;
     if (tid == 64) {
         mbar_init(q_full, 1);
         for (int s = 0; s < C::KS; ++s) {
             mbar_init(&k_full[s], 1);
-            mbar_init(&k_empty[s], 1);
+            mbar_init(&k_empty[s], 2);  // one commit per MMA issuer
         }
         for (int s = 0; s < C::VS; ++s) {
             mbar_init(&v_full[s], 1);
-            mbar_init(&v_empty[s], 1);
+            mbar_init(&v_empty[s], 2);
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(&s_full[x], 1);
             mbar_init(&p_full[x], 4);  // one arrive per softmax warp
             mbar_init(&pv_done[x], 1);
         }
-        mbar_init(drain, 1);
+        mbar_init(&drain[0], 1);
+        mbar_init(&drain[1], 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -328,98 +329,81 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 issue_kv_tile(p, map, ring + s * C::KV_TILE, &fullb[s], tile, jt, hk, kb, k0, C::CH);
             }
         }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
+    } else if (warp == 1 || warp == 3) {
+        // ---------------- MMA issuers: warp 1 for tile A, warp 3 for tile B ----------------
+        // A tcgen05.mma costs its issuing thread ~50 cycles, close to the 64 cycles a
+        // 128x128x16 product takes; two issuers keep the pipe fed while each also waits on
+        // its tile's barriers.  Per issuer the order is S_x(0), PV_x(0), S_x(1), PV_x(1), ...
+        // so S_x(j+1) overwrites the P_x(j) columns only after PV_x(j) (in-order per thread).
         constexpr uint32_t IDESC_S = tc::idesc_f16(128, 128, kBF16, false, false);
         constexpr uint32_t IDESC_O = tc::idesc_f16(128, DP, kBF16, false, true);
-        const int nx = has_b ? 2 : 1;
+        const int x = warp == 1 ? 0 : 1;
+        const bool active = x == 0 || has_b;  // without tile B, warp 3 only releases the stages
         // Shared-memory descriptors are built once; the start-address field (address / 16,
         // bits 0..13) then advances by a compile-time constant per MMA.
-        const uint64_t dq0 = tc::smem_desc_sw128(smem_addr(smem + C::OFF_Q), 16, 1024);
+        const uint64_t da = tc::smem_desc_sw128(smem_addr(smem + C::OFF_Q + x * C::Q_TILE), 16, 1024);
         const uint64_t dk0 = tc::smem_desc_sw128(smem_addr(smem + C::OFF_K), 16, 1024);
         const uint64_t dv0 = tc::smem_desc_sw128(smem_addr(smem + C::OFF_V), 128 * 128, 1024);
-        // S_x = Q_x K_j^T into S buffer x
-        auto issue_s = [&](int x, int j) {
-            if (lane == 0) {
-                const uint64_t da = dq0 + (uint64_t)(x * (C::Q_TILE >> 4));
-                const uint64_t db = dk0 + (uint64_t)((j % C::KS) * (C::KV_TILE >> 4));
-                const uint32_t d = tmem + (x ? C::T_S1 : C::T_S0);
-#pragma unroll
-                for (int kk = 0; kk < DP / 16; ++kk) {
-                    const uint64_t off = (uint64_t)((kk >> 2) * (128 * 128 / 16) + (kk & 3) * 2);
-                    tc::mma_ss(d, da + off, db + off, IDESC_S, kk > 0 ? 1u : 0u);
-                }
-                tc::commit(&s_full[x]);
-            }
-        };
-        // O_x += P_x V_j, P_x read from the columns of S buffer x
-        auto issue_pv = [&](int x, int j) {
-            if (lane == 0) {
-                const uint64_t db = dv0 + (uint64_t)((j % C::VS) * (C::KV_TILE >> 4));
-                const uint32_t pt = tmem + (x ? C::T_S1 : C::T_S0);
-                const uint32_t d = tmem + (x ? C::T_O1 : C::T_O0);
-                const uint32_t first = j > 0 ? 1u : 0u;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    tc::mma_ts(d, pt + kk * 8, db + (uint64_t)(kk * (2048 / 16)), IDESC_O, kk > 0 ? 1u : first);
-            }
-        };
-        auto wait_k = [&](int j) {
-            const bool r = __all_sync(0xffffffffu, wait_bar(&k_full[j % C::KS], (j / C::KS) & 1, abort_flag,
-                                                             p.err, p.wait_ns));
+        const uint32_t d_s = tmem + (x ? C::T_S1 : C::T_S0);
+        const uint32_t d_o = tmem + (x ? C::T_O1 : C::T_O0);
+        auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+            const bool r = __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, p.err, p.wait_ns));
             tc::fence_after_sync();
             return r;
         };
-        // Tensor-pipe order: S_A(0), S_B(0), then for each tile j:
-        //   PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
-        // S_x(j+1) overwrites the P_x(j) columns only after PV_x(j) in pipe order.
-        bool ok = __all_sync(0xffffffffu, wait_bar(q_full, 0, abort_flag, p.err, p.wait_ns));
-        if (ok) ok = wait_k(0);
-        if (ok) {
-            for (int x = 0; x < nx; ++x) issue_s(x, 0);
-            if (lane == 0) tc::commit(&k_empty[0]);
+        bool ok = !active || wait_all(q_full, 0);
+        for (int j = 0; ok && j < n_tiles; ++j) {
+            // S_x(j) = Q_x K_j^T
+            if (!(ok = wait_all(&k_full[j % C::KS], (j / C::KS) & 1))) break;
+            if (lane == 0) {
+                if (active) {
+                    const uint64_t db = dk0 + (uint64_t)((j % C::KS) * (C::KV_TILE >> 4));
+#pragma unroll
+                    for (int kk = 0; kk < DP / 16; ++kk) {
+                        const uint64_t off = (uint64_t)((kk >> 2) * (128 * 128 / 16) + (kk & 3) * 2);
+                        tc::mma_ss(d_s, da + off, db + off, IDESC_S, kk > 0 ? 1u : 0u);
+                    }
+                    tc::commit(&s_full[x]);
+                }
+                tc::commit(&k_empty[j % C::KS]);
+            }
+            __syncwarp();
+            // O_x += P_x(j) V_j, P_x read from the columns of S buffer x
+            if (active && !(ok = wait_all(&p_full[x], j & 1))) break;
+            if (!(ok = wait_all(&v_full[j % C::VS], (j / C::VS) & 1))) break;
+            if (active) {
+                uint8_t* vst = smem + C::OFF_V + (j % C::VS) * C::KV_TILE;
+                const int valid = min(128, sk - (kt0 + j * 128));
+                if (valid < 128) {  // keys at or past sk: zero V rows so P = 0 never meets NaN
+                    // (both issuers write the same zeros; each orders its own writes before its MMAs)
+                    const int zr = 128 - valid;
+                    for (int idx = lane; idx < C::CH * zr * 8; idx += 32) {
+                        const int c = idx / (zr * 8), rem = idx - c * zr * 8;
+                        *reinterpret_cast<int4*>(vst + (c * 128 + valid + (rem >> 3)) * 128 + ((rem & 7) << 4)) =
+                            make_int4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    tc::fence_after_sync();
+                }
+            }
+            if (lane == 0) {
+                if (active) {
+                    const uint64_t db = dv0 + (uint64_t)((j % C::VS) * (C::KV_TILE >> 4));
+                    const uint32_t first = j > 0 ? 1u : 0u;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc::mma_ts(d_o, d_s + kk * 8, db + (uint64_t)(kk * (2048 / 16)), IDESC_O, kk > 0 ? 1u : first);
+                    if (j + 1 == n_tiles) tc::commit(&pv_done[x]);
+                }
+                tc::commit(&v_empty[j % C::VS]);
+            }
             __syncwarp();
         }
-        for (int j = 0; ok && j < n_tiles; ++j) {
-            const bool more = j + 1 < n_tiles;
-            for (int x = 0; ok && x < nx; ++x) {
-                ok = __all_sync(0xffffffffu, wait_bar(&p_full[x], j & 1, abort_flag, p.err, p.wait_ns));
-                if (!ok) break;
-                if (x == 0) {
-                    ok = __all_sync(0xffffffffu, wait_bar(&v_full[j % C::VS], (j / C::VS) & 1, abort_flag,
-                                                          p.err, p.wait_ns));
-                    if (!ok) break;
-                    uint8_t* vst = smem + C::OFF_V + (j % C::VS) * C::KV_TILE;
-                    const int valid = min(128, sk - (kt0 + j * 128));
-                    if (valid < 128) {  // keys at or past sk: zero V rows so P = 0 never meets NaN
-                        const int zr = 128 - valid;
-                        for (int idx = lane; idx < C::CH * zr * 8; idx += 32) {
-                            const int c = idx / (zr * 8), rem = idx - c * zr * 8;
-                            *reinterpret_cast<int4*>(vst + (c * 128 + valid + (rem >> 3)) * 128 + ((rem & 7) << 4)) =
-                                make_int4(0, 0, 0, 0);
-                        }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                    }
-                }
-                tc::fence_after_sync();
-                issue_pv(x, j);
-                if (lane == 0) {
-                    if (x == nx - 1) tc::commit(&v_empty[j % C::VS]);
-                    if (!more) tc::commit(&pv_done[x]);
-                }
-                if (more) {
-                    if (x == 0 && !(ok = wait_k(j + 1))) break;
-                    issue_s(x, j + 1);
-                    if (lane == 0 && x == nx - 1) tc::commit(&k_empty[(j + 1) % C::KS]);
-                }
-                __syncwarp();
-            }
-        }
-        // every MMA issued above has completed before tensor memory is released
+        // every MMA this issuer started has completed before tensor memory is released
         if (lane == 0) {
-            tc::commit(drain);
-            mbar_wait(drain, 0, p.wait_ns);  // not cut short by an abort: MMAs may be in flight
+            tc::commit(&drain[x]);
+            mbar_wait(&drain[x], 0, p.wait_ns);  // not cut short by an abort: MMAs may be in flight
         }
         __syncwarp();
     }
