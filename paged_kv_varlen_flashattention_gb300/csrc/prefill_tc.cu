@@ -81,8 +81,9 @@ struct PfCfg {
     static constexpr int OFF_K = 2 * Q_TILE;
     static constexpr int OFF_V = OFF_K + KS * KV_TILE;
     static constexpr int OFF_BAR = OFF_V + VS * KV_TILE;
-    // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2], p_full[2], pv_done[2], drain[2]
-    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 8;
+    // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2], p_full[2], pv_done[2],
+    // drain[2], turn[2]
+    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 10;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag, picked pair
     static constexpr int OFF_IDS = OFF_MISC + 16;         // block id of every TMA box of the CTA
     static constexpr int MAX_BOXES = 256;
@@ -158,6 +159,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     uint64_t* p_full = s_full + 2;       // [tile]
     uint64_t* pv_done = p_full + 2;      // [tile]: the tile's last P.V has completed
     uint64_t* drain = pv_done + 2;       // [issuer]
+    uint64_t* turn = drain + 2;          // [tile]: the other tile's softmax finished its step
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile uint32_t* abort_flag = tmem_slot + 1;
     if (tid == 64) {
@@ -177,6 +179,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
         mbar_init(&drain[0], 1);
         mbar_init(&drain[1], 1);
+        mbar_init(&turn[0], 4);  // one arrive per softmax warp of the other tile
+        mbar_init(&turn[1], 4);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -432,6 +436,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             const int kt = kt0 + j * 128;
             ok = __all_sync(0xffffffffu, wait_bar(&s_full[x], j & 1, abort_flag, p.err, p.wait_ns));
             if (!ok) break;
+            // The two softmax warpgroups take turns (A runs step j, then B runs step j, then A
+            // runs step j + 1, ...): each one's tensor-core products then run under the
+            // other's softmax instead of both idling the pipe at once.
+            if (has_b && (x == 1 || j > 0)) {
+                ok = __all_sync(0xffffffffu, wait_bar(&turn[x], (x == 1 ? j : j - 1) & 1, abort_flag, p.err, p.wait_ns));
+                if (!ok) break;
+            }
             tc::fence_after_sync();
             float sv[128];
             tc::ld_32cols(s_col + 0, *reinterpret_cast<float(*)[32]>(&sv[0]));
@@ -500,7 +511,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             tc::wait_st();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[x]);
+            if (lane == 0) {
+                mbar_arrive(&p_full[x]);
+                if (has_b) mbar_arrive(&turn[x ^ 1]);
+            }
         }
         if (ok) ok = __all_sync(0xffffffffu, wait_bar(&pv_done[x], 0, abort_flag, p.err, p.wait_ns));
         if (ok) {
