@@ -355,25 +355,28 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             tc::fence_after_sync();
             return r;
         };
-        bool ok = !active || wait_all(q_full, 0);
-        for (int j = 0; ok && j < n_tiles; ++j) {
-            // S_x(j) = Q_x K_j^T
-            if (!(ok = wait_all(&k_full[j % C::KS], (j / C::KS) & 1))) break;
-            if (lane == 0) {
-                if (active) {
-                    const uint64_t db = dk0 + (uint64_t)((j % C::KS) * (C::KV_TILE >> 4));
+        // S_x(j) = Q_x K_j^T into S buffer x; releases K stage j once complete
+        auto issue_s = [&](int j) {
+            if (active) {
+                const uint64_t db = dk0 + (uint64_t)((j % C::KS) * (C::KV_TILE >> 4));
 #pragma unroll
-                    for (int kk = 0; kk < DP / 16; ++kk) {
-                        const uint64_t off = (uint64_t)((kk >> 2) * (128 * 128 / 16) + (kk & 3) * 2);
-                        tc::mma_ss(d_s, da + off, db + off, IDESC_S, kk > 0 ? 1u : 0u);
-                    }
-                    tc::commit(&s_full[x]);
+                for (int kk = 0; kk < DP / 16; ++kk) {
+                    const uint64_t off = (uint64_t)((kk >> 2) * (128 * 128 / 16) + (kk & 3) * 2);
+                    tc::mma_ss(d_s, da + off, db + off, IDESC_S, kk > 0 ? 1u : 0u);
                 }
-                tc::commit(&k_empty[j % C::KS]);
+                tc::commit(&s_full[x]);
             }
+            tc::commit(&k_empty[j % C::KS]);
+        };
+        bool ok = !active || wait_all(q_full, 0);
+        if (ok && n_tiles > 0 && (ok = wait_all(&k_full[0], 0))) {
+            if (lane == 0) issue_s(0);
             __syncwarp();
-            // O_x += P_x(j) V_j, P_x read from the columns of S buffer x
-            if (active && !(ok = wait_all(&p_full[x], j & 1))) break;
+        }
+        for (int j = 0; ok && j < n_tiles; ++j) {
+            // Everything that does not depend on P_x(j) is settled first (V_j and K_{j+1}
+            // resident, V_j's rows past the last key zeroed), so that once the softmax hands
+            // over P_x(j), PV_x(j) and S_x(j+1) issue back to back.
             if (!(ok = wait_all(&v_full[j % C::VS], (j / C::VS) & 1))) break;
             if (active) {
                 uint8_t* vst = smem + C::OFF_V + (j % C::VS) * C::KV_TILE;
@@ -391,6 +394,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     tc::fence_after_sync();
                 }
             }
+            const bool more = j + 1 < n_tiles;
+            if (more && !(ok = wait_all(&k_full[(j + 1) % C::KS], ((j + 1) / C::KS) & 1))) break;
+            // O_x += P_x(j) V_j, P_x read from the columns of S buffer x
+            if (active && !(ok = wait_all(&p_full[x], j & 1))) break;
             if (lane == 0) {
                 if (active) {
                     const uint64_t db = dv0 + (uint64_t)((j % C::VS) * (C::KV_TILE >> 4));
@@ -401,6 +408,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     if (j + 1 == n_tiles) tc::commit(&pv_done[x]);
                 }
                 tc::commit(&v_empty[j % C::VS]);
+                if (more) issue_s(j + 1);
             }
             __syncwarp();
         }
