@@ -12,12 +12,12 @@
 //               tensor memory):
 //               S_X = Q_X K_j^T  (tcgen05.mma, A and B from shared memory, S in TMEM)
 //               O_X += P_X V_j   (tcgen05.mma, A = P from TMEM, B = V from shared memory)
-//   warps 4..7  softmax of tile A, warps 8..11 softmax of tile B: thread r owns row r
-//               (TMEM lane r); reads S from TMEM, masks, keeps the running max and sum,
-//               writes P (16-bit) over the columns of S it came from, and rescales O in
-//               TMEM only when the running max grew by more than 2^8 (otherwise the stale
-//               max stays: exact after the final division).
-// The two tiles ping-pong: while one warpgroup runs its softmax, the tensor pipe runs the
+//   warps 4..11 softmax, all eight on tile A and then on tile B at every key tile: each
+//               warp owns 16 rows (TMEM lanes), four threads per row; reads S from TMEM,
+//               masks, keeps the running max and sum, writes P (16-bit) over the columns of
+//               S it came from, and rescales O in TMEM only when the running max grew by
+//               more than 2^8 (otherwise the stale max stays: exact after the final division).
+// The two tiles ping-pong: while the softmax works on one tile, the tensor pipe runs the
 // other tile's P.V and next Q.K^T.  TMEM columns: S_A [0,128), S_B [128,256),
 // O_A [256, 256+DP), O_B [256+DP, 256+2 DP).
 //
@@ -82,8 +82,8 @@ struct PfCfg {
     static constexpr int OFF_V = OFF_K + KS * KV_TILE;
     static constexpr int OFF_BAR = OFF_V + VS * KV_TILE;
     // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2], p_full[2], pv_done[2],
-    // drain[2], turn[2]
-    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 10;
+    // drain[2]
+    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 8;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag, picked pair
     static constexpr int OFF_IDS = OFF_MISC + 16;         // block id of every TMA box of the CTA
     static constexpr int MAX_BOXES = 256;
@@ -159,7 +159,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     uint64_t* p_full = s_full + 2;       // [tile]
     uint64_t* pv_done = p_full + 2;      // [tile]: the tile's last P.V has completed
     uint64_t* drain = pv_done + 2;       // [issuer]
-    uint64_t* turn = drain + 2;          // [tile]: the other tile's softmax finished its step
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile uint32_t* abort_flag = tmem_slot + 1;
     if (tid == 64) {
@@ -174,13 +173,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(&s_full[x], 1);
-            mbar_init(&p_full[x], 4);  // one arrive per softmax warp
+            mbar_init(&p_full[x], 8);  // one arrive per softmax warp
             mbar_init(&pv_done[x], 1);
         }
         mbar_init(&drain[0], 1);
         mbar_init(&drain[1], 1);
-        mbar_init(&turn[0], 4);  // one arrive per softmax warp of the other tile
-        mbar_init(&turn[1], 4);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -421,140 +418,176 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     }
     } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-    if (warp < 8 || has_b) {
-        // ---------------- softmax warpgroups ----------------
-        const int x = (warp - 4) >> 2;  // 0: tile A (warps 4..7), 1: tile B (warps 8..11)
-        const int wq = warp & 3;
-        const int r = wq * 32 + lane;
-        const int64_t rho = row0 + x * 128 + r;
-        const bool row_valid = rho < rows_total;
-        const int i = (int)(rho / p.G), g = (int)(rho - (int64_t)i * p.G);
-        int lo_r = 0, hi_r = -1;
-        if (row_valid) {
-            const int64_t diag = i + cdiag;
-            lo_r = p.wl >= 0 ? (int)max64(0, diag - p.wl) : 0;
-            hi_r = p.wr >= 0 ? (int)max64(-1, min64((int64_t)sk - 1, diag + p.wr)) : sk - 1;
-        }
-        const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-        const uint32_t s_col = tmem + lane_base + (x ? C::T_S1 : C::T_S0);
-        const uint32_t o_col = tmem + lane_base + (x ? C::T_O1 : C::T_O0);
-        float m_run = -INFINITY, l_run = 0.f;
-        bool ok = true;
-        for (int j = 0; j < n_tiles; ++j) {
-            const int kt = kt0 + j * 128;
-            ok = __all_sync(0xffffffffu, wait_bar(&s_full[x], j & 1, abort_flag, p.err, p.wait_ns));
-            if (!ok) break;
-            // The two softmax warpgroups take turns (A runs step j, then B runs step j, then A
-            // runs step j + 1, ...): each one's tensor-core products then run under the
-            // other's softmax instead of both idling the pipe at once.
-            if (has_b && (x == 1 || j > 0)) {
-                ok = __all_sync(0xffffffffu, wait_bar(&turn[x], (x == 1 ? j : j - 1) & 1, abort_flag, p.err, p.wait_ns));
-                if (!ok) break;
-            }
-            tc::fence_after_sync();
-            float sv[128];
-            tc::ld_32cols(s_col + 0, *reinterpret_cast<float(*)[32]>(&sv[0]));
-            tc::ld_32cols(s_col + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
-            tc::ld_32cols(s_col + 64, *reinterpret_cast<float(*)[32]>(&sv[64]));
-            tc::ld_32cols(s_col + 96, *reinterpret_cast<float(*)[32]>(&sv[96]));
-            tc::wait_ld();
-            if (!(kt >= lo_r && kt + 127 <= hi_r)) {
+    {
+        // ---------------- softmax: warps 4..11, tile A then tile B at every key tile ----------------
+        // Warp w reaches TMEM lanes 32 (w % 4) .. +31 and takes the half hh = (w - 4) / 4 of
+        // them: lanes lb .. lb + 15 with lb = 32 (w % 4) + 16 hh.  Thread t holds rows
+        // lb + t/4 (q = 0) and lb + t/4 + 8 (q = 1) of each tile; the four threads of a quad
+        // split a row's 128 keys (keys 8k + 2 (t % 4) + {0, 1}, k = 0..15), so row maxima and
+        // sums are quad reductions and P lands in the columns its own thread read S from.
+        const int lg = warp & 3, hh = (warp - 4) >> 2;
+        const int gid = lane >> 2, tig = lane & 3;
+        const int lb = lg * 32 + hh * 16;
+        const uint32_t lane_addr = (uint32_t)lb << 16;
+        struct TileRows {
+            int lo[2], hi[2];  // attended key range of each row (empty for padding rows)
+            float m[2], l[2];  // running max (log2 domain) and this thread's share of the sum
+        };
+        auto init_rows = [&](int x, TileRows& st) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    const int key = kt + c;
-                    sv[c] = (key >= lo_r && key <= hi_r) ? sv[c] : -INFINITY;
+            for (int q = 0; q < 2; ++q) {
+                const int64_t rho = row0 + x * 128 + lb + gid + 8 * q;
+                st.lo[q] = 0;
+                st.hi[q] = -1;
+                if (rho < rows_total) {
+                    const int64_t diag = rho / p.G + cdiag;
+                    st.lo[q] = p.wl >= 0 ? (int)max64(0, diag - p.wl) : 0;
+                    st.hi[q] = p.wr >= 0 ? (int)max64(-1, min64((int64_t)sk - 1, diag + p.wr)) : sk - 1;
                 }
+                st.m[q] = -INFINITY;
+                st.l[q] = 0.f;
             }
-            // row maximum: four independent chains of three-input max
-            float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
+        };
+        TileRows rows_a, rows_b;
+        init_rows(0, rows_a);
+        init_rows(1, rows_b);
+
+        // One key tile of one query tile: S -> running max -> (rare) O rescale -> P.
+        auto step = [&](int x, TileRows& st, int j) -> bool {
+            const int kt = kt0 + j * 128;
+            if (!__all_sync(0xffffffffu, wait_bar(&s_full[x], j & 1, abort_flag, p.err, p.wait_ns))) return false;
+            tc::fence_after_sync();
+            const uint32_t s_addr = tmem + lane_addr + (x ? C::T_S1 : C::T_S0);
+            const uint32_t o_addr = tmem + lane_addr + (x ? C::T_O1 : C::T_O0);
+            // sv[4k + 2q + e] = S[row q][key 8k + 2 tig + e]
+            float sv[64];
+            tc::ld_16x256b_x8(s_addr, *reinterpret_cast<float(*)[32]>(&sv[0]));
+            tc::ld_16x256b_x8(s_addr + 64, *reinterpret_cast<float(*)[32]>(&sv[32]));
+            tc::wait_ld();
+            if (!(kt >= max(st.lo[0], st.lo[1]) && kt + 127 <= min(st.hi[0], st.hi[1]))) {
 #pragma unroll
-            for (int c = 4; c < 128; c += 8) {
-                mx0 = max3f(mx0, sv[c], sv[c + 1]);
-                mx1 = max3f(mx1, sv[c + 2], sv[c + 3]);
-                mx2 = max3f(mx2, sv[c + 4], sv[c + 5]);
-                mx3 = max3f(mx3, sv[c + 6], sv[c + 7]);
+                for (int k = 0; k < 16; ++k)
+#pragma unroll
+                    for (int q = 0; q < 2; ++q)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int key = kt + 8 * k + 2 * tig + e;
+                            float& v = sv[4 * k + 2 * q + e];
+                            v = (key >= st.lo[q] && key <= st.hi[q]) ? v : -INFINITY;
+                        }
             }
-            const float mx = max3f(mx0, mx1, fmaxf(mx2, mx3));
-            const float m_cand = mx * p.scale_log2;  // softmax_scale > 0 on this path
-            float alpha = 1.f;
+            float alpha[2];
             bool resc = false;
-            if (m_cand > m_run + 8.f) {
-                alpha = fast_exp2(m_run - m_cand);
-                m_run = m_cand;
-                resc = true;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                float c0 = fmaxf(sv[2 * q], sv[2 * q + 1]), c1 = fmaxf(sv[4 + 2 * q], sv[5 + 2 * q]);
+#pragma unroll
+                for (int k = 2; k < 16; k += 2) {
+                    c0 = max3f(c0, sv[4 * k + 2 * q], sv[4 * k + 2 * q + 1]);
+                    c1 = max3f(c1, sv[4 * k + 4 + 2 * q], sv[4 * k + 5 + 2 * q]);
+                }
+                float mx = fmaxf(c0, c1);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                const float m_cand = mx * p.scale_log2;  // softmax_scale > 0 on this path
+                alpha[q] = 1.f;
+                if (m_cand > st.m[q] + 8.f) {
+                    alpha[q] = fast_exp2(st.m[q] - m_cand);
+                    st.m[q] = m_cand;
+                    resc = true;
+                }
             }
             // O_x was accumulated with the old maximum.  Its last P.V (PV_x(j-1)) precedes
             // S_x(j) in the tensor pipe, so it is complete once S_x(j) is.
             if (j > 0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
-                for (int cc = 0; cc < DP / 32; ++cc) {
+                for (int cc = 0; cc < DP / 64; ++cc) {
                     float o[32];
-                    tc::ld_32cols(o_col + cc * 32, o);
+                    tc::ld_16x256b_x8(o_addr + cc * 64, o);
                     tc::wait_ld();
                     uint32_t ob[32];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) ob[e] = __float_as_uint(o[e] * alpha);
-                    tc::st_32cols(o_col + cc * 32, ob);
+                    for (int e = 0; e < 32; ++e) ob[e] = __float_as_uint(o[e] * alpha[(e >> 1) & 1]);
+                    tc::st_16x256b_x8(o_addr + cc * 64, ob);
                 }
             }
-            const float m_use = m_run == -INFINITY ? 0.f : m_run;
-            const float sl = p.scale_log2, nm = -m_use;
-            float sums[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            uint32_t pk[64];
+            const float sl = p.scale_log2;
+            float nm[2];
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                float x0, x1;
-                ffma2(x0, x1, sv[2 * c], sv[2 * c + 1], sl, sl, nm, nm);  // scores -> log2 domain
-                const bool on_fma = kPolyEvery > 0 && (c % (kPolyEvery > 0 ? kPolyEvery : 1)) == kPolyEvery - 1;
-                const float p0 = on_fma ? poly_exp2(x0) : fast_exp2(x0);
-                const float p1 = on_fma ? poly_exp2(x1) : fast_exp2(x1);
-                fadd2_acc(sums[2 * (c & 3)], sums[2 * (c & 3) + 1], p0, p1);
-                pk[c] = pack2<T>(p0, p1);
-            }
-            const float sum = ((sums[0] + sums[1]) + (sums[2] + sums[3])) + ((sums[4] + sums[5]) + (sums[6] + sums[7]));
-            l_run = l_run * alpha + sum;
-            // P overwrites the first 64 columns of the S it came from
-            tc::st_32cols(s_col, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-            tc::st_32cols(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+            for (int q = 0; q < 2; ++q) nm[q] = st.m[q] == -INFINITY ? 0.f : -st.m[q];
+            float sums[4] = {0.f, 0.f, 0.f, 0.f};
+            // pk[2k + q] = P[row q][packed column 4k + tig] = (keys 8k + 2 tig, 8k + 2 tig + 1),
+            // the register order of the 16x128b store
+            uint32_t pk[32];
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    float x0, x1;
+                    ffma2(x0, x1, sv[4 * k + 2 * q], sv[4 * k + 2 * q + 1], sl, sl, nm[q], nm[q]);
+                    const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                    fadd2_acc(sums[2 * q], sums[2 * q + 1], p0, p1);
+                    pk[2 * k + q] = pack2<T>(p0, p1);
+                }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) st.l[q] = st.l[q] * alpha[q] + (sums[2 * q] + sums[2 * q + 1]);
+            // P overwrites the first 64 columns of the S it came from (this thread's own cells)
+            tc::st_16x128b_x16(s_addr, pk);
             tc::wait_st();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&p_full[x]);
-                if (has_b) mbar_arrive(&turn[x ^ 1]);
-            }
-        }
-        if (ok) ok = __all_sync(0xffffffffu, wait_bar(&pv_done[x], 0, abort_flag, p.err, p.wait_ns));
-        if (ok) {
+            if (lane == 0) mbar_arrive(&p_full[x]);
+            return true;
+        };
+
+        auto epilogue = [&](int x, TileRows& st) -> bool {
+            if (!__all_sync(0xffffffffu, wait_bar(&pv_done[x], 0, abort_flag, p.err, p.wait_ns))) return false;
             tc::fence_after_sync();
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-            const int64_t t = q0 + i;
-            const int h = hk * p.G + g;
-            T* orow = out + t * p.o_s0 + (int64_t)h * p.o_s1;
-#pragma unroll 1
-            for (int cc = 0; cc < DP / 32; ++cc) {
-                float o[32];
-                tc::ld_32cols(o_col + cc * 32, o);
-                tc::wait_ld();
-                if (row_valid) {
+            const uint32_t o_addr = tmem + lane_addr + (x ? C::T_O1 : C::T_O0);
+            float inv[2];
+            T* orow[2];
+            bool valid[2];
 #pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        const int d = cc * 32 + e;
-                        if (d < p.D) {
-                            int4 v;
-                            v.x = (int)pack2<T>(o[e] * inv, o[e + 1] * inv);
-                            v.y = (int)pack2<T>(o[e + 2] * inv, o[e + 3] * inv);
-                            v.z = (int)pack2<T>(o[e + 4] * inv, o[e + 5] * inv);
-                            v.w = (int)pack2<T>(o[e + 6] * inv, o[e + 7] * inv);
-                            *reinterpret_cast<int4*>(orow + d) = v;
-                        }
-                    }
+            for (int q = 0; q < 2; ++q) {
+                float l = st.l[q];
+                l += __shfl_xor_sync(0xffffffffu, l, 1);
+                l += __shfl_xor_sync(0xffffffffu, l, 2);
+                inv[q] = l > 0.f ? 1.f / l : 0.f;
+                const int64_t rho = row0 + x * 128 + lb + gid + 8 * q;
+                valid[q] = rho < rows_total;
+                const int i = (int)(rho / p.G), g = (int)(rho - (int64_t)i * p.G);
+                const int64_t t = q0 + i;
+                const int h = hk * p.G + g;
+                orow[q] = out + t * p.o_s0 + (int64_t)h * p.o_s1;
+                if (valid[q] && tig == 0)
+                    p.lse[(int64_t)h * p.lse_s0 + t] =
+                        l > 0.f ? (st.m[q] + log2f(l)) * 0.69314718055994531f : -INFINITY;
+            }
+#pragma unroll 1
+            for (int cc = 0; cc < DP / 64; ++cc) {
+                float o[32];
+                tc::ld_16x256b_x8(o_addr + cc * 64, o);
+                tc::wait_ld();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int d = cc * 64 + 8 * k + 2 * tig;
+#pragma unroll
+                    for (int q = 0; q < 2; ++q)
+                        if (valid[q] && d < p.D)
+                            *reinterpret_cast<uint32_t*>(orow[q] + d) =
+                                pack2<T>(o[4 * k + 2 * q] * inv[q], o[4 * k + 2 * q + 1] * inv[q]);
                 }
             }
-            if (row_valid)
-                p.lse[(int64_t)h * p.lse_s0 + t] =
-                    l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+            return true;
+        };
+
+        bool ok = true;
+        for (int j = 0; ok && j < n_tiles; ++j) {
+            ok = step(0, rows_a, j);
+            if (ok && has_b) ok = step(1, rows_b, j);
         }
+        if (ok) ok = epilogue(0, rows_a);
+        if (ok && has_b) epilogue(1, rows_b);
         tc::fence_before_sync();
     }
     }

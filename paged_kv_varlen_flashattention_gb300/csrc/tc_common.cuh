@@ -114,6 +114,49 @@ __device__ __forceinline__ void st_32cols(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
+// 16-lane shapes (a warp reaches 16 lanes starting at the lane field of `taddr`, inside its
+// own 32-lane group).  Thread t holds lanes base + t/4 and base + t/4 + 8:
+//   16x256b: per 8-column repetition k, registers 4k..4k+3 are (lane t/4, columns 8k + 2(t%4)
+//            and +1), then (lane t/4 + 8, the same two columns);
+//   16x128b: per 4-column repetition k, registers 2k, 2k+1 are (lane t/4, column 4k + t%4) and
+//            (lane t/4 + 8, the same column).
+#define PA_R32(r)                                                                                            \
+    "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),       \
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),       \
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),      \
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+#define PA_W32(r)                                                                                            \
+    "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),          \
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), \
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),          \
+        "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),          \
+        "=r"(r[30]), "=r"(r[31])
+#define PA_OPS32                                                                                  \
+    "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, " \
+    "%20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}"
+#define PA_OPS32_FROM1                                                                               \
+    "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, " \
+    "%21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32}"
+
+// 16 lanes x 64 columns
+__device__ __forceinline__ void ld_16x256b_x8(uint32_t taddr, float (&v)[32]) {
+    uint32_t* r = reinterpret_cast<uint32_t*>(v);
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x8.b32 " PA_OPS32 ", [%32];" : PA_W32(r) : "r"(taddr));
+}
+__device__ __forceinline__ void st_16x256b_x8(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile("tcgen05.st.sync.aligned.16x256b.x8.b32 [%0], " PA_OPS32_FROM1 ";" ::"r"(taddr), PA_R32(r)
+                 : "memory");
+}
+// 16 lanes x 64 columns
+__device__ __forceinline__ void st_16x128b_x16(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile("tcgen05.st.sync.aligned.16x128b.x16.b32 [%0], " PA_OPS32_FROM1 ";" ::"r"(taddr), PA_R32(r)
+                 : "memory");
+}
+#undef PA_R32
+#undef PA_W32
+#undef PA_OPS32
+#undef PA_OPS32_FROM1
+
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
