@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         mbar_init(q_full, 1);
         for (int s = 0; s < C::KS; ++s) {
             mbar_init(&k_full[s], 1);
-            mbar_init(&k_empty[s], 2);  // one commit per MMA issuer
+            mbar_init(&k_empty[s], 2);  // one arrive per query tile (softmax side)
         }
         for (int s = 0; s < C::VS; ++s) {
             mbar_init(&v_full[s], 1);
@@ -363,9 +363,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 }
                 tc::commit(&s_full[x]);
             }
-            tc::commit(&k_empty[j % C::KS]);
         };
-        bool ok = !active || wait_all(q_full, 0);
+        // Stages are released on the softmax side (see there); an issuer without a tile idles.
+        bool ok = active && wait_all(q_full, 0);
         if (ok && n_tiles > 0 && (ok = wait_all(&k_full[0], 0))) {
             if (lane == 0) issue_s(0);
             __syncwarp();
@@ -404,7 +404,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                         tc::mma_ts(d_o, d_s + kk * 8, db + (uint64_t)(kk * (2048 / 16)), IDESC_O, kk > 0 ? 1u : first);
                     if (j + 1 == n_tiles) tc::commit(&pv_done[x]);
                 }
-                tc::commit(&v_empty[j % C::VS]);
                 if (more) issue_s(j + 1);
             }
             __syncwarp();
@@ -457,6 +456,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             const int kt = kt0 + j * 128;
             if (!__all_sync(0xffffffffu, wait_bar(&s_full[x], j & 1, abort_flag, p.err, p.wait_ns))) return false;
             tc::fence_after_sync();
+            // S_x(j) is complete, and so is PV_x(j-1), which its issuer started before it: this
+            // tile is done with K stage j and V stage j-1.  (Releasing them here instead of by
+            // tcgen05.commit spares the issuers two commits per key tile.)
+            if (warp == 4 && lane == 0) {
+                const uint32_t n = has_b ? 1u : 2u;
+                mbar_arrive_n(&k_empty[j % C::KS], n);
+                if (j > 0) mbar_arrive_n(&v_empty[(j - 1) % C::VS], n);
+            }
             const uint32_t s_addr = tmem + lane_addr + (x ? C::T_S1 : C::T_S0);
             const uint32_t o_addr = tmem + lane_addr + (x ? C::T_O1 : C::T_O0);
             // sv[4k + 2q + e] = S[row q][key 8k + 2 tig + e]
@@ -476,8 +483,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                             v = (key >= st.lo[q] && key <= st.hi[q]) ? v : -INFINITY;
                         }
             }
-            float alpha[2];
-            bool resc = false;
+            // Running max: each thread first checks its own 32 keys of each row against the
+            // running max; only when some row of the warp grew past it by more than 2^8 (the
+            // first tile, or a jump in the scores) are the exact row maxima taken over the quad
+            // and O rescaled.
+            const float sl = p.scale_log2;  // softmax_scale > 0 on this path
+            float lm[2];
+            bool grow = false;
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
                 float c0 = fmaxf(sv[2 * q], sv[2 * q + 1]), c1 = fmaxf(sv[4 + 2 * q], sv[5 + 2 * q]);
@@ -486,32 +498,39 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     c0 = max3f(c0, sv[4 * k + 2 * q], sv[4 * k + 2 * q + 1]);
                     c1 = max3f(c1, sv[4 * k + 4 + 2 * q], sv[4 * k + 5 + 2 * q]);
                 }
-                float mx = fmaxf(c0, c1);
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                const float m_cand = mx * p.scale_log2;  // softmax_scale > 0 on this path
-                alpha[q] = 1.f;
-                if (m_cand > st.m[q] + 8.f) {
-                    alpha[q] = fast_exp2(st.m[q] - m_cand);
-                    st.m[q] = m_cand;
-                    resc = true;
-                }
+                lm[q] = fmaxf(c0, c1);
+                grow |= lm[q] * sl > st.m[q] + 8.f;
             }
-            // O_x was accumulated with the old maximum.  Its last P.V (PV_x(j-1)) precedes
-            // S_x(j) in the tensor pipe, so it is complete once S_x(j) is.
-            if (j > 0 && __any_sync(0xffffffffu, resc)) {
-#pragma unroll 1
-                for (int cc = 0; cc < DP / 64; ++cc) {
-                    float o[32];
-                    tc::ld_16x256b_x8(o_addr + cc * 64, o);
-                    tc::wait_ld();
-                    uint32_t ob[32];
+            float alpha[2] = {1.f, 1.f};
+            if (__any_sync(0xffffffffu, grow)) {
+                bool resc = false;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) ob[e] = __float_as_uint(o[e] * alpha[(e >> 1) & 1]);
-                    tc::st_16x256b_x8(o_addr + cc * 64, ob);
+                for (int q = 0; q < 2; ++q) {
+                    float mx = lm[q];
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                    const float m_cand = mx * sl;
+                    if (m_cand > st.m[q] + 8.f) {
+                        alpha[q] = fast_exp2(st.m[q] - m_cand);
+                        st.m[q] = m_cand;
+                        resc = true;
+                    }
+                }
+                // O_x was accumulated with the old maximum.  Its last P.V (PV_x(j-1)) precedes
+                // S_x(j) in the tensor pipe, so it is complete once S_x(j) is.
+                if (j > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+                    for (int cc = 0; cc < DP / 64; ++cc) {
+                        float o[32];
+                        tc::ld_16x256b_x8(o_addr + cc * 64, o);
+                        tc::wait_ld();
+                        uint32_t ob[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) ob[e] = __float_as_uint(o[e] * alpha[(e >> 1) & 1]);
+                        tc::st_16x256b_x8(o_addr + cc * 64, ob);
+                    }
                 }
             }
-            const float sl = p.scale_log2;
             float nm[2];
 #pragma unroll
             for (int q = 0; q < 2; ++q) nm[q] = st.m[q] == -INFINITY ? 0.f : -st.m[q];
