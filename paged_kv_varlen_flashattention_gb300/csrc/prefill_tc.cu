@@ -456,20 +456,21 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             const int kt = kt0 + j * 128;
             if (!__all_sync(0xffffffffu, wait_bar(&s_full[x], j & 1, abort_flag, p.err, p.wait_ns))) return false;
             tc::fence_after_sync();
-            // S_x(j) is complete, and so is PV_x(j-1), which its issuer started before it: this
-            // tile is done with K stage j and V stage j-1.  (Releasing them here instead of by
-            // tcgen05.commit spares the issuers two commits per key tile.)
-            if (warp == 4 && lane == 0) {
-                const uint32_t n = has_b ? 1u : 2u;
-                mbar_arrive_n(&k_empty[j % C::KS], n);
-                if (j > 0) mbar_arrive_n(&v_empty[(j - 1) % C::VS], n);
-            }
             const uint32_t s_addr = tmem + lane_addr + (x ? C::T_S1 : C::T_S0);
             const uint32_t o_addr = tmem + lane_addr + (x ? C::T_O1 : C::T_O0);
             // sv[4k + 2q + e] = S[row q][key 8k + 2 tig + e]
             float sv[64];
             tc::ld_16x256b_x8(s_addr, *reinterpret_cast<float(*)[32]>(&sv[0]));
             tc::ld_16x256b_x8(s_addr + 64, *reinterpret_cast<float(*)[32]>(&sv[32]));
+            // S_x(j) is complete, and so is PV_x(j-1), which its issuer started before it: this
+            // tile is done with K stage j and V stage j-1.  (Released here, while the TMEM load
+            // is in flight, instead of by tcgen05.commit: that spares the issuers two commits
+            // per key tile.)
+            if (warp == 4 && lane == 0) {
+                const uint32_t n = has_b ? 1u : 2u;
+                mbar_arrive_n(&k_empty[j % C::KS], n);
+                if (j > 0) mbar_arrive_n(&v_empty[(j - 1) % C::VS], n);
+            }
             tc::wait_ld();
             if (!(kt >= max(st.lo[0], st.lo[1]) && kt + 127 <= min(st.hi[0], st.hi[1]))) {
 #pragma unroll
