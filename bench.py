@@ -69,6 +69,56 @@ def algorithmic(lay, seqs=None):
     return flops, kv + qo + lse
 
 
+def workload_config(lay, flops, nbytes, world):
+    """The `config` object of the JSON line (both arms)."""
+    return {"workload": lay.name, "batch": lay.batch, "num_heads": lay.num_heads,
+            "num_heads_k": lay.num_heads_k, "head_dim": lay.head_dim,
+            "page_block_size": lay.page_block_size, "max_seqlen_k": lay.max_seqlen_k,
+            "total_keys": lay.total_k, "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+            "l2": "inputs larger than L2 (no flush)" if nbytes > 2 * L2_BYTES else "L2 not flushed; inputs fit",
+            "parallelism": f"replicas{world}"}
+
+
+def headline_unit(flops, nbytes):
+    """("TFLOP/s", 1e12) for a workload above the ridge point of the peaks, else ("GB/s", 1e9),
+    with the matching amount of work per step."""
+    hbm, bf16, _, _ = peaks()
+    if flops / nbytes > (bf16 * 1e12) / (hbm * 1e9):
+        return "TFLOP/s", flops / 1e12
+    return "GB/s", nbytes / 1e9
+
+
+def kernel_class_seqs(lay):
+    """Sequences per kernel class, mirroring the library's dispatch: sequences with more
+    than 32 rows (sq * G) go to the tensor-core prefill kernel when it takes the call
+    (head_dim <= 128, G divides 128, softmax_scale > 0), the rest to the split-KV pass."""
+    G = lay.num_heads // lay.num_heads_k
+    tc = (lay.head_dim <= 128 and 128 % G == 0 and lay.softmax_scale > 0
+          and max(lay.seqlens_q) * G > 32 and not os.environ.get("PA_DISABLE_TC_PREFILL"))
+    pre = [b for b in range(lay.batch) if tc and lay.seqlens_q[b] * G > 32]
+    split = [b for b in range(lay.batch) if b not in set(pre)]
+    return {"prefill": pre, "splitkv": split}
+
+
+def time_kernels(binding, g, lay, steps):
+    """Per-kernel device time: the library brackets each launch with CUDA events on the
+    stream it is launched on.  Returns {class: (ms per launch, launches per step)}."""
+    import torch
+    out = torch.empty_like(g.q)
+    lse = torch.empty((lay.num_heads, lay.total_q), dtype=torch.float32, device=g.q.device)
+    torch.cuda.synchronize()
+    binding.kernel_times()  # drop anything recorded earlier
+    binding.kernel_timing(True)
+    try:
+        for _ in range(steps):
+            _call(binding, g, lay, out, lse)
+        torch.cuda.synchronize()
+    finally:
+        binding.kernel_timing(False)
+    t = binding.kernel_times()
+    return {k: (ms / n, n / steps) for k, (ms, n) in t.items() if n > 0}
+
+
 # ---- peaks, profiles, clocks ------------------------------------------------------------------
 
 def peaks():
@@ -228,30 +278,44 @@ def time_e2e(binding, g, lay, steps, warmup):
 
 
 def cpu_baseline(lay, inp_cpu, budget_s=20.0):
-    """The oracle, as it stands, on the host cores over a bounded sample of the workload
-    (whole sequences, all heads); returns (GB/s, seconds, threads, sample text)."""
+    """The oracle, as it stands, on the host cores over a bounded sample of the workload:
+    whole sequences (all heads) in a seeded order, repeated until about half the budget has
+    been spent and never past the budget; returns (value in the workload's headline unit,
+    unit, seconds, threads, sample text)."""
     import oracle
     order = list(range(lay.batch))
     rng = np.random.default_rng(0)
     rng.shuffle(order)
     cq, _ = lay.cu_seqlens()
     bt = inp_cpu.block_table.numpy() if inp_cpu.block_table is not None else None
-    done, t_total = [], 0.0
-    for b in order:
-        rows = np.arange(cq[b] * lay.num_heads, cq[b + 1] * lay.num_heads, dtype=np.int64)
-        if len(rows) == 0:
-            continue
-        t0 = time.perf_counter()
-        oracle.attention(lay.dtype, inp_cpu.q, inp_cpu.k_cache, inp_cpu.v_cache, inp_cpu.cu_seqlens_q.numpy(),
-                         inp_cpu.cu_seqlens_k.numpy(), bt, lay.softmax_scale, lay.window_left, lay.window_right,
-                         rows=rows)
-        t_total += time.perf_counter() - t0
-        done.append(b)
-        if t_total > budget_s:
+    nbytes, nflops, t_total, runs, distinct, passes = 0, 0, 0.0, 0, set(), 0
+    while t_total < 0.5 * budget_s:
+        progressed = False
+        for b in order:
+            rows = np.arange(cq[b] * lay.num_heads, cq[b + 1] * lay.num_heads, dtype=np.int64)
+            if len(rows) == 0:
+                continue
+            t0 = time.perf_counter()
+            oracle.attention(lay.dtype, inp_cpu.q, inp_cpu.k_cache, inp_cpu.v_cache, inp_cpu.cu_seqlens_q.numpy(),
+                             inp_cpu.cu_seqlens_k.numpy(), bt, lay.softmax_scale, lay.window_left,
+                             lay.window_right, rows=rows)
+            t_total += time.perf_counter() - t0
+            f_b, b_b = algorithmic(lay, [b])
+            nflops += f_b
+            nbytes += b_b
+            runs += 1
+            distinct.add(b)
+            progressed = True
+            if t_total > budget_s:
+                break
+        passes += 1
+        if not progressed or t_total > budget_s:
             break
-    _, nbytes = algorithmic(lay, done)
-    sample = f"{len(done)} of {lay.batch} sequences (all heads), {t_total:.1f} s"
-    return nbytes / t_total / 1e9, t_total, oracle.threads(), sample
+    sample = (f"{runs} sequence runs ({len(distinct)} of {lay.batch} sequences, all heads; "
+              f"{passes} pass(es) in a seeded order), {t_total:.1f} s")
+    unit, _ = headline_unit(*algorithmic(lay))
+    work = nflops / 1e12 if unit == "TFLOP/s" else nbytes / 1e9
+    return work / t_total, unit, t_total, oracle.threads(), sample
 
 
 def run_ours(args):
@@ -299,24 +363,43 @@ def run_ours(args):
     else:
         unit, peak, scale_w = "GB/s", hbm, nbytes / 1e9
     value = world * scale_w / (ms * 1e-3)
-    achieved = scale_w / (ms * 1e-3)
+
+    # roofline of the dominant kernel: its algorithmic work per launch over its own average
+    # launch duration (CUDA events around each launch, on the stream it runs on)
+    per_kernel = time_kernels(binding, g, lay, max(3, min(args.steps, 20)))
+    # a class without sequences of its own (e.g. the split-KV pass of a prefill-only batch)
+    # launches CTAs that exit at once; its events then mostly time the wait for SMs
+    with_work = {k: v for k, v in per_kernel.items()
+                 if k == "combine" or kernel_class_seqs(lay).get(k)}
+    dom = max((k for k in with_work if k != "combine"),
+              key=lambda k: with_work[k][0] * with_work[k][1], default="combine")
+    dom_ms, dom_launches = per_kernel[dom]
+    f_d, b_d = algorithmic(lay, kernel_class_seqs(lay)[dom]) if dom != "combine" else (flops, nbytes)
+    dom_tensor = dom == "prefill" or (f_d / max(b_d, 1) > (bf16 * 1e12) / (hbm * 1e9))
+    if dom_tensor:
+        r_unit, r_peak, r_work = "TFLOP/s", bf16, f_d / 1e12 / dom_launches
+    else:
+        r_unit, r_peak, r_work = "GB/s", hbm, b_d / 1e9 / dom_launches
+    achieved = r_work / (dom_ms * 1e-3)
+    total_ms = sum(v[0] * v[1] for v in with_work.values())
+    kernel_names = {"prefill": "prefill_kernel", "combine": "combine_kernel",
+                    "splitkv": "decode_kernel" if max(lay.seqlens_q) * lay.num_heads // lay.num_heads_k <= 32
+                    and lay.head_dim <= 256 else "decode_kernel/splitkv_kernel"}
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if lay.dtype == "bf16" else "f16", "data": "synthetic",
-        "config": {"workload": lay.name, "batch": lay.batch, "num_heads": lay.num_heads,
-                   "num_heads_k": lay.num_heads_k, "head_dim": lay.head_dim,
-                   "page_block_size": lay.page_block_size, "max_seqlen_k": lay.max_seqlen_k,
-                   "total_keys": lay.total_k, "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
-                   "l2": "inputs larger than L2 (no flush)" if nbytes > 2 * L2_BYTES else "L2 not flushed; inputs fit",
-                   "parallelism": f"replicas{world}"},
-        "roofline": {"bound": "tensor" if tensor_bound else "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": unit, "frac": round(achieved / peak, 4), "traffic": profiled_traffic(lay.name),
-                     "peak_source": (f"measured (MEASURED_PEAKS.json {'bf16_tflops' if tensor_bound else 'hbm_gbs'})"
+        "config": workload_config(lay, flops, nbytes, world),
+        "roofline": {"bound": "tensor" if dom_tensor else "hbm", "achieved": round(achieved, 1), "peak": r_peak,
+                     "unit": r_unit, "frac": round(achieved / r_peak, 4), "traffic": profiled_traffic(lay.name),
+                     "kernel": kernel_names[dom], "kernel_ms": round(dom_ms, 5),
+                     "kernel_share": round(dom_ms * dom_launches / total_ms, 4),
+                     "work_per_launch": r_work * (1e12 if dom_tensor else 1e9),
+                     "peak_source": (f"measured (MEASURED_PEAKS.json {'bf16_tflops' if dom_tensor else 'hbm_gbs'})"
                                      if peak_kind == "measured" else
-                                     ("fallback 1.9 PFLOP/s" if tensor_bound else "fallback 6.8 TB/s")),
-                     "timed": "whole pa_varlen_fwd call (every kernel it launches) per step"},
+                                     ("fallback 1.9 PFLOP/s" if dom_tensor else "fallback 6.8 TB/s")),
+                     "timed": "CUDA events around each launch of the kernel, on its stream"},
         "gpu_launches": int(launches),
         "clocks": clocks,
     }
@@ -333,18 +416,24 @@ def run_ours(args):
             f2, b2 = algorithmic(lay2)
             ms2, l2 = time_device(binding, g2, lay2, 3, 2, None)
             tf = f2 / (ms2 * 1e-3) / 1e12
+            pk = time_kernels(binding, g2, lay2, 3).get("prefill")
+            f_pre = algorithmic(lay2, kernel_class_seqs(lay2)["prefill"])[0]
+            tf_k = f_pre / pk[1] / (pk[0] * 1e-3) / 1e12 if pk else None
             result["secondary"] = {"workload": lay2.name, "value": round(tf, 2), "unit": "TFLOP/s",
                                    "ms_per_step": round(ms2, 4), "algorithmic_flops": f2,
-                                   "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": bf16,
-                                                "unit": "TFLOP/s", "frac": round(tf / bf16, 4)},
+                                   "roofline": {"bound": "tensor", "kernel": "prefill_kernel",
+                                                "achieved": round(tf_k, 2) if tf_k else None, "peak": bf16,
+                                                "unit": "TFLOP/s", "frac": round(tf_k / bf16, 4) if tf_k else None,
+                                                "kernel_ms": round(pk[0], 5) if pk else None,
+                                                "traffic": profiled_traffic(lay2.name)},
                                    "gpu_launches": int(l2)}
             del g2
         except Exception as e:  # reported, not hidden
             result["secondary"] = {"error": str(e)[:300]}
     if rank == 0 and not args.no_cpu_baseline:
         inp_cpu = g.to("cpu")
-        gbs, secs, cores, sample = cpu_baseline(lay, inp_cpu, budget_s=args.cpu_budget)
-        result["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+        val, cunit, secs, cores, sample = cpu_baseline(lay, inp_cpu, budget_s=args.cpu_budget)
+        result["cpu_baseline"] = {"value": round(val, 4), "unit": cunit, "cores": cores, "kind": "oracle",
                                   "sample": sample}
     if dist:
         dist.barrier()
@@ -370,7 +459,10 @@ def run_reference(args):
     n_seq = max(1, min(lay.batch, args.ref_sequences))
     seqs = sorted(rng.choice(lay.batch, size=n_seq, replace=False).tolist())
     rows = np.concatenate([np.arange(cq[b] * lay.num_heads, cq[b + 1] * lay.num_heads) for b in seqs]).astype(np.int64)
-    _, nbytes = algorithmic(lay, seqs)
+    flops_all, bytes_all = algorithmic(lay)
+    unit, _ = headline_unit(flops_all, bytes_all)
+    f_s, b_s = algorithmic(lay, seqs)
+    work = f_s / 1e12 if unit == "TFLOP/s" else b_s / 1e9
 
     def step():
         oracle.attention(lay.dtype, inp.q, inp.k_cache, inp.v_cache, inp.cu_seqlens_q.numpy(),
@@ -383,17 +475,18 @@ def run_reference(args):
     for _ in range(args.steps):
         step()
     secs = (time.perf_counter() - t0) / args.steps
-    value = nbytes / secs / 1e9
-    sample = f"{n_seq} of {lay.batch} sequences (all heads) per step"
+    value = work / secs
+    sample = f"{n_seq} of {lay.batch} sequences (all heads) per step, seeded choice"
+    world = int(os.environ.get("WORLD_SIZE", "1"))
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
-        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": unit,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(secs * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": {"workload": lay.name, "sample": sample, "parallelism": "host cores"},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.threads(), "kind": "oracle",
+        "config": workload_config(lay, flops_all, bytes_all, world),
+        "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": oracle.threads(), "kind": "oracle",
                          "sample": sample},
-        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
 

@@ -193,6 +193,25 @@ void pa_set_withhold_loads(int enable);
  * devices), for profiling: a caller reads it before and after a region. */
 uint64_t pa_kernel_launches(void);
 
+/* Per-kernel device timing, for profiling.  After pa_kernel_timing(1), every kernel this
+ * library launches (any thread, any device) is bracketed by two CUDA events recorded on
+ * the stream it is launched on; launches into a stream that is being captured are not
+ * timed, and at most 65,536 launches are kept between two reads.  pa_kernel_timing(0)
+ * stops recording; what was recorded stays until it is read.
+ * pa_kernel_times waits for the recorded events, writes to ms[c] the summed elapsed
+ * milliseconds and to launches[c] the number of timed launches of kernel class c, and
+ * clears the record.  Classes: PA_KC_PREFILL (the tensor-core prefill kernel),
+ * PA_KC_SPLITKV (the split-KV pass: decode_kernel or splitkv_kernel), PA_KC_COMBINE (the
+ * split-KV combine).  ms and launches are caller-owned host arrays of PA_KERNEL_CLASSES
+ * entries.  Returns PA_OK, PA_ERR_ARG for a null array, or PA_ERR_CUDA if an event
+ * query failed (message in pa_last_error; the record is cleared either way). */
+#define PA_KC_PREFILL 0
+#define PA_KC_SPLITKV 1
+#define PA_KC_COMBINE 2
+#define PA_KERNEL_CLASSES 3
+void pa_kernel_timing(int enable);
+int pa_kernel_times(double* ms, uint64_t* launches);
+
 #ifdef __cplusplus
 }
 #endif

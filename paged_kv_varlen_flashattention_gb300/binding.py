@@ -74,6 +74,10 @@ def load():
         lib.pa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
         lib.pa_set_withhold_loads.restype = None
         lib.pa_set_withhold_loads.argtypes = [ctypes.c_int]
+        lib.pa_kernel_timing.restype = None
+        lib.pa_kernel_timing.argtypes = [ctypes.c_int]
+        lib.pa_kernel_times.restype = ctypes.c_int
+        lib.pa_kernel_times.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_uint64)]
         _lib = lib
     return _lib
 
@@ -104,6 +108,25 @@ def _ref(d):
 def kernel_launches() -> int:
     """Kernels the library has launched in this process so far."""
     return int(load().pa_kernel_launches())
+
+
+KERNEL_CLASSES = ("prefill", "splitkv", "combine")  # PA_KC_PREFILL, PA_KC_SPLITKV, PA_KC_COMBINE
+
+
+def kernel_timing(enable: bool) -> None:
+    """Start (or stop) bracketing every launch with CUDA events on its stream."""
+    load().pa_kernel_timing(1 if enable else 0)
+
+
+def kernel_times() -> dict:
+    """{class: (summed ms, launches)} of the launches timed since the last read; clears them."""
+    n = len(KERNEL_CLASSES)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_uint64 * n)()
+    rc = load().pa_kernel_times(ms, cnt)
+    if rc != 0:
+        raise PaError(rc, last_error())
+    return {name: (float(ms[i]), int(cnt[i])) for i, name in enumerate(KERNEL_CLASSES)}
 
 
 def set_wait_limit_ns(ns: int) -> None:

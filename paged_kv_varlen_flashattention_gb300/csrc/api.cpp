@@ -18,6 +18,7 @@
 #include <map>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "pa_internal.h"
 
@@ -359,6 +360,73 @@ static std::atomic<uint64_t> g_wait_ns{PA_WAIT_LIMIT_NS};
 static std::atomic<int> g_withhold{0};
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
+// ---- per-kernel timing ----------------------------------------------------------------------
+namespace {
+struct TimedLaunch {
+    int cls, dev;
+    cudaEvent_t begin, end;
+};
+constexpr size_t kMaxTimed = 65536;
+std::atomic<int> g_timing{0};
+std::mutex g_timer_mu;
+std::vector<TimedLaunch> g_timed;                       // guarded by g_timer_mu
+std::vector<std::pair<int, cudaEvent_t>> g_event_pool;  // (device, event), guarded by g_timer_mu
+thread_local cudaEvent_t t_pending = nullptr;           // begin event of this thread's launch
+thread_local int t_pending_dev = -1;
+
+// An event of device `dev` from the pool, or a new one (nullptr on failure).  Caller holds
+// g_timer_mu and has `dev` current.
+cudaEvent_t pooled_event(int dev) {
+    for (size_t i = g_event_pool.size(); i-- > 0;) {
+        if (g_event_pool[i].first == dev) {
+            cudaEvent_t e = g_event_pool[i].second;
+            g_event_pool.erase(g_event_pool.begin() + (long)i);
+            return e;
+        }
+    }
+    cudaEvent_t e = nullptr;
+    return cudaEventCreate(&e) == cudaSuccess ? e : nullptr;
+}
+}  // namespace
+
+void timer_begin(int, cudaStream_t stream) {
+    if (!g_timing.load(std::memory_order_relaxed)) return;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+        (void)cudaGetLastError();
+        return;
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return;
+    std::lock_guard<std::mutex> lock(g_timer_mu);
+    if (t_pending) {  // the previous launch of this thread failed: recycle its event
+        g_event_pool.emplace_back(t_pending_dev, t_pending);
+        t_pending = nullptr;
+    }
+    if (g_timed.size() >= kMaxTimed) return;
+    cudaEvent_t e = pooled_event(dev);
+    if (!e) return;
+    if (cudaEventRecord(e, stream) != cudaSuccess) {
+        g_event_pool.emplace_back(dev, e);
+        return;
+    }
+    t_pending = e;
+    t_pending_dev = dev;
+}
+
+void timer_end(int cls, cudaStream_t stream) {
+    if (!t_pending) return;
+    std::lock_guard<std::mutex> lock(g_timer_mu);
+    cudaEvent_t e = pooled_event(t_pending_dev);
+    if (e && cudaEventRecord(e, stream) == cudaSuccess) {
+        g_timed.push_back({cls, t_pending_dev, t_pending, e});
+    } else {
+        if (e) g_event_pool.emplace_back(t_pending_dev, e);
+        g_event_pool.emplace_back(t_pending_dev, t_pending);
+    }
+    t_pending = nullptr;
+}
+
 int encode_tmap_4d(void* map, int dtype, const void* base, const uint64_t dims_[4], const uint64_t strides_bytes[3],
                    const uint32_t box[4], int swizzle128, char* msg, size_t msg_len) {
     auto fn = encode_fn();
@@ -550,5 +618,37 @@ void pa_set_wait_limit_ns(uint64_t ns) { pa::g_wait_ns.store(ns ? ns : PA_WAIT_L
 void pa_set_withhold_loads(int enable) { pa::g_withhold.store(enable ? 1 : 0); }
 
 uint64_t pa_kernel_launches(void) { return pa::g_launches.load(std::memory_order_relaxed); }
+
+void pa_kernel_timing(int enable) { pa::g_timing.store(enable ? 1 : 0, std::memory_order_relaxed); }
+
+int pa_kernel_times(double* ms, uint64_t* launches) {
+    if (!ms || !launches) return fail(PA_ERR_ARG, "pa_kernel_times: null output array");
+    for (int c = 0; c < PA_KERNEL_CLASSES; ++c) {
+        ms[c] = 0.0;
+        launches[c] = 0;
+    }
+    std::lock_guard<std::mutex> lock(pa::g_timer_mu);
+    if (pa::g_timed.empty()) return PA_OK;
+    int prev = 0;
+    cudaGetDevice(&prev);
+    int rc = PA_OK;
+    for (const auto& t : pa::g_timed) {
+        float el = 0.f;
+        cudaError_t e = cudaSetDevice(t.dev);
+        if (e == cudaSuccess) e = cudaEventSynchronize(t.end);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&el, t.begin, t.end);
+        if (e != cudaSuccess && rc == PA_OK)
+            rc = fail(PA_ERR_CUDA, "pa_kernel_times: %s", cudaGetErrorString(e));
+        if (e == cudaSuccess && t.cls >= 0 && t.cls < PA_KERNEL_CLASSES) {
+            ms[t.cls] += el;
+            launches[t.cls] += 1;
+        }
+        pa::g_event_pool.emplace_back(t.dev, t.begin);
+        pa::g_event_pool.emplace_back(t.dev, t.end);
+    }
+    pa::g_timed.clear();
+    cudaSetDevice(prev);
+    return rc;
+}
 
 }  // extern "C"

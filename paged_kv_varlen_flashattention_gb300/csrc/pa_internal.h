@@ -84,6 +84,12 @@ int error_word(unsigned int** ptr);
 // Counts successful kernel launches (pa_kernel_launches).
 void count_launches(int n);
 
+// Per-kernel timing (pa_kernel_timing): timer_begin before a launch of kernel class `cls`
+// (PA_KC_*) into `stream`, timer_end after it launched successfully.  Both do nothing
+// unless timing is on.
+void timer_begin(int cls, cudaStream_t stream);
+void timer_end(int cls, cudaStream_t stream);
+
 // Supplier of the split-KV scratch for one call: sets *ptr to at least `bytes` bytes of
 // device memory usable on `stream`, or returns a status with a message in msg.
 using ScratchFn = int (*)(void* ctx, cudaStream_t stream, size_t bytes, void** ptr, char* msg, size_t msg_len);

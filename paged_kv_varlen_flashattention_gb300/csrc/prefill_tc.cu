@@ -667,12 +667,14 @@ int run_prefill(const Args& a, const PrefillParams& pp, cudaStream_t stream, cha
         configured = true;
     }
     dim3 grid(pp.pairs, a.Hkv, 1);
+    timer_begin(PA_KC_PREFILL, stream);
     kern<<<grid, kPrefillThreads, C::SMEM, stream>>>(tq, tk, tv, pp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "prefill launch: %s", cudaGetErrorString(e));
         return PA_ERR_CUDA;
     }
+    timer_end(PA_KC_PREFILL, stream);
     count_launches(1);
     return PA_OK;
 }

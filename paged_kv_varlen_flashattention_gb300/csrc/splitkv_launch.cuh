@@ -46,21 +46,25 @@ static int run_splitkv(const CUtensorMap& tk, const CUtensorMap& tv, const Split
         configured = true;
     }
     dim3 grid(plan.max_splits, sp.Hkv * plan.row_tiles, sp.batch);
+    timer_begin(PA_KC_SPLITKV, stream);
     kern<<<grid, 128, C::SMEM, stream>>>(tk, tv, sp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "split-KV launch: %s", cudaGetErrorString(e));
         return PA_ERR_CUDA;
     }
+    timer_end(PA_KC_SPLITKV, stream);
     count_launches(1);
     if (plan.max_splits > 1) {
         dim3 g2((plan.tile_rows + kCombineRows - 1) / kCombineRows, sp.Hkv * plan.row_tiles, sp.batch);
+        timer_begin(PA_KC_COMBINE, stream);
         combine_kernel<T, C::M, NT><<<g2, 128, 0, stream>>>(sp);
         e = cudaGetLastError();
         if (e != cudaSuccess) {
             snprintf(msg, msg_len, "split-KV combine launch: %s", cudaGetErrorString(e));
             return PA_ERR_CUDA;
         }
+        timer_end(PA_KC_COMBINE, stream);
         count_launches(1);
     }
     return PA_OK;
@@ -97,21 +101,25 @@ static int run_decode(const CUtensorMap& tk, const CUtensorMap& tv, const SplitP
         configured = true;
     }
     dim3 grid(plan.max_splits, sp.Hkv, sp.batch);
+    timer_begin(PA_KC_SPLITKV, stream);
     kern<<<grid, 160, C::SMEM, stream>>>(tk, tv, sp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "decode launch: %s", cudaGetErrorString(e));
         return PA_ERR_CUDA;
     }
+    timer_end(PA_KC_SPLITKV, stream);
     count_launches(1);
     if (plan.max_splits > 1) {
         dim3 g2((plan.tile_rows + kCombineRows - 1) / kCombineRows, sp.Hkv, sp.batch);
+        timer_begin(PA_KC_COMBINE, stream);
         combine_kernel<T, C::M, NT><<<g2, 128, 0, stream>>>(sp);
         e = cudaGetLastError();
         if (e != cudaSuccess) {
             snprintf(msg, msg_len, "decode combine launch: %s", cudaGetErrorString(e));
             return PA_ERR_CUDA;
         }
+        timer_end(PA_KC_COMBINE, stream);
         count_launches(1);
     }
     return PA_OK;

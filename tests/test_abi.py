@@ -36,3 +36,13 @@ def test_version_and_empty_error():
     lib = binding.load()
     assert lib.pa_version() >= 100
     assert isinstance(lib.pa_last_error(), bytes)
+
+
+def test_kernel_timing_record_starts_empty():
+    """With nothing launched, the per-kernel timing record reads as zeros, and a null
+    output array is an argument error (no CUDA call is made on either path)."""
+    assert "pa_kernel_times" in declared_symbols() and "pa_kernel_timing" in declared_symbols()
+    assert binding.kernel_times() == {name: (0.0, 0) for name in binding.KERNEL_CLASSES}
+    lib = binding.load()
+    assert lib.pa_kernel_times(None, None) == 10  # PA_ERR_ARG
+    assert b"null" in lib.pa_last_error()

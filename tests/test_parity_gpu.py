@@ -155,3 +155,28 @@ def test_long_prefill_spans_many_tiles_and_pages():
 
 def test_non_causal_prefill_with_sq_below_sk():
     _gpu.check_layout(_custom([200, 64], [1000, 64], H=8, Hkv=2, D=128, wl=-1, wr=-1))
+
+
+def test_kernel_timing_counts_each_class():
+    """Per-kernel timing sees one prefill launch per call for a prefill-only batch and the
+    split-KV pass (plus its combine when split) for a decode batch; times are positive."""
+    for name, cls in (("prefill", "prefill"), ("decode", "splitkv")):
+        lay = workloads.small(name)
+        lay.nan_fill = False
+        g = workloads.materialize(lay, device="cuda")
+        out = torch.empty_like(g.q)
+        lse = torch.empty((lay.num_heads, lay.total_q), dtype=torch.float32, device="cuda")
+        binding.kernel_times()
+        binding.kernel_timing(True)
+        try:
+            for _ in range(3):
+                binding.varlen_fwd(g.q, g.k_cache, g.v_cache, g.cu_seqlens_q, g.cu_seqlens_k, g.block_table,
+                                   max_seqlen_q=lay.max_seqlen_q, max_seqlen_k=lay.max_seqlen_k,
+                                   softmax_scale=lay.softmax_scale, window_left=lay.window_left,
+                                   window_right=lay.window_right, out=out, softmax_lse=lse)
+            torch.cuda.synchronize()
+        finally:
+            binding.kernel_timing(False)
+        t = binding.kernel_times()
+        assert t[cls][1] >= 3 and t[cls][0] > 0.0, (name, t)
+        assert binding.kernel_times() == {k: (0.0, 0) for k in binding.KERNEL_CLASSES}
