@@ -50,7 +50,7 @@ def load(path: str):
     lib.pa_oracle_fwd.argtypes = [
         ctypes.c_int, u16p, i64p, u16p, u16p, i64p, i32p, i32p, ctypes.c_int64,
         i32p, ctypes.c_int64, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
-        ctypes.c_double, ctypes.c_int, ctypes.c_int, i64p, ctypes.c_int64, f64p, f64p,
+        ctypes.c_double, ctypes.c_int, ctypes.c_int, f64p, i64p, ctypes.c_int64, f64p, f64p,
     ]
     lib.pa_oracle_threads.restype = ctypes.c_int
     lib.pa_oracle_decode.restype = ctypes.c_double
@@ -94,14 +94,16 @@ def _ptr(a, ctype):
 
 
 def attention(dtype, q, k, v, cu_seqlens_q, cu_seqlens_k, block_table, softmax_scale,
-              window_left=-1, window_right=0, rows=None, lib=None):
+              window_left=-1, window_right=0, rows=None, lib=None, alibi_slopes=None):
     """Masked softmax attention through the block table, in fp64.
 
     q: (total_q, H, D); k, v: (num_blocks, P, Hkv, D) when ``block_table`` is given,
     else (total_k, Hkv, D).  Arrays are fp16/bf16 (torch CPU tensors or numpy fp16
     or uint16 bit patterns), contiguous.  ``rows``: optional int64 array of
     token * H + head.  Returns (out float64 [n, D], lse float64 [n]) where n is
-    len(rows) or total_q * H (row r = token * H + head).
+    len(rows) or total_q * H (row r = token * H + head).  ``alibi_slopes``: optional
+    per-query-head slopes (H values); the score of query i and key j then gets
+    -slope_h * |i + sk - sq - j|.
     """
     lib = lib if lib is not None else _load()
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
@@ -140,6 +142,13 @@ def attention(dtype, q, k, v, cu_seqlens_q, cu_seqlens_k, block_table, softmax_s
         rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
         n = len(rows_arr)
         rows_ptr = _ptr(rows_arr, ctypes.c_int64)
+    if alibi_slopes is not None:
+        slopes = np.ascontiguousarray(np.asarray(alibi_slopes, dtype=np.float64).reshape(-1))
+        if slopes.shape != (H,):
+            raise ValueError("alibi_slopes must hold one slope per query head")
+        slopes_ptr = _ptr(slopes, ctypes.c_double)
+    else:
+        slopes, slopes_ptr = None, None
     out = np.zeros((n, D), dtype=np.float64)
     lse = np.zeros((n,), dtype=np.float64)
     rc = lib.pa_oracle_fwd(
@@ -147,7 +156,7 @@ def attention(dtype, q, k, v, cu_seqlens_q, cu_seqlens_k, block_table, softmax_s
         _ptr(kb, ctypes.c_uint16), _ptr(vb, ctypes.c_uint16), _ptr(kv_stride, ctypes.c_int64),
         _ptr(cu_q, ctypes.c_int32), _ptr(cu_k, ctypes.c_int32), batch,
         bt_ptr, bt_stride, P, H, Hkv, D, float(softmax_scale), int(window_left), int(window_right),
-        rows_ptr, n, _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double))
+        slopes_ptr, rows_ptr, n, _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double))
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return out, lse

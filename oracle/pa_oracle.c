@@ -27,7 +27,14 @@
  *  - the mask is bottom-right aligned with inclusive window bounds; a negative
  *    window side is unbounded; causal is (window_left, window_right) = (-1, 0).
  *  - a row with no attended key gives out = 0 and lse = -inf.
- *  - lse is the natural log of sum_j exp(softmax_scale * q.k_j).
+ *  - lse is the natural log of sum_j exp(s_j) over the attended keys.
+ *  - alibi_slopes: the pages name the argument only through its shape check
+ *    ("shape mismatch alibi_slopes {:?}, expected {:?}" among the related errors of
+ *    "paged flash-attn requires page_block_size to be a multiple of 32" and of "flash-attn-
+ *    varlen paged expects k/v tensors of rank 4").  The reading taken is the usual
+ *    linear-bias definition: one fp32 slope per query head, and the score of query i
+ *    and key j is shifted by -slope_h * |i + sk - sq - j|, the distance to the query's
+ *    bottom-right aligned diagonal.
  *
  * All arithmetic is IEEE binary64 on the exact fp16 / bf16 input values, in two
  * passes (scores and their maximum first, then the exponentials), with no
@@ -83,6 +90,12 @@ static int attends(int64_t i, int64_t j, int64_t sq, int64_t sk, int wl, int wr)
     return 1;
 }
 
+/* Linear position bias (the reading above): -slope * |i + sk - sq - j|. */
+static double alibi_bias(double slope, int64_t i, int64_t j, int64_t sq, int64_t sk) {
+    int64_t c = sk - sq;
+    return -slope * fabs((double)(i + c - j));
+}
+
 /* Address of key (or value) row j of sequence b, kv head hk.
  * Paged: logical page j / P of row b of the block table names the physical
  * block; the row sits at slot j mod P of that block.
@@ -109,7 +122,8 @@ int pa_oracle_threads(void) {
 /*
  * out[r, :] and lse[r] for each requested (token, head) row r:
  *   J    = { j : attends(i, j) }                      (i = token - cu_q[b])
- *   s_j  = softmax_scale * sum_d q[token, h, d] * K_j[d]
+ *   s_j  = softmax_scale * sum_d q[token, h, d] * K_j[d]  (+ alibi_bias(slope_h, i, j) when
+ *          alibi_slopes is given)
  *   m    = max_{j in J} s_j,   l = sum_{j in J} exp(s_j - m)
  *   out  = sum_{j in J} exp(s_j - m) * V_j / l,   lse = m + ln(l)
  *
@@ -119,6 +133,7 @@ int pa_oracle_threads(void) {
  *                         non-paged: (token, head) strides of (total_k, Hkv, D)
  *   cu_q, cu_k            int32 [batch + 1]
  *   block_table           int32 [batch, bt_row_stride-spaced rows], NULL = non-paged
+ *   alibi_slopes          double [H] (one slope per query head), or NULL for no bias
  *   rows                  int64 [n_rows] of token * H + head, or NULL for all rows
  *   out                   double [n_rows, D] (or [total_q * H, D])
  *   lse                   double [n_rows]
@@ -131,6 +146,7 @@ int pa_oracle_fwd(int dtype,
                   const int32_t* block_table, int64_t bt_row_stride, int page_block_size,
                   int64_t num_heads, int64_t num_heads_k, int64_t head_dim,
                   double softmax_scale, int window_left, int window_right,
+                  const double* alibi_slopes,
                   const int64_t* rows, int64_t n_rows,
                   double* out, double* lse) {
     if (dtype != ORACLE_F16 && dtype != ORACLE_BF16) return -1;
@@ -167,6 +183,7 @@ int pa_oracle_fwd(int dtype,
             double dot = 0.0;
             for (int64_t d = 0; d < head_dim; ++d) dot += decode(dtype, qrow[d]) * decode(dtype, krow[d]);
             score[j] = softmax_scale * dot;
+            if (alibi_slopes) score[j] += alibi_bias(alibi_slopes[h], i, j, sq, sk);
             if (score[j] > m) m = score[j];
             ++attended;
         }

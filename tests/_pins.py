@@ -329,6 +329,79 @@ def pin_bf16_path(attn):
         assert np.allclose(lse[cq[b]:cq[b + 1]], l_ref, rtol=1e-12, atol=1e-13)
 
 
+def alibi_bias_matrix(sq, sk, slope):
+    """-slope * (distance of key j from query i's bottom-right aligned diagonal), built
+    with numpy's outer difference of the two position ranges."""
+    diag = np.arange(sq, dtype=np.float64) + (sk - sq)
+    return -slope * np.abs(np.subtract.outer(diag, np.arange(sk, dtype=np.float64)))
+
+
+def pin_alibi_sdpa(attn):
+    """Linear position bias: the oracle equals torch's scaled_dot_product_attention in
+    float64 with the bias (and -inf outside the window) as an additive float mask, per
+    sequence (sq < sk, so the bottom-right offset matters) and per query head (distinct
+    slopes under grouped-query heads); lse equals torch.logsumexp of the biased scores."""
+    import torch
+    import torch.nn.functional as F
+    rng = np.random.default_rng(111)
+    H, Hkv, D, scale = 4, 2, 16, 0.35
+    slopes = np.array([0.5, 0.125, 0.03125, 0.0078125])
+    sq, sk = [1, 6, 9], [13, 30, 9]
+    q = f16(rng, (sum(sq), H, D))
+    k = f16(rng, (sum(sk), Hkv, D))
+    v = f16(rng, (sum(sk), Hkv, D))
+    cq, ck = cu(sq), cu(sk)
+    for wl, wr in ((-1, 0), (-1, -1), (5, 2)):
+        out, lse = attn("f16", q, k, v, cq, ck, None, scale, wl, wr, alibi_slopes=slopes)
+        for b in range(len(sq)):
+            allowed = mask_by_library(sq[b], sk[b], wl, wr)
+            for h in range(H):
+                hk = h // (H // Hkv)
+                bias = np.where(allowed, alibi_bias_matrix(sq[b], sk[b], slopes[h]), -np.inf)
+                tq = torch.from_numpy(q[cq[b]:cq[b + 1], h].astype(np.float64))
+                tk = torch.from_numpy(k[ck[b]:ck[b + 1], hk].astype(np.float64))
+                tv = torch.from_numpy(v[ck[b]:ck[b + 1], hk].astype(np.float64))
+                tb = torch.from_numpy(bias)
+                live = allowed.any(axis=1)
+                ref = F.scaled_dot_product_attention(tq[None], tk[None], tv[None], attn_mask=tb[None],
+                                                     scale=scale)[0].numpy()
+                lref = torch.logsumexp(scale * (tq @ tk.T) + tb, dim=-1).numpy()
+                rows = (cq[b] + np.arange(sq[b])) * H + h
+                assert np.allclose(out[rows][live], ref[live], rtol=1e-10, atol=1e-12), (wl, wr, b, h)
+                assert np.allclose(lse[rows][live], lref[live], rtol=1e-12, atol=1e-12), (wl, wr, b, h)
+                assert np.all(np.isneginf(lse[rows][~live])) and np.all(out[rows][~live] == 0)
+
+
+def pin_alibi_two_keys(attn):
+    """Closed forms with equal scores, so only the bias separates the keys.  q = (1, 0.5)
+    and every key (1, 1): each score is 0.5 * 1.5 = 0.75.  (a) sq = 1, sk = 2, causal:
+    the query's diagonal is key 1, distances 1 and 0.  (b) sq = 1, sk = 4, window (3, 0):
+    distances 3, 2, 1, 0."""
+    slope = 0.25
+    q = np.array([[[1.0, 0.5]]], dtype=np.float16)
+    k2 = np.ones((2, 1, 2), dtype=np.float16)
+    v2 = np.array([[[4.0, -2.0]], [[2.0, 0.0]]], dtype=np.float16)
+    out, lse = attn("f16", q, k2, v2, cu([1]), cu([2]), None, 0.5, -1, 0, alibi_slopes=[slope])
+    w = np.exp(0.75 - slope * np.array([1.0, 0.0]))
+    assert np.allclose(out[0], (w[:, None] * v2[:, 0].astype(np.float64)).sum(0) / w.sum(), rtol=1e-14, atol=1e-15)
+    assert abs(lse[0] - math.log(w.sum())) < 1e-14
+    k4 = np.ones((4, 1, 2), dtype=np.float16)
+    v4 = np.array([[[4.0, -2.0]], [[8.0, 8.0]], [[-1.0, 6.0]], [[2.0, 0.0]]], dtype=np.float16)
+    out, lse = attn("f16", q, k4, v4, cu([1]), cu([4]), None, 0.5, 3, 0, alibi_slopes=[slope])
+    w = np.exp(0.75 - slope * np.array([3.0, 2.0, 1.0, 0.0]))
+    assert np.allclose(out[0], (w[:, None] * v4[:, 0].astype(np.float64)).sum(0) / w.sum(), rtol=1e-14, atol=1e-15)
+    assert abs(lse[0] - math.log(w.sum())) < 1e-14
+
+
+def pin_alibi_zero_slopes(attn):
+    """Zero slopes leave every output and lse bit-identical to no bias."""
+    rng = np.random.default_rng(112)
+    sq, sk, q, k, v = _multi_seq(rng)
+    a = attn("f16", q, k, v, cu(sq), cu(sk), None, 0.25, -1, 0)
+    b = attn("f16", q, k, v, cu(sq), cu(sk), None, 0.25, -1, 0, alibi_slopes=np.zeros(q.shape[1]))
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
 ALL_PINS = [
     pin_mask_bruteforce,
     lambda a: pin_mask_bruteforce(a, paged=True),
@@ -342,4 +415,7 @@ ALL_PINS = [
     pin_chunking,
     pin_closed_form,
     pin_bf16_path,
+    pin_alibi_sdpa,
+    pin_alibi_two_keys,
+    pin_alibi_zero_slopes,
 ]

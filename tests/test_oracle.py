@@ -71,3 +71,15 @@ def test_rejects_bad_arguments():
     with pytest.raises(ValueError):
         oracle.attention("f16", q, k, v, _pins.cu(sq), _pins.cu(sk), None, 0.3, -1, 0,
                          rows=np.array([10 ** 6]))
+
+
+def test_alibi_equals_sdpa_with_bias_mask():
+    _pins.pin_alibi_sdpa(oracle.attention)
+
+
+def test_alibi_two_key_closed_forms():
+    _pins.pin_alibi_two_keys(oracle.attention)
+
+
+def test_alibi_zero_slopes_is_no_bias():
+    _pins.pin_alibi_zero_slopes(oracle.attention)

@@ -29,6 +29,10 @@ MUTANTS = {
     "no_normalisation": ("o[d] /= l;", "o[d] /= 1.0;"),
     "exp_without_max": ("double w = exp(score[j] - m);", "double w = exp(score[j]);"),
     "empty_row_lse_zero": ("lse[r] = -INFINITY;", "lse[r] = 0.0;"),
+    "alibi_sign": ("return -slope * fabs(", "return slope * fabs("),
+    "alibi_no_abs": ("fabs((double)(i + c - j))", "((double)(i + c - j))"),
+    "alibi_top_left": ("fabs((double)(i + c - j))", "fabs((double)(i - j))"),
+    "alibi_kv_head": ("alibi_slopes[h]", "alibi_slopes[hk]"),
 }
 
 
