@@ -165,6 +165,40 @@ int pa_varlen_check(const pa_tensor* q, const pa_tensor* k_cache, const pa_tenso
                     int32_t page_block_size, float softmax_scale, int32_t window_left,
                     int32_t window_right, const pa_tensor* out, const pa_tensor* softmax_lse);
 
+/*
+ * pa_varlen_fwd_alibi -- pa_varlen_fwd with a linear position bias.  The pages name
+ * alibi_slopes only through the condition "shape mismatch alibi_slopes {:?}, expected
+ * {:?}" (a related error of "paged flash-attn requires page_block_size to be a multiple of
+ * 32" and of "flash-attn-varlen paged expects k/v tensors of rank 4"); the bias taken is
+ * the usual one: the score of query i and key j of a sequence with sq queries and sk
+ * keys, for query head h, becomes
+ *     softmax_scale * q.k_j - alibi_slopes[h] * |i + sk - sq - j|,
+ * before the mask and the softmax (lse includes the bias).
+ *
+ *  alibi_slopes  (num_heads,) f32, contiguous, device memory, borrowed for the call;
+ *                NULL gives exactly pa_varlen_fwd.
+ * Extra status codes, checked after the q/k/v shape conditions: PA_ERR_SHAPE "shape
+ * mismatch alibi_slopes [n], expected [num_heads]" (rank other than 1 or a wrong
+ * length), PA_ERR_NONCONTIG (stride != 1), PA_ERR_NOT_DEVICE, PA_ERR_ARG (dtype not f32).
+ * Everything else is as for pa_varlen_fwd.
+ */
+int pa_varlen_fwd_alibi(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                        const pa_tensor* cu_seqlens_q, const pa_tensor* cu_seqlens_k,
+                        const pa_tensor* block_table, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                        int32_t num_heads, int32_t num_heads_k, int32_t head_dim,
+                        int32_t page_block_size, float softmax_scale, int32_t window_left,
+                        int32_t window_right, const pa_tensor* alibi_slopes, const pa_tensor* out,
+                        const pa_tensor* softmax_lse, void* stream);
+
+/* pa_varlen_check with alibi_slopes (host-side checks only, as pa_varlen_check). */
+int pa_varlen_check_alibi(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                          const pa_tensor* cu_seqlens_q, const pa_tensor* cu_seqlens_k,
+                          const pa_tensor* block_table, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                          int32_t num_heads, int32_t num_heads_k, int32_t head_dim,
+                          int32_t page_block_size, float softmax_scale, int32_t window_left,
+                          int32_t window_right, const pa_tensor* alibi_slopes, const pa_tensor* out,
+                          const pa_tensor* softmax_lse);
+
 /* Message of the calling thread's last failed call ("" after a success).  The string
  * stays valid until that thread's next call into the library. */
 const char* pa_last_error(void);

@@ -48,6 +48,8 @@ class PaTensor(ctypes.Structure):
 _TP = ctypes.POINTER(PaTensor)
 _FWD_ARGS = [_TP, _TP, _TP, _TP, _TP, _TP, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
              ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_int32, ctypes.c_int32, _TP, _TP]
+# the same with alibi_slopes between window_right and out
+_FWD_ALIBI_ARGS = _FWD_ARGS[:15] + [_TP] + _FWD_ARGS[15:]
 
 
 def library_path() -> str:
@@ -65,6 +67,10 @@ def load():
         lib.pa_varlen_fwd.argtypes = _FWD_ARGS + [ctypes.c_void_p]
         lib.pa_varlen_check.restype = ctypes.c_int
         lib.pa_varlen_check.argtypes = list(_FWD_ARGS)
+        lib.pa_varlen_fwd_alibi.restype = ctypes.c_int
+        lib.pa_varlen_fwd_alibi.argtypes = _FWD_ALIBI_ARGS + [ctypes.c_void_p]
+        lib.pa_varlen_check_alibi.restype = ctypes.c_int
+        lib.pa_varlen_check_alibi.argtypes = list(_FWD_ALIBI_ARGS)
         lib.pa_last_error.restype = ctypes.c_char_p
         lib.pa_device_status.restype = ctypes.c_int
         lib.pa_device_status.argtypes = [ctypes.c_void_p]
@@ -152,8 +158,9 @@ def device_status(stream=None) -> int:
 
 def check(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, max_seqlen_q, max_seqlen_k,
           softmax_scale, window_left, window_right, out, softmax_lse, page_block_size=None,
-          num_heads=None, num_heads_k=None, head_dim=None, descriptors=None) -> int:
-    """Host-only validation (no CUDA call); returns the status code."""
+          num_heads=None, num_heads_k=None, head_dim=None, descriptors=None, alibi_slopes=None) -> int:
+    """Host-only validation (no CUDA call); returns the status code.  ``alibi_slopes`` (a
+    tensor, or a ready descriptor) selects pa_varlen_check_alibi."""
     lib = load()
     ds = descriptors or [describe(t) for t in (q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table,
                                                 out, softmax_lse)]
@@ -161,21 +168,26 @@ def check(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, max_seql
     D = head_dim if head_dim is not None else q.shape[-1]
     Hkv = num_heads_k if num_heads_k is not None else k_cache.shape[-2]
     P = page_block_size if page_block_size is not None else (k_cache.shape[1] if block_table is not None else 0)
-    return lib.pa_varlen_check(_ref(ds[0]), _ref(ds[1]), _ref(ds[2]), _ref(ds[3]), _ref(ds[4]), _ref(ds[5]),
-                               int(max_seqlen_q), int(max_seqlen_k), int(H), int(Hkv), int(D), int(P),
-                               float(softmax_scale), int(window_left), int(window_right), _ref(ds[6]),
-                               _ref(ds[7]))
+    scalars = (int(max_seqlen_q), int(max_seqlen_k), int(H), int(Hkv), int(D), int(P), float(softmax_scale),
+               int(window_left), int(window_right))
+    if alibi_slopes is not None:
+        da = alibi_slopes if isinstance(alibi_slopes, PaTensor) else describe(alibi_slopes)
+        return lib.pa_varlen_check_alibi(*[_ref(d) for d in ds[:6]], *scalars, _ref(da), _ref(ds[6]),
+                                         _ref(ds[7]))
+    return lib.pa_varlen_check(*[_ref(d) for d in ds[:6]], *scalars, _ref(ds[6]), _ref(ds[7]))
 
 
 def varlen_fwd(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table=None, max_seqlen_q=None,
                max_seqlen_k=None, softmax_scale=None, window_left=-1, window_right=0, out=None,
                softmax_lse=None, page_block_size=None, num_heads=None, num_heads_k=None, head_dim=None,
-               stream=None) -> Tuple[object, object]:
-    """pa_varlen_fwd on torch CUDA tensors; returns (out, softmax_lse).
+               stream=None, alibi_slopes=None) -> Tuple[object, object]:
+    """pa_varlen_fwd (pa_varlen_fwd_alibi when ``alibi_slopes`` is given) on torch CUDA
+    tensors; returns (out, softmax_lse).
 
     ``out`` (total_q, H, D) and ``softmax_lse`` (H, total_q) fp32 are allocated with torch
     when not given.  ``max_seqlen_q/k`` must be given (no device read is made to find them).
-    ``page_block_size`` defaults to ``k_cache.shape[1]`` in paged mode.
+    ``page_block_size`` defaults to ``k_cache.shape[1]`` in paged mode.  ``alibi_slopes``:
+    (num_heads,) fp32 CUDA tensor of per-head linear position-bias slopes.
     """
     import torch
     lib = load()
@@ -194,10 +206,14 @@ def varlen_fwd(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table=None
         page_block_size = k_cache.shape[1] if block_table is not None and k_cache.dim() == 4 else 0
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
     ds = [describe(t) for t in (q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, out, softmax_lse)]
-    rc = lib.pa_varlen_fwd(_ref(ds[0]), _ref(ds[1]), _ref(ds[2]), _ref(ds[3]), _ref(ds[4]), _ref(ds[5]),
-                           int(max_seqlen_q), int(max_seqlen_k), int(H), int(Hkv), int(D), int(page_block_size),
-                           float(softmax_scale), int(window_left), int(window_right), _ref(ds[6]), _ref(ds[7]),
-                           ctypes.c_void_p(s.cuda_stream))
+    scalars = (int(max_seqlen_q), int(max_seqlen_k), int(H), int(Hkv), int(D), int(page_block_size),
+               float(softmax_scale), int(window_left), int(window_right))
+    if alibi_slopes is not None:
+        rc = lib.pa_varlen_fwd_alibi(*[_ref(d) for d in ds[:6]], *scalars, _ref(describe(alibi_slopes)),
+                                     _ref(ds[6]), _ref(ds[7]), ctypes.c_void_p(s.cuda_stream))
+    else:
+        rc = lib.pa_varlen_fwd(*[_ref(d) for d in ds[:6]], *scalars, _ref(ds[6]), _ref(ds[7]),
+                               ctypes.c_void_p(s.cuda_stream))
     if rc != 0:
         raise PaError(rc, lib.pa_last_error().decode())
     return out, softmax_lse

@@ -80,7 +80,8 @@ bool is_device_memory(const void* p) {
 int validate(const pa_tensor* q, const pa_tensor* k, const pa_tensor* v, const pa_tensor* cu_q,
              const pa_tensor* cu_k, const pa_tensor* bt, int32_t max_sq, int32_t max_sk, int32_t num_heads,
              int32_t num_heads_k, int32_t head_dim, int32_t page_block_size, float softmax_scale, int32_t wl,
-             int32_t wr, const pa_tensor* out, const pa_tensor* lse, bool check_device, pa::Args* a) {
+             int32_t wr, const pa_tensor* alibi, const pa_tensor* out, const pa_tensor* lse, bool check_device,
+             pa::Args* a) {
     if (!q || !k || !v || !cu_q || !cu_k || !out || !lse)
         return fail(PA_ERR_ARG, "a tensor descriptor is NULL (only block_table may be NULL)");
     const bool paged = bt != nullptr;
@@ -132,6 +133,11 @@ int validate(const pa_tensor* q, const pa_tensor* k, const pa_tensor* v, const p
         if (!(v->shape[0] == num_blocks && v->shape[1] == hkv && v->shape[2] == head_size))
             return fail(PA_ERR_SHAPE, "shape mismatch q %s and v %s", dims(q).c_str(), dims(v).c_str());
     }
+    // -- alibi_slopes (optional): one slope per query head (the "shape mismatch alibi_slopes"
+    // condition the pages list beside the k/v shape checks)
+    if (alibi && (alibi->ndim != 1 || alibi->shape[0] != hq))
+        return fail(PA_ERR_SHAPE, "shape mismatch alibi_slopes %s, expected [%lld]", dims(alibi).c_str(),
+                    (long long)hq);
 
     // -- index tensors
     if (cu_q->ndim != 1) return fail(PA_ERR_ARG, "seqlens_q must be rank 1, got rank %d", cu_q->ndim);
@@ -142,6 +148,7 @@ int validate(const pa_tensor* q, const pa_tensor* k, const pa_tensor* v, const p
         if (bt->ndim != 2) return fail(PA_ERR_ARG, "block_table must be rank 2, got rank %d", bt->ndim);
         if (bt->stride[1] != 1) return fail(PA_ERR_NONCONTIG, "block_table last dimension must be contiguous");
     }
+    if (alibi && alibi->stride[0] != 1) return fail(PA_ERR_NONCONTIG, "alibi_slopes has to be contiguous");
     if (check_device) {  // tensors with no elements are never read or written
         auto on_device = [](const pa_tensor* t) { return numel(t) == 0 || is_device_memory(t->data); };
         if (paged && !on_device(bt)) return fail(PA_ERR_NOT_DEVICE, "block_table must be a cuda tensor");
@@ -152,6 +159,7 @@ int validate(const pa_tensor* q, const pa_tensor* k, const pa_tensor* v, const p
         if (!on_device(v)) return fail(PA_ERR_NOT_DEVICE, "v must be a cuda tensor");
         if (!on_device(out)) return fail(PA_ERR_NOT_DEVICE, "out must be a cuda tensor");
         if (!on_device(lse)) return fail(PA_ERR_NOT_DEVICE, "softmax_lse must be a cuda tensor");
+        if (alibi && !on_device(alibi)) return fail(PA_ERR_NOT_DEVICE, "alibi_slopes must be a cuda tensor");
     }
 
     // -- this library's own argument checks
@@ -161,6 +169,7 @@ int validate(const pa_tensor* q, const pa_tensor* k, const pa_tensor* v, const p
         return fail(PA_ERR_ARG, "q, k, v and out must share one dtype (q %d, k %d, v %d, out %d)", q->dtype,
                     k->dtype, v->dtype, out->dtype);
     if (lse->dtype != PA_F32) return fail(PA_ERR_ARG, "softmax_lse must be f32");
+    if (alibi && alibi->dtype != PA_F32) return fail(PA_ERR_ARG, "alibi_slopes must be f32");
     if (cu_q->dtype != PA_I32 || cu_k->dtype != PA_I32 || (paged && bt->dtype != PA_I32))
         return fail(PA_ERR_ARG, "cu_seqlens and block_table must be int32");
     if (num_heads != hq || head_dim != head_size || num_heads_k != hkv)
@@ -254,6 +263,7 @@ int validate(const pa_tensor* q, const pa_tensor* k, const pa_tensor* v, const p
     a->lse = static_cast<float*>(lse->data);
     a->lse_s0 = lse->stride[0];
     a->total_q = total_q;
+    a->alibi = alibi ? static_cast<const float*>(alibi->data) : nullptr;
     g_msg[0] = '\0';
     return PA_OK;
 }
@@ -513,12 +523,12 @@ int forward_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
                  const pa_tensor* cu_seqlens_q, const pa_tensor* cu_seqlens_k, const pa_tensor* block_table,
                  int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_heads, int32_t num_heads_k,
                  int32_t head_dim, int32_t page_block_size, float softmax_scale, int32_t window_left,
-                 int32_t window_right, const pa_tensor* out, const pa_tensor* softmax_lse, void* stream,
-                 ScratchFn scratch, void* scratch_ctx) {
+                 int32_t window_right, const pa_tensor* alibi_slopes, const pa_tensor* out,
+                 const pa_tensor* softmax_lse, void* stream, ScratchFn scratch, void* scratch_ctx) {
     pa::Args a{};
     int rc = validate(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, max_seqlen_q, max_seqlen_k,
                       num_heads, num_heads_k, head_dim, page_block_size, softmax_scale, window_left, window_right,
-                      out, softmax_lse, true, &a);
+                      alibi_slopes, out, softmax_lse, true, &a);
     if (rc != PA_OK) return rc;
     a.stream = static_cast<cudaStream_t>(stream);
     a.wait_ns = pa::g_wait_ns.load(std::memory_order_relaxed);
@@ -571,10 +581,21 @@ int pa_varlen_check(const pa_tensor* q, const pa_tensor* k_cache, const pa_tenso
                     int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_heads, int32_t num_heads_k,
                     int32_t head_dim, int32_t page_block_size, float softmax_scale, int32_t window_left,
                     int32_t window_right, const pa_tensor* out, const pa_tensor* softmax_lse) {
+    return pa_varlen_check_alibi(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, max_seqlen_q,
+                                 max_seqlen_k, num_heads, num_heads_k, head_dim, page_block_size, softmax_scale,
+                                 window_left, window_right, nullptr, out, softmax_lse);
+}
+
+int pa_varlen_check_alibi(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                          const pa_tensor* cu_seqlens_q, const pa_tensor* cu_seqlens_k, const pa_tensor* block_table,
+                          int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_heads, int32_t num_heads_k,
+                          int32_t head_dim, int32_t page_block_size, float softmax_scale, int32_t window_left,
+                          int32_t window_right, const pa_tensor* alibi_slopes, const pa_tensor* out,
+                          const pa_tensor* softmax_lse) {
     pa::Args a{};
     return validate(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, max_seqlen_q, max_seqlen_k,
-                    num_heads, num_heads_k, head_dim, page_block_size, softmax_scale, window_left, window_right, out,
-                    softmax_lse, false, &a);
+                    num_heads, num_heads_k, head_dim, page_block_size, softmax_scale, window_left, window_right,
+                    alibi_slopes, out, softmax_lse, false, &a);
 }
 
 int pa_varlen_fwd(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
@@ -584,7 +605,20 @@ int pa_varlen_fwd(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor*
                   int32_t window_right, const pa_tensor* out, const pa_tensor* softmax_lse, void* stream) {
     return pa::forward_impl(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, max_seqlen_q,
                             max_seqlen_k, num_heads, num_heads_k, head_dim, page_block_size, softmax_scale,
-                            window_left, window_right, out, softmax_lse, stream, library_workspace, nullptr);
+                            window_left, window_right, nullptr, out, softmax_lse, stream, library_workspace,
+                            nullptr);
+}
+
+int pa_varlen_fwd_alibi(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                        const pa_tensor* cu_seqlens_q, const pa_tensor* cu_seqlens_k, const pa_tensor* block_table,
+                        int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_heads, int32_t num_heads_k,
+                        int32_t head_dim, int32_t page_block_size, float softmax_scale, int32_t window_left,
+                        int32_t window_right, const pa_tensor* alibi_slopes, const pa_tensor* out,
+                        const pa_tensor* softmax_lse, void* stream) {
+    return pa::forward_impl(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, max_seqlen_q,
+                            max_seqlen_k, num_heads, num_heads_k, head_dim, page_block_size, softmax_scale,
+                            window_left, window_right, alibi_slopes, out, softmax_lse, stream, library_workspace,
+                            nullptr);
 }
 
 const char* pa_last_error(void) { return g_msg; }

@@ -25,8 +25,8 @@ struct DecCfg {
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
     static constexpr int Q_BYTES = CH * M * 128;
     static constexpr int OFF_Q = STAGES * STAGE_BYTES;
-    static constexpr int OFF_ROW = OFF_Q + Q_BYTES;            // row_lo[M], row_hi[M]
-    static constexpr int OFF_ML = OFF_ROW + 2 * M * 4;         // m[4][16], l[4][16] of the merge
+    static constexpr int OFF_ROW = OFF_Q + Q_BYTES;            // row_lo[M], row_hi[M], row_dg[M], row_ab[M]
+    static constexpr int OFF_ML = OFF_ROW + 4 * M * 4;         // m[4][16], l[4][16] of the merge
     static constexpr int OFF_BAR = (OFF_ML + 2 * 4 * 16 * 4 + 15) & ~15;
     static constexpr int OFF_FLAG = OFF_BAR + 2 * STAGES * 8;
     static constexpr int OFF_IDS = OFF_FLAG + 16;              // block id of every TMA box of the split
@@ -74,6 +74,8 @@ __global__ void __launch_bounds__(160) decode_kernel(const __grid_constant__ CUt
 
     int* row_lo = reinterpret_cast<int*>(smem + C::OFF_ROW);
     int* row_hi = row_lo + M;
+    int* row_dg = row_hi + M;
+    float* row_ab = reinterpret_cast<float*>(row_dg + M);
     float* m_sm = reinterpret_cast<float*>(smem + C::OFF_ML);
     float* l_sm = m_sm + 4 * 16;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -81,15 +83,20 @@ __global__ void __launch_bounds__(160) decode_kernel(const __grid_constant__ CUt
     volatile uint32_t* abort_flag = reinterpret_cast<uint32_t*>(smem + C::OFF_FLAG);
 
     if (tid < M) {
-        int lo = 0, hi = -1;  // padding rows attend nothing
+        int lo = 0, hi = -1, dg = 0;  // padding rows attend nothing
+        float ab = 0.f;
         if (tid < tv.rows) {
             const int64_t i = (tv.row0 + tid) / p.G;
             const int64_t diag = i + tv.sk - tv.sq;
             lo = p.wl >= 0 ? (int)max64(0, diag - p.wl) : 0;
             hi = p.wr >= 0 ? (int)max64(-1, min64(tv.sk - 1, diag + p.wr)) : tv.sk - 1;
+            dg = (int)diag;
+            if (p.alibi) ab = p.alibi[hk * p.G + (int)(tv.row0 + tid - i * p.G)] * kLog2e;
         }
         row_lo[tid] = lo;
         row_hi[tid] = hi;
+        row_dg[tid] = dg;
+        row_ab[tid] = ab;
     }
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -176,6 +183,8 @@ __global__ void __launch_bounds__(160) decode_kernel(const __grid_constant__ CUt
     const int mi = lane >> 3, rr = lane & 7;
     const int r0 = rg * 16 + gq, r1 = r0 + 8;  // the two rows this lane holds
     const int lo0 = row_lo[r0], hi0 = row_hi[r0], lo1 = row_lo[r1], hi1 = row_hi[r1];
+    const int dg0 = row_dg[r0], dg1 = row_dg[r1];
+    const float ab0 = row_ab[r0], ab1 = row_ab[r1];
     const uint32_t q_base = smem_addr(smem + C::OFF_Q);
 
     uint32_t qf[C::Q_IN_REGS ? DP / 16 : 1][4];
@@ -253,7 +262,7 @@ __global__ void __launch_bounds__(160) decode_kernel(const __grid_constant__ CUt
                     const int key = kt + kk0 + n * 8 + tq * 2 + (e & 1);
                     const bool up = e < 2;
                     const bool in = up ? (key >= lo0 && key <= hi0) : (key >= lo1 && key <= hi1);
-                    s[n][e] = in ? s[n][e] * p.scale_log2 : -INFINITY;
+                    s[n][e] = in ? biased_log2(s[n][e], p.scale_log2, up ? ab0 : ab1, up ? dg0 : dg1, key) : -INFINITY;
                     if (up)
                         mx0 = fmaxf(mx0, s[n][e]);
                     else

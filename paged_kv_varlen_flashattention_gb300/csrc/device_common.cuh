@@ -231,22 +231,13 @@ __device__ __forceinline__ void fadd2_acc(float& d0, float& d1, float a0, float 
         : "f"(a0), "f"(a1));
 }
 
-// 2^x on the FMA/ALU pipes, to take part of the softmax exponentials off MUFU.
-// Cody-Waite style range reduction x = n + f with n = round(x) (by adding and removing
-// 1.5 * 2^23, which leaves n in the low mantissa bits) and f in [-1/2, 1/2]; 2^f by a
-// degree-3 polynomial whose coefficients were fitted by the Remez exchange algorithm to
-// minimise the relative error on [-1/2, 1/2] (max 7.5e-5, below the rounding of the
-// 16-bit P it feeds); 2^n by adding n to the exponent field.  x is clamped below at -126
-// (the result is then ~0); x = -inf gives ~0 as well.
-__device__ __forceinline__ float poly_exp2(float x) {
-    x = fmaxf(x, -126.f);
-    const float t = x + 12582912.f;
-    const float n = t - 12582912.f;
-    const float f = x - n;
-    float p = fmaf(0.0551716685f, f, 0.242611125f);
-    p = fmaf(p, f, 0.693260968f);
-    p = fmaf(p, f, 0.999928057f);
-    return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Score of one (row, key) pair in the log2 domain with the linear position bias:
+// s * scale_log2 - ab * |dg - key|, where ab = slope * log2(e) (0 without a bias) and dg is
+// the row's bottom-right aligned diagonal key.  With ab = 0 this is exactly s * scale_log2.
+__device__ __forceinline__ float biased_log2(float s, float scale_log2, float ab, int dg, int key) {
+    return fmaf(-ab, fabsf((float)(dg - key)), s * scale_log2);
 }
 
 // Byte offset of 16-byte unit `u` (0..7) of row `r` in a tile whose rows are 128 bytes

@@ -71,5 +71,6 @@ extern "C" int pa_varlen_fwd_noalloc(const pa_tensor* q, const pa_tensor* k_cach
                                      void* stream) {
     return pa::forward_impl(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, max_seqlen_q,
                             max_seqlen_k, num_heads, num_heads_k, head_dim, page_block_size, softmax_scale,
-                            window_left, window_right, out, softmax_lse, stream, pa::static_scratch, nullptr);
+                            window_left, window_right, nullptr, out, softmax_lse, stream, pa::static_scratch,
+                            nullptr);
 }

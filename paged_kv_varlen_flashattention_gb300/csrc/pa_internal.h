@@ -43,6 +43,7 @@ struct Args {
     cudaStream_t stream;
     uint64_t wait_ns;    // bound on every in-kernel wait
     int withhold_loads;  // test hook: producers issue no loads
+    const float* alibi;  // per-query-head slopes of the linear position bias, or nullptr
 };
 
 // Scratch the split-KV path needs for a call (bytes), and where to put it.
@@ -99,8 +100,8 @@ int forward_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
                  const pa_tensor* cu_seqlens_q, const pa_tensor* cu_seqlens_k, const pa_tensor* block_table,
                  int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_heads, int32_t num_heads_k,
                  int32_t head_dim, int32_t page_block_size, float softmax_scale, int32_t window_left,
-                 int32_t window_right, const pa_tensor* out, const pa_tensor* softmax_lse, void* stream,
-                 ScratchFn scratch, void* scratch_ctx);
+                 int32_t window_right, const pa_tensor* alibi_slopes, const pa_tensor* out,
+                 const pa_tensor* softmax_lse, void* stream, ScratchFn scratch, void* scratch_ctx);
 
 // Tensor-map encoding through the driver entry point (no libcuda link needed).
 // Rank-4 bf16/f16 map over (d0 fastest .. d3), strides in bytes for dims 1..3.

@@ -39,12 +39,6 @@ constexpr int kPrefillThreads = 384;  // three warpgroups
 // issuers, V producer) drops to 72 and the two softmax warpgroups rise to 216:
 // 128 x 72 + 256 x 216 = 64,512, the launch total.
 constexpr int kRegsControl = 72, kRegsSoftmax = 216;
-#ifndef PA_POLY_EVERY
-#define PA_POLY_EVERY 0
-#endif
-// One softmax pair in kPolyEvery takes its exponentials on the FMA pipe (poly_exp2);
-// 0 (the default) keeps them all on MUFU, which measured faster.
-constexpr int kPolyEvery = PA_POLY_EVERY;
 
 struct PrefillParams {
     void* out;
@@ -63,6 +57,7 @@ struct PrefillParams {
     int max_sq, max_sk;
     float scale_log2;
     int wl, wr;
+    const float* alibi;  // per-query-head slopes of the linear position bias, or nullptr
     int rows_cap;
     int pairs;  // grid.x: an upper bound of the number of tile pairs
     unsigned int* err;
@@ -136,7 +131,9 @@ __device__ __forceinline__ void issue_kv_tile(const PrefillParams& p, const CUte
     }
 }
 
-template <typename T, int DP>
+// ALIBI: the scores carry the linear position bias -slope_h * |diagonal - key| (a separate
+// instantiation, so the unbiased softmax has no extra arithmetic).
+template <typename T, int DP, bool ALIBI>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -431,6 +428,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         struct TileRows {
             int lo[2], hi[2];  // attended key range of each row (empty for padding rows)
             float m[2], l[2];  // running max (log2 domain) and this thread's share of the sum
+            int dg[2];         // the row's bottom-right aligned diagonal key (ALIBI)
+            float ab[2];       // its bias slope times log2(e) (ALIBI)
         };
         auto init_rows = [&](int x, TileRows& st) {
 #pragma unroll
@@ -438,10 +437,16 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 const int64_t rho = row0 + x * 128 + lb + gid + 8 * q;
                 st.lo[q] = 0;
                 st.hi[q] = -1;
+                st.dg[q] = 0;
+                st.ab[q] = 0.f;
                 if (rho < rows_total) {
                     const int64_t diag = rho / p.G + cdiag;
                     st.lo[q] = p.wl >= 0 ? (int)max64(0, diag - p.wl) : 0;
                     st.hi[q] = p.wr >= 0 ? (int)max64(-1, min64((int64_t)sk - 1, diag + p.wr)) : sk - 1;
+                    if (ALIBI) {
+                        st.dg[q] = (int)diag;
+                        st.ab[q] = p.alibi[hk * p.G + (int)(rho - (rho / p.G) * p.G)] * kLog2e;
+                    }
                 }
                 st.m[q] = -INFINITY;
                 st.l[q] = 0.f;
@@ -484,11 +489,27 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                             v = (key >= st.lo[q] && key <= st.hi[q]) ? v : -INFINITY;
                         }
             }
+            // With the position bias, S becomes the biased score in the log2 domain here and
+            // the rest runs with a unit scale.
+            float sl = p.scale_log2;  // softmax_scale > 0 on this path
+            if (ALIBI) {
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const float d0 = (float)(st.dg[q] - kt - 2 * tig);  // distance of key kt + 2 tig
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            float& v = sv[4 * k + 2 * q + e];
+                            v = fmaf(-st.ab[q], fabsf(d0 - (float)(8 * k + e)), v * sl);
+                        }
+                }
+                sl = 1.f;
+            }
             // Running max: each thread first checks its own 32 keys of each row against the
             // running max; only when some row of the warp grew past it by more than 2^8 (the
             // first tile, or a jump in the scores) are the exact row maxima taken over the quad
             // and O rescaled.
-            const float sl = p.scale_log2;  // softmax_scale > 0 on this path
             float lm[2];
             bool grow = false;
 #pragma unroll
@@ -619,7 +640,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     }
 }
 
-template <typename T, int DP>
+template <typename T, int DP, bool ALIBI>
 int run_prefill(const Args& a, const PrefillParams& pp, cudaStream_t stream, char* msg, size_t msg_len) {
     using C = PfCfg<DP>;
     // tensor maps: q as (D, H, total_q, 1), box (64, G, 128 / G, 1); K/V as in the split-KV path
@@ -656,7 +677,7 @@ int run_prefill(const Args& a, const PrefillParams& pp, cudaStream_t stream, cha
         rc = encode_tmap_4d(&tv, a.dtype, a.v, dims, strides, box, 1, msg, msg_len);
         if (rc != PA_OK) return rc;
     }
-    auto kern = prefill_kernel<T, DP>;
+    auto kern = prefill_kernel<T, DP, ALIBI>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -724,6 +745,7 @@ int launch_prefill(const Args& a, unsigned int* err, char* msg, size_t msg_len) 
     pp.max_sq = a.max_sq;
     pp.max_sk = a.max_sk;
     pp.scale_log2 = a.scale * 1.4426950408889634f;
+    pp.alibi = a.alibi;
     pp.wl = a.wl;
     pp.wr = a.wr;
     pp.rows_cap = prefill_rows_threshold();
@@ -734,12 +756,19 @@ int launch_prefill(const Args& a, unsigned int* err, char* msg, size_t msg_len) 
     pp.wait_ns = a.wait_ns;
     pp.withhold = a.withhold_loads;
     const int dp = a.D <= 64 ? 64 : 128;
+    const bool alibi = a.alibi != nullptr;
     if (a.dtype == PA_BF16) {
-        return dp == 64 ? run_prefill<__nv_bfloat16, 64>(a, pp, a.stream, msg, msg_len)
-                        : run_prefill<__nv_bfloat16, 128>(a, pp, a.stream, msg, msg_len);
+        if (alibi)
+            return dp == 64 ? run_prefill<__nv_bfloat16, 64, true>(a, pp, a.stream, msg, msg_len)
+                            : run_prefill<__nv_bfloat16, 128, true>(a, pp, a.stream, msg, msg_len);
+        return dp == 64 ? run_prefill<__nv_bfloat16, 64, false>(a, pp, a.stream, msg, msg_len)
+                        : run_prefill<__nv_bfloat16, 128, false>(a, pp, a.stream, msg, msg_len);
     }
-    return dp == 64 ? run_prefill<__half, 64>(a, pp, a.stream, msg, msg_len)
-                    : run_prefill<__half, 128>(a, pp, a.stream, msg, msg_len);
+    if (alibi)
+        return dp == 64 ? run_prefill<__half, 64, true>(a, pp, a.stream, msg, msg_len)
+                        : run_prefill<__half, 128, true>(a, pp, a.stream, msg, msg_len);
+    return dp == 64 ? run_prefill<__half, 64, false>(a, pp, a.stream, msg, msg_len)
+                    : run_prefill<__half, 128, false>(a, pp, a.stream, msg, msg_len);
 }
 
 }  // namespace pa

@@ -41,6 +41,7 @@ struct SplitParams {
     int max_sq, max_sk;
     float scale_log2;
     int wl, wr;
+    const float* alibi;  // per-query-head slopes of the linear position bias, or nullptr
     int rows_cap, row_tiles, split_tiles, max_splits;
     float* part_o;
     float* part_lse;
@@ -116,8 +117,9 @@ struct SplitCfg {
     static constexpr int OFF_Q = STAGES * STAGE_BYTES;
     static constexpr int OFF_P = OFF_Q + Q_BYTES;
     static constexpr int OFF_S = OFF_P + P_BYTES;
-    static constexpr int OFF_ROW = OFF_S + S_BYTES;  // row_lo[M], row_hi[M], alpha[M], m[M], l[M]
-    static constexpr int OFF_BAR = (OFF_ROW + 5 * M * 4 + 15) & ~15;
+    // row_lo[M], row_hi[M], alpha[M], m[M], l[M], row_dg[M], row_ab[M]
+    static constexpr int OFF_ROW = OFF_S + S_BYTES;
+    static constexpr int OFF_BAR = (OFF_ROW + 7 * M * 4 + 15) & ~15;
     static constexpr int SMEM = OFF_BAR + STAGES * 8 + 1024;  // + slack for 1024-byte alignment
     static constexpr int KW = NT / 4;               // keys per warp in Q.K^T
     static constexpr int DW = DP / 4;               // output columns per warp in P.V
@@ -150,20 +152,27 @@ __global__ void __launch_bounds__(128) splitkv_kernel(const __grid_constant__ CU
     float* alpha_sm = reinterpret_cast<float*>(row_hi + M);
     float* m_sm = alpha_sm + M;
     float* l_sm = m_sm + M;
+    int* row_dg = reinterpret_cast<int*>(l_sm + M);
+    float* row_ab = reinterpret_cast<float*>(row_dg + M);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     float* S = reinterpret_cast<float*>(smem + C::OFF_S);
     uint8_t* Ps = smem + C::OFF_P;
 
     if (tid < M) {
-        int lo = 0, hi = -1;  // padding rows attend nothing
+        int lo = 0, hi = -1, dg = 0;  // padding rows attend nothing
+        float ab = 0.f;
         if (tid < tv.rows) {
             const int64_t i = (tv.row0 + tid) / p.G;
             const int64_t diag = i + tv.sk - tv.sq;
             lo = p.wl >= 0 ? (int)max64(0, diag - p.wl) : 0;
             hi = p.wr >= 0 ? (int)max64(-1, min64(tv.sk - 1, diag + p.wr)) : tv.sk - 1;
+            dg = (int)diag;
+            if (p.alibi) ab = p.alibi[hk * p.G + (int)(tv.row0 + tid - i * p.G)] * kLog2e;
         }
         row_lo[tid] = lo;
         row_hi[tid] = hi;
+        row_dg[tid] = dg;
+        row_ab[tid] = ab;
     }
     if (tid == 0) {
         prefetch_tmap(&tm_k);
@@ -314,10 +323,14 @@ __global__ void __launch_bounds__(128) splitkv_kernel(const __grid_constant__ CU
                     const int r = mt * 16 + (lane >> 2) + h2 * 8;
                     const int col = warp * C::KW + n * 8 + (lane & 3) * 2;
                     const int j = kt + col;
-                    const int lo = row_lo[r], hi = row_hi[r];
+                    const int lo = row_lo[r], hi = row_hi[r], dg = row_dg[r];
+                    const float ab = row_ab[r];
                     float2 sv;
-                    sv.x = (j >= lo && j <= hi) ? s_acc[mt][n][h2 * 2] * p.scale_log2 : -INFINITY;
-                    sv.y = (j + 1 >= lo && j + 1 <= hi) ? s_acc[mt][n][h2 * 2 + 1] * p.scale_log2 : -INFINITY;
+                    sv.x = (j >= lo && j <= hi) ? biased_log2(s_acc[mt][n][h2 * 2], p.scale_log2, ab, dg, j)
+                                                : -INFINITY;
+                    sv.y = (j + 1 >= lo && j + 1 <= hi)
+                               ? biased_log2(s_acc[mt][n][h2 * 2 + 1], p.scale_log2, ab, dg, j + 1)
+                               : -INFINITY;
                     *reinterpret_cast<float2*>(S + r * C::S_STRIDE + col) = sv;
                 }
         if (__syncthreads_or(!ok)) {

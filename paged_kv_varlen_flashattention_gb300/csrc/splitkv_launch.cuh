@@ -187,6 +187,7 @@ static int launch_splitkv_t(const Args& a, const SplitPlan& plan, void* workspac
     sp.max_sq = a.max_sq;
     sp.max_sk = a.max_sk;
     sp.scale_log2 = a.scale * 1.4426950408889634f;
+    sp.alibi = a.alibi;
     sp.wl = a.wl;
     sp.wr = a.wr;
     sp.rows_cap = plan.rows_cap;

@@ -42,12 +42,20 @@ def sample_rows(lay, limit, seed=0):
     return np.unique(np.concatenate([np.array(must, dtype=np.int64), extra.astype(np.int64)]))
 
 
-def oracle_for(inp_cpu: workloads.Inputs, rows=None):
+def oracle_for(inp_cpu: workloads.Inputs, rows=None, alibi_slopes=None):
     lay = inp_cpu.layout
     bt = inp_cpu.block_table.numpy() if inp_cpu.block_table is not None else None
     return oracle.attention(lay.dtype, inp_cpu.q, inp_cpu.k_cache, inp_cpu.v_cache,
                             inp_cpu.cu_seqlens_q.numpy(), inp_cpu.cu_seqlens_k.numpy(), bt, lay.softmax_scale,
-                            lay.window_left, lay.window_right, rows=rows)
+                            lay.window_left, lay.window_right, rows=rows, alibi_slopes=alibi_slopes)
+
+
+def alibi_slopes(num_heads, kind="geometric", seed=0):
+    """Slopes for the linear position bias: the usual geometric sequence 2^(-8 (h + 1) / H),
+    or seeded uniform values in [0, 0.5) ("random"), as float32."""
+    if kind == "geometric":
+        return np.array([2.0 ** (-8.0 * (h + 1) / num_heads) for h in range(num_heads)], dtype=np.float32)
+    return (np.random.default_rng(seed).random(num_heads) * 0.5).astype(np.float32)
 
 
 def compare(lay, out, lse, ref_o, ref_l, rows=None):
@@ -72,11 +80,14 @@ def compare(lay, out, lse, ref_o, ref_l, rows=None):
     return float(err.max()), float(lerr.max())
 
 
-def check_layout(lay, limit=1 << 30, gen_device="cuda", seed_rows=0, **overrides):
-    """Materialise ``lay``, run the CUDA path, and check (sampled) rows against the oracle."""
+def check_layout(lay, limit=1 << 30, gen_device="cuda", seed_rows=0, alibi=None, **overrides):
+    """Materialise ``lay``, run the CUDA path, and check (sampled) rows against the oracle.
+    ``alibi``: optional float32 numpy slopes (one per query head) given to both sides."""
     inp_gpu = workloads.materialize(lay, device=gen_device).to("cuda")
+    if alibi is not None:
+        overrides["alibi_slopes"] = torch.from_numpy(np.asarray(alibi, dtype=np.float32)).to("cuda")
     out, lse = run_cuda(inp_gpu, **overrides)
     inp_cpu = inp_gpu.to("cpu")
     rows = sample_rows(lay, limit, seed_rows)
-    ref_o, ref_l = oracle_for(inp_cpu, rows)
+    ref_o, ref_l = oracle_for(inp_cpu, rows, alibi_slopes=None if alibi is None else np.asarray(alibi, np.float64))
     return compare(lay, out, lse, ref_o, ref_l, rows)

@@ -180,3 +180,54 @@ def test_kernel_timing_counts_each_class():
         t = binding.kernel_times()
         assert t[cls][1] >= 3 and t[cls][0] > 0.0, (name, t)
         assert binding.kernel_times() == {k: (0.0, 0) for k in binding.KERNEL_CLASSES}
+
+
+# ---- linear position bias (alibi_slopes) ----------------------------------------------------
+
+@pytest.mark.parametrize("name", ["decode", "prefill", "mixed", "long", "d512"])
+def test_alibi_reduced_workloads_all_rows(name):
+    lay = workloads.small(name)
+    _gpu.check_layout(lay, alibi=_gpu.alibi_slopes(lay.num_heads))
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_alibi_head_dims_random_slopes(D):
+    """Random slopes under GQA; prefill rows (tensor-core kernel up to D = 128), long-query
+    rows past it and decode rows in one batch."""
+    _gpu.check_layout(_custom([150, 1, 40, 1], [150, 300, 700, 64], H=8, Hkv=2, D=D),
+                      alibi=_gpu.alibi_slopes(8, "random", seed=D))
+
+
+def test_alibi_windows_and_fp16():
+    lay = _custom([200, 33, 1], [260, 33, 500], H=4, Hkv=1, D=128, dtype="f16", wl=50, wr=7)
+    _gpu.check_layout(lay, alibi=_gpu.alibi_slopes(4))
+
+
+@pytest.mark.parametrize("tiles", [1, 3])
+def test_alibi_forced_splits(tiles, monkeypatch):
+    """Split-KV partials and the combine carry the bias (a split count forced small)."""
+    monkeypatch.setenv("PA_SPLIT_TILES", str(tiles))
+    lay = workloads.small("decode")
+    _gpu.check_layout(lay, alibi=_gpu.alibi_slopes(lay.num_heads, "random", seed=7))
+
+
+def test_alibi_zero_slopes_match_no_bias():
+    lay = workloads.small("mixed")
+    _gpu.check_layout(lay, alibi=np.zeros(lay.num_heads, dtype=np.float32))
+
+
+@pytest.mark.parametrize("name,limit", [("decode_bf16", 1024), ("prefill_bf16", 768)])
+def test_alibi_full_size_sampled_rows(name, limit):
+    lay = workloads.CONFIGS[name]()
+    _gpu.check_layout(lay, limit=limit, alibi=_gpu.alibi_slopes(lay.num_heads))
+
+
+def test_alibi_slopes_on_host_are_rejected():
+    lay = workloads.small("decode")
+    lay.nan_fill = False
+    g = workloads.materialize(lay, device="cuda")
+    with pytest.raises(binding.PaError) as ei:
+        binding.varlen_fwd(g.q, g.k_cache, g.v_cache, g.cu_seqlens_q, g.cu_seqlens_k, g.block_table,
+                           max_seqlen_q=lay.max_seqlen_q, max_seqlen_k=lay.max_seqlen_k,
+                           alibi_slopes=torch.zeros(lay.num_heads, dtype=torch.float32))
+    assert ei.value.name == "PA_ERR_NOT_DEVICE"

@@ -159,3 +159,31 @@ def test_check_order_follows_the_pages():
     ds, H, Hkv, D, P = build({"q": [8, 4, 576], "k": [6, 16, 2, 576], "v": [6, 16, 2, 576], "out": [8, 4, 576],
                               "head_dim": 576, "page_block_size": 16})
     assert run_check(ds, H, Hkv, D, P)[0] == CODES["PA_ERR_PAGE_MULT32"]
+
+
+def run_check_alibi(ds, alibi, H, Hkv, D, P, max_sq=5, max_sk=64, wl=-1, wr=0, scale=0.125):
+    lib = binding.load()
+    r = lambda d: None if d is None else binding.ctypes.byref(d)  # noqa: E731
+    rc = lib.pa_varlen_check_alibi(r(ds[0]), r(ds[1]), r(ds[2]), r(ds[3]), r(ds[4]), r(ds[5]), max_sq, max_sk, H,
+                                   Hkv, D, P, scale, wl, wr, r(alibi), r(ds[6]), r(ds[7]))
+    return rc, lib.pa_last_error().decode()
+
+
+def test_alibi_slopes_checks():
+    """alibi_slopes: one f32 slope per query head.  The shape condition carries the text of
+    the "shape mismatch alibi_slopes {:?}, expected {:?}" related error of "paged flash-attn
+    requires page_block_size to be a multiple of 32"; NULL behaves as pa_varlen_check."""
+    ds, H, Hkv, D, P = _base()
+    assert run_check_alibi(ds, None, H, Hkv, D, P) == run_check(ds, H, Hkv, D, P)
+    assert run_check_alibi(ds, desc([H], binding.PA_F32), H, Hkv, D, P)[0] == 0
+    for bad in ([H + 1], [H - 1], [1, H], [H, 1]):
+        rc, msg = run_check_alibi(ds, desc(bad, binding.PA_F32), H, Hkv, D, P)
+        assert rc == CODES["PA_ERR_SHAPE"] and "shape mismatch alibi_slopes" in msg and f"expected [{H}]" in msg
+    rc, msg = run_check_alibi(ds, desc([H], binding.PA_F32, [2]), H, Hkv, D, P)
+    assert rc == CODES["PA_ERR_NONCONTIG"] and "alibi_slopes" in msg
+    rc, msg = run_check_alibi(ds, desc([H], binding.PA_BF16), H, Hkv, D, P)
+    assert rc == CODES["PA_ERR_ARG"] and "alibi_slopes must be f32" in msg
+    # the q/k/v conditions of the pages come first: a rank error wins over a bad alibi shape
+    bad_q = list(ds)
+    bad_q[0] = desc([8, 4, 64, 1], binding.PA_BF16)
+    assert run_check_alibi(bad_q, desc([H + 1], binding.PA_F32), H, Hkv, D, P)[0] == CODES["PA_ERR_RANK"]
