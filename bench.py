@@ -76,7 +76,8 @@ def workload_config(lay, flops, nbytes, world):
             "page_block_size": lay.page_block_size, "max_seqlen_k": lay.max_seqlen_k,
             "total_keys": lay.total_k, "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
             "l2": "inputs larger than L2 (no flush)" if nbytes > 2 * L2_BYTES else "L2 not flushed; inputs fit",
-            "parallelism": f"replicas{world}"}
+            "parallelism": f"replicas{world}",
+            **({"alibi_slopes": "2^(-8 (h + 1) / H)"} if ALIBI["slopes"] is not None else {})}
 
 
 def headline_unit(flops, nbytes):
@@ -205,11 +206,36 @@ class ClockSampler:
 
 # ---- the measured arm ----------------------------------------------------------------------------
 
+ALIBI = {"slopes": None}  # set by --alibi: per-head slopes (numpy float32) given to every leg
+
+
+def alibi_slopes(num_heads):
+    """The usual geometric slopes of the linear position bias, 2^(-8 (h + 1) / H)."""
+    return np.array([2.0 ** (-8.0 * (h + 1) / num_heads) for h in range(num_heads)], dtype=np.float32)
+
+
+def set_alibi(args, lay):
+    ALIBI.clear()
+    ALIBI["slopes"] = alibi_slopes(lay.num_heads) if getattr(args, "alibi", False) else None
+
+
+def _slopes_on(device):
+    import torch
+    s = ALIBI["slopes"]
+    if s is None:
+        return None
+    key = f"t_{device}"
+    if key not in ALIBI:
+        ALIBI[key] = torch.from_numpy(s).to(device)
+    return ALIBI[key]
+
+
 def _call(binding, g, lay, out, lse, stream=None):
     binding.varlen_fwd(g.q, g.k_cache, g.v_cache, g.cu_seqlens_q, g.cu_seqlens_k, g.block_table,
                        max_seqlen_q=lay.max_seqlen_q, max_seqlen_k=lay.max_seqlen_k,
                        softmax_scale=lay.softmax_scale, window_left=lay.window_left,
-                       window_right=lay.window_right, out=out, softmax_lse=lse, stream=stream)
+                       window_right=lay.window_right, out=out, softmax_lse=lse, stream=stream,
+                       alibi_slopes=_slopes_on(g.q.device))
 
 
 def time_device(binding, g, lay, steps, warmup, dist):
@@ -243,8 +269,9 @@ def time_e2e(binding, g, lay, steps, warmup):
     """Same step through the public call with host-resident inputs: pinned host -> device
     copies of every input, the call, and device -> host copies of out and lse, all timed."""
     import torch
+    sl = _slopes_on("cpu")
     host = [t.cpu().pin_memory() if t is not None else None
-            for t in (g.q, g.k_cache, g.v_cache, g.cu_seqlens_q, g.cu_seqlens_k, g.block_table)]
+            for t in (g.q, g.k_cache, g.v_cache, g.cu_seqlens_q, g.cu_seqlens_k, g.block_table, sl)]
     dev = [torch.empty_like(t, device="cuda") if t is not None else None for t in host]
     out_h = torch.empty(g.q.shape, dtype=g.q.dtype).pin_memory()
     lse_h = torch.empty((lay.num_heads, lay.total_q), dtype=torch.float32).pin_memory()
@@ -260,7 +287,7 @@ def time_e2e(binding, g, lay, steps, warmup):
         binding.varlen_fwd(dev[0], dev[1], dev[2], dev[3], dev[4], dev[5], max_seqlen_q=lay.max_seqlen_q,
                            max_seqlen_k=lay.max_seqlen_k, softmax_scale=lay.softmax_scale,
                            window_left=lay.window_left, window_right=lay.window_right, out=out_d,
-                           softmax_lse=lse_d)
+                           softmax_lse=lse_d, alibi_slopes=dev[6])
         out_h.copy_(out_d, non_blocking=True)
         lse_h.copy_(lse_d, non_blocking=True)
 
@@ -298,7 +325,7 @@ def cpu_baseline(lay, inp_cpu, budget_s=20.0):
             t0 = time.perf_counter()
             oracle.attention(lay.dtype, inp_cpu.q, inp_cpu.k_cache, inp_cpu.v_cache, inp_cpu.cu_seqlens_q.numpy(),
                              inp_cpu.cu_seqlens_k.numpy(), bt, lay.softmax_scale, lay.window_left,
-                             lay.window_right, rows=rows)
+                             lay.window_right, rows=rows, alibi_slopes=ALIBI["slopes"])
             t_total += time.perf_counter() - t0
             f_b, b_b = algorithmic(lay, [b])
             nflops += f_b
@@ -335,6 +362,7 @@ def run_ours(args):
 
     lay = workloads.CONFIGS[args.workload]()
     lay.nan_fill = False
+    set_alibi(args, lay)
     g = workloads.materialize(lay, device="cuda")
     flops, nbytes = algorithmic(lay)
     hbm, bf16, bf16_sus, peak_kind = peaks()
@@ -412,6 +440,7 @@ def run_ours(args):
         try:
             lay2 = workloads.CONFIGS["prefill_bf16"]()
             lay2.nan_fill = False
+            set_alibi(args, lay2)
             g2 = workloads.materialize(lay2, device="cuda")
             f2, b2 = algorithmic(lay2)
             ms2, l2 = time_device(binding, g2, lay2, 3, 2, None)
@@ -430,6 +459,7 @@ def run_ours(args):
             del g2
         except Exception as e:  # reported, not hidden
             result["secondary"] = {"error": str(e)[:300]}
+        set_alibi(args, lay)
     if rank == 0 and not args.no_cpu_baseline:
         inp_cpu = g.to("cpu")
         val, cunit, secs, cores, sample = cpu_baseline(lay, inp_cpu, budget_s=args.cpu_budget)
@@ -452,6 +482,7 @@ def run_reference(args):
 
     lay = workloads.CONFIGS[args.workload]()
     lay.nan_fill = False
+    set_alibi(args, lay)
     inp = workloads.materialize(lay, device="cpu")
     cq, _ = lay.cu_seqlens()
     bt = inp.block_table.numpy() if inp.block_table is not None else None
@@ -467,7 +498,7 @@ def run_reference(args):
     def step():
         oracle.attention(lay.dtype, inp.q, inp.k_cache, inp.v_cache, inp.cu_seqlens_q.numpy(),
                          inp.cu_seqlens_k.numpy(), bt, lay.softmax_scale, lay.window_left, lay.window_right,
-                         rows=rows)
+                         rows=rows, alibi_slopes=ALIBI["slopes"])
 
     for _ in range(args.warmup):
         step()
@@ -497,6 +528,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_bf16")
+    ap.add_argument("--alibi", action="store_true",
+                    help="run every leg with the linear position bias (geometric per-head slopes)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
