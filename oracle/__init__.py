@@ -7,7 +7,9 @@ and shares no code with the CUDA library.
 
 Parity pins: every function here is pinned by ``tests/test_oracle.py`` against
 closed forms, library routines (numpy masks, torch SDPA in float64) and
-invariances; none is "parity unpinned".
+invariances; none is "parity unpinned".  ``kv_append`` (a plain numpy scatter) is
+pinned by a gather through the block table written independently in the tests and by
+the attention oracle's non-paged mode.
 """
 from __future__ import annotations
 
@@ -160,3 +162,37 @@ def attention(dtype, q, k, v, cu_seqlens_q, cu_seqlens_k, block_table, softmax_s
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return out, lse
+
+
+def kv_append(k_new, v_new, cu_seqlens_new, cu_seqlens_k, block_table, k_cache, v_cache):
+    """Writes new key/value rows into a paged cache, in place (numpy arrays, any dtype).
+
+    Sequence b owns sk_b = cu_seqlens_k[b+1] - cu_seqlens_k[b] keys after the append, the
+    last n_b = cu_seqlens_new[b+1] - cu_seqlens_new[b] of which are its new tokens (the same
+    bottom-right alignment as the mask: new token t sits at key position sk_b - n_b + t).
+    Logical position j lives at slot j mod P of block block_table[b, j // P] ("flash-attn-
+    varlen paged expects k/v tensors of rank 4", What it means: the block table maps a
+    sequence's logical pages to physical blocks of the (num_blocks, P, Hkv, D) caches).
+
+    k_new, v_new: (total_new, Hkv, D); k_cache, v_cache: (num_blocks, P, Hkv, D), modified.
+    Raises ValueError when a sequence has more new tokens than keys, or a position falls
+    outside the block table or the pool.
+    """
+    cu_new = np.asarray(cu_seqlens_new, dtype=np.int64)
+    cu_k = np.asarray(cu_seqlens_k, dtype=np.int64)
+    bt = np.asarray(block_table, dtype=np.int64)
+    P = k_cache.shape[1]
+    for b in range(len(cu_new) - 1):
+        n_b = int(cu_new[b + 1] - cu_new[b])
+        sk_b = int(cu_k[b + 1] - cu_k[b])
+        if n_b > sk_b:
+            raise ValueError(f"sequence {b}: {n_b} new tokens but only {sk_b} keys")
+        for t in range(n_b):
+            j = sk_b - n_b + t
+            if j // P >= bt.shape[1]:
+                raise ValueError(f"sequence {b}: position {j} is past its block table row")
+            blk = int(bt[b, j // P])
+            if not 0 <= blk < k_cache.shape[0]:
+                raise ValueError(f"sequence {b}: block id {blk} outside the pool")
+            k_cache[blk, j % P] = k_new[cu_new[b] + t]
+            v_cache[blk, j % P] = v_new[cu_new[b] + t]
