@@ -199,6 +199,48 @@ int pa_varlen_check_alibi(const pa_tensor* q, const pa_tensor* k_cache, const pa
                           int32_t window_right, const pa_tensor* alibi_slopes, const pa_tensor* out,
                           const pa_tensor* softmax_lse);
 
+/*
+ * pa_kv_append -- writes new key/value tokens into the paged caches, the step that comes
+ * before pa_varlen_fwd in a serving loop.  The pages give no append operation; they say
+ * that a sequence's occupancy of its pages is tracked through the block table ("paged
+ * flash-attn requires page_block_size to be a multiple of 32", Solutions) and that the
+ * table maps a sequence's logical pages to physical blocks ("flash-attn-varlen paged
+ * expects k/v tensors of rank 4", What it means).  The placement taken is the one the
+ * bottom-right aligned mask implies: sequence b has sk_b = cu_seqlens_k[b+1] -
+ * cu_seqlens_k[b] keys after the append, and its n_b = cu_seqlens_new[b+1] -
+ * cu_seqlens_new[b] new tokens are the last n_b of them.  New token t (0-based) goes to
+ * logical key pos = sk_b - n_b + t, i.e. slot pos % P of block block_table[b, pos / P].
+ * For a chunked-prefill or decode step, cu_seqlens_new is the step's cu_seqlens_q and the
+ * attention call that follows uses the same cu_seqlens_k and block_table.
+ *
+ *  k_new, v_new    (total_new, num_heads_k, head_dim), the caches' dtype (f16 or bf16),
+ *                  last dim contiguous, other strides multiples of 8 elements
+ *  cu_seqlens_new  int32 [batch + 1], contiguous
+ *  cu_seqlens_k    int32 [batch + 1], contiguous: lengths after the append
+ *  block_table     int32 [batch, max_pages], last dim contiguous
+ *  k_cache,
+ *  v_cache         (num_blocks, page_block_size, num_heads_k, head_dim), same shape and
+ *                  strides; written in place (only the new tokens' slots)
+ *  stream          cudaStream_t the copy is ordered on; the call is asynchronous and
+ *                  every tensor is borrowed until it completes.
+ * Host checks, in the pages' order where they apply, with pa_varlen_fwd's codes and texts:
+ * ranks (k_new/v_new 3: PA_ERR_RANK; caches 4: PA_ERR_RANK_PAGED), last-dim contiguity
+ * (PA_ERR_NONCONTIG), shapes (PA_ERR_SHAPE), page size (PA_ERR_PAGE_UNSET / _MISMATCH /
+ * _MULT32), head_dim > 512 (PA_ERR_HEADDIM), index tensors, device residency
+ * (PA_ERR_NOT_DEVICE), dtypes and batch sizes (PA_ERR_ARG), alignment (PA_ERR_UNSUPPORTED).
+ * On the device, a sequence with n_b > sk_b, a position past its block-table row or a
+ * block id outside [0, num_blocks) is skipped and reported by pa_device_status() as
+ * PA_ERR_DEVICE_BOUNDS.  Tokens of other sequences are still written.
+ */
+int pa_kv_append(const pa_tensor* k_new, const pa_tensor* v_new, const pa_tensor* cu_seqlens_new,
+                 const pa_tensor* cu_seqlens_k, const pa_tensor* block_table, const pa_tensor* k_cache,
+                 const pa_tensor* v_cache, int32_t page_block_size, void* stream);
+
+/* The host-side checks of pa_kv_append alone: no device-residency check, no CUDA call. */
+int pa_kv_append_check(const pa_tensor* k_new, const pa_tensor* v_new, const pa_tensor* cu_seqlens_new,
+                       const pa_tensor* cu_seqlens_k, const pa_tensor* block_table, const pa_tensor* k_cache,
+                       const pa_tensor* v_cache, int32_t page_block_size);
+
 /* Message of the calling thread's last failed call ("" after a success).  The string
  * stays valid until that thread's next call into the library. */
 const char* pa_last_error(void);
@@ -236,13 +278,14 @@ uint64_t pa_kernel_launches(void);
  * milliseconds and to launches[c] the number of timed launches of kernel class c, and
  * clears the record.  Classes: PA_KC_PREFILL (the tensor-core prefill kernel),
  * PA_KC_SPLITKV (the split-KV pass: decode_kernel or splitkv_kernel), PA_KC_COMBINE (the
- * split-KV combine).  ms and launches are caller-owned host arrays of PA_KERNEL_CLASSES
+ * split-KV combine), PA_KC_APPEND (pa_kv_append's kernel).  ms and launches are caller-owned host arrays of PA_KERNEL_CLASSES
  * entries.  Returns PA_OK, PA_ERR_ARG for a null array, or PA_ERR_CUDA if an event
  * query failed (message in pa_last_error; the record is cleared either way). */
 #define PA_KC_PREFILL 0
 #define PA_KC_SPLITKV 1
 #define PA_KC_COMBINE 2
-#define PA_KERNEL_CLASSES 3
+#define PA_KC_APPEND 3
+#define PA_KERNEL_CLASSES 4
 void pa_kernel_timing(int enable);
 int pa_kernel_times(double* ms, uint64_t* launches);
 

@@ -80,6 +80,10 @@ def load():
         lib.pa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
         lib.pa_set_withhold_loads.restype = None
         lib.pa_set_withhold_loads.argtypes = [ctypes.c_int]
+        lib.pa_kv_append.restype = ctypes.c_int
+        lib.pa_kv_append.argtypes = [_TP] * 7 + [ctypes.c_int32, ctypes.c_void_p]
+        lib.pa_kv_append_check.restype = ctypes.c_int
+        lib.pa_kv_append_check.argtypes = [_TP] * 7 + [ctypes.c_int32]
         lib.pa_kernel_timing.restype = None
         lib.pa_kernel_timing.argtypes = [ctypes.c_int]
         lib.pa_kernel_times.restype = ctypes.c_int
@@ -116,7 +120,7 @@ def kernel_launches() -> int:
     return int(load().pa_kernel_launches())
 
 
-KERNEL_CLASSES = ("prefill", "splitkv", "combine")  # PA_KC_PREFILL, PA_KC_SPLITKV, PA_KC_COMBINE
+KERNEL_CLASSES = ("prefill", "splitkv", "combine", "append")  # PA_KC_PREFILL, _SPLITKV, _COMBINE, _APPEND
 
 
 def kernel_timing(enable: bool) -> None:
@@ -217,3 +221,22 @@ def varlen_fwd(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table=None
     if rc != 0:
         raise PaError(rc, lib.pa_last_error().decode())
     return out, softmax_lse
+
+
+def kv_append(k_new, v_new, cu_seqlens_new, cu_seqlens_k, block_table, k_cache, v_cache, page_block_size=None,
+              stream=None) -> None:
+    """pa_kv_append on torch CUDA tensors: writes the new tokens of every sequence (the last
+    n_b of its sk_b keys) into their pages of ``k_cache`` / ``v_cache``, in place."""
+    import torch
+    lib = load()
+    P = page_block_size if page_block_size is not None else k_cache.shape[1]
+    s = stream if stream is not None else torch.cuda.current_stream(k_new.device)
+    ds = [describe(t) for t in (k_new, v_new, cu_seqlens_new, cu_seqlens_k, block_table, k_cache, v_cache)]
+    rc = lib.pa_kv_append(*[_ref(d) for d in ds], int(P), ctypes.c_void_p(s.cuda_stream))
+    if rc != 0:
+        raise PaError(rc, lib.pa_last_error().decode())
+
+
+def kv_append_check(descriptors, page_block_size) -> int:
+    """Host-only checks of pa_kv_append on seven descriptors (PaTensor or None)."""
+    return load().pa_kv_append_check(*[_ref(d) for d in descriptors], int(page_block_size))

@@ -268,6 +268,110 @@ int validate(const pa_tensor* q, const pa_tensor* k, const pa_tensor* v, const p
     return PA_OK;
 }
 
+// ---- KV append: host checks ----------------------------------------------------------------
+int validate_append(const pa_tensor* kn, const pa_tensor* vn, const pa_tensor* cu_new, const pa_tensor* cu_k,
+                    const pa_tensor* bt, const pa_tensor* kc, const pa_tensor* vc, int32_t page_block_size,
+                    bool check_device, pa::AppendArgs* a) {
+    if (!kn || !vn || !cu_new || !cu_k || !bt || !kc || !vc)
+        return fail(PA_ERR_ARG, "a tensor descriptor is NULL");
+    // -- ranks: new tokens are packed like non-paged k/v, the caches are paged
+    if (kn->ndim != 3 || vn->ndim != 3)
+        return fail(PA_ERR_RANK, "kv append expects k_new/v_new tensors of rank 3 (k_new: %d, v_new: %d)", kn->ndim,
+                    vn->ndim);
+    if (kc->ndim != 4 || vc->ndim != 4)
+        return fail(PA_ERR_RANK_PAGED, "flash-attn-varlen paged expects k/v tensors of rank 4 (k: %d, v: %d)",
+                    kc->ndim, vc->ndim);
+    // -- last-dim contiguity
+    for (const pa_tensor* t : {kn, vn, kc, vc})
+        if (t->stride[t->ndim - 1] != 1)
+            return fail(PA_ERR_NONCONTIG, "the last dim of %s must be contiguous %s",
+                        t == kn ? "k_new" : t == vn ? "v_new" : t == kc ? "k" : "v", strides(t).c_str());
+    // -- shapes
+    if (!same_shape(kc, vc)) return fail(PA_ERR_SHAPE, "shape mismatch k %s and v %s", dims(kc).c_str(), dims(vc).c_str());
+    if (!same_shape(kn, vn))
+        return fail(PA_ERR_SHAPE, "shape mismatch k_new %s and v_new %s", dims(kn).c_str(), dims(vn).c_str());
+    if (kn->shape[1] != kc->shape[2] || kn->shape[2] != kc->shape[3])
+        return fail(PA_ERR_SHAPE, "shape mismatch k_new %s and k %s", dims(kn).c_str(), dims(kc).c_str());
+    const int64_t page = kc->shape[1], head_size = kc->shape[3];
+    // -- page size and head size, as for the paged forward call
+    if (page_block_size <= 0) return fail(PA_ERR_PAGE_UNSET, "paged flash-attn requires page_block_size");
+    if (page_block_size != page)
+        return fail(PA_ERR_PAGE_MISMATCH, "page_block_size %d does not match k shape %s", page_block_size,
+                    dims(kc).c_str());
+    if (page % 32 != 0)
+        return fail(PA_ERR_PAGE_MULT32, "paged flash-attn requires page_block_size to be a multiple of 32 (got %lld)",
+                    (long long)page);
+    if (head_size > 512)
+        return fail(PA_ERR_HEADDIM, "paged flash-attn supports head sizes up to 512 (got %lld)", (long long)head_size);
+    // -- index tensors
+    if (cu_new->ndim != 1 || cu_k->ndim != 1) return fail(PA_ERR_ARG, "cu_seqlens_new and cu_seqlens_k must be rank 1");
+    if (cu_new->stride[0] != 1) return fail(PA_ERR_NONCONTIG, "seqlens_new has to be contiguous");
+    if (cu_k->stride[0] != 1) return fail(PA_ERR_NONCONTIG, "seqlens_k has to be contiguous");
+    if (bt->ndim != 2) return fail(PA_ERR_ARG, "block_table must be rank 2, got rank %d", bt->ndim);
+    if (bt->stride[1] != 1) return fail(PA_ERR_NONCONTIG, "block_table last dimension must be contiguous");
+    if (check_device) {
+        auto on_device = [](const pa_tensor* t) { return numel(t) == 0 || is_device_memory(t->data); };
+        if (!on_device(bt)) return fail(PA_ERR_NOT_DEVICE, "block_table must be a cuda tensor");
+        if (!on_device(cu_new)) return fail(PA_ERR_NOT_DEVICE, "seqlens_new must be a cuda tensor");
+        if (!on_device(cu_k)) return fail(PA_ERR_NOT_DEVICE, "seqlens_k must be a cuda tensor");
+        if (!on_device(kn) || !on_device(vn)) return fail(PA_ERR_NOT_DEVICE, "k_new and v_new must be cuda tensors");
+        if (!on_device(kc) || !on_device(vc)) return fail(PA_ERR_NOT_DEVICE, "k and v must be cuda tensors");
+    }
+    // -- this library's own argument checks
+    if (kc->dtype != PA_F16 && kc->dtype != PA_BF16)
+        return fail(PA_ERR_UNSUPPORTED, "cache dtype %d: only f16 and bf16 are supported", kc->dtype);
+    if (vc->dtype != kc->dtype || kn->dtype != kc->dtype || vn->dtype != kc->dtype)
+        return fail(PA_ERR_ARG, "k_new, v_new and the caches must share one dtype");
+    if (cu_new->dtype != PA_I32 || cu_k->dtype != PA_I32 || bt->dtype != PA_I32)
+        return fail(PA_ERR_ARG, "cu_seqlens and block_table must be int32");
+    if (cu_new->shape[0] < 1 || cu_new->shape[0] != cu_k->shape[0])
+        return fail(PA_ERR_ARG, "cu_seqlens_new and cu_seqlens_k must both have batch + 1 >= 1 entries (%lld, %lld)",
+                    (long long)cu_new->shape[0], (long long)cu_k->shape[0]);
+    const int64_t batch = cu_new->shape[0] - 1;
+    if (bt->shape[0] != batch)
+        return fail(PA_ERR_ARG, "block_table has %lld rows for a batch of %lld", (long long)bt->shape[0],
+                    (long long)batch);
+    if (kc->stride[0] != vc->stride[0] || kc->stride[1] != vc->stride[1] || kc->stride[2] != vc->stride[2])
+        return fail(PA_ERR_UNSUPPORTED, "k and v caches must share strides (k %s, v %s)", strides(kc).c_str(),
+                    strides(vc).c_str());
+    if (head_size % 8 != 0)
+        return fail(PA_ERR_UNSUPPORTED, "head_dim %lld: the copy needs a multiple of 8", (long long)head_size);
+    if (batch > (1ll << 30) || kn->shape[0] >= (1ll << 31) || kc->shape[0] >= (1ll << 31))
+        return fail(PA_ERR_UNSUPPORTED, "sizes beyond 2^31 rows are not supported");
+    for (const pa_tensor* t : {kn, vn, kc, vc}) {
+        if (numel(t) == 0) continue;
+        if (!aligned16(t->data)) return fail(PA_ERR_UNSUPPORTED, "k_new/v_new/cache base addresses must be 16-byte aligned");
+        for (int d = 0; d < t->ndim - 1; ++d)
+            if (t->stride[d] % 8 != 0 || t->stride[d] <= 0)
+                return fail(PA_ERR_UNSUPPORTED, "strides %s: all but the last must be positive multiples of 8 elements",
+                            strides(t).c_str());
+    }
+    a->k_new = kn->data;
+    a->v_new = vn->data;
+    a->kn_s0 = kn->stride[0];
+    a->kn_s1 = kn->stride[1];
+    a->vn_s0 = vn->stride[0];
+    a->vn_s1 = vn->stride[1];
+    a->k_cache = kc->data;
+    a->v_cache = vc->data;
+    a->c_s0 = kc->stride[0];
+    a->c_s1 = kc->stride[1];
+    a->c_s2 = kc->stride[2];
+    a->cu_new = static_cast<const int32_t*>(cu_new->data);
+    a->cu_k = static_cast<const int32_t*>(cu_k->data);
+    a->bt = static_cast<const int32_t*>(bt->data);
+    a->bt_s0 = bt->stride[0];
+    a->bt_cols = (int)bt->shape[1];
+    a->batch = (int)batch;
+    a->total_new = kn->shape[0];
+    a->num_blocks = kc->shape[0];
+    a->P = (int)page;
+    a->Hkv = (int)kc->shape[2];
+    a->D = (int)head_size;
+    g_msg[0] = '\0';
+    return PA_OK;
+}
+
 // ---- per-(device, stream) split-KV workspace ------------------------------------------------
 std::mutex g_ws_mu;
 std::map<std::pair<int, cudaStream_t>, pa::Workspace> g_ws;
@@ -619,6 +723,30 @@ int pa_varlen_fwd_alibi(const pa_tensor* q, const pa_tensor* k_cache, const pa_t
                             max_seqlen_k, num_heads, num_heads_k, head_dim, page_block_size, softmax_scale,
                             window_left, window_right, alibi_slopes, out, softmax_lse, stream, library_workspace,
                             nullptr);
+}
+
+int pa_kv_append_check(const pa_tensor* k_new, const pa_tensor* v_new, const pa_tensor* cu_seqlens_new,
+                       const pa_tensor* cu_seqlens_k, const pa_tensor* block_table, const pa_tensor* k_cache,
+                       const pa_tensor* v_cache, int32_t page_block_size) {
+    pa::AppendArgs a{};
+    return validate_append(k_new, v_new, cu_seqlens_new, cu_seqlens_k, block_table, k_cache, v_cache,
+                           page_block_size, false, &a);
+}
+
+int pa_kv_append(const pa_tensor* k_new, const pa_tensor* v_new, const pa_tensor* cu_seqlens_new,
+                 const pa_tensor* cu_seqlens_k, const pa_tensor* block_table, const pa_tensor* k_cache,
+                 const pa_tensor* v_cache, int32_t page_block_size, void* stream) {
+    pa::AppendArgs a{};
+    int rc = validate_append(k_new, v_new, cu_seqlens_new, cu_seqlens_k, block_table, k_cache, v_cache,
+                             page_block_size, true, &a);
+    if (rc != PA_OK) return rc;
+    a.stream = static_cast<cudaStream_t>(stream);
+    unsigned int* err = nullptr;
+    int ce = pa::error_word(&err);
+    if (ce != cudaSuccess) return fail(PA_ERR_CUDA, "error word: %s", cudaGetErrorString((cudaError_t)ce));
+    rc = pa::launch_kv_append(a, err, g_msg, sizeof g_msg);
+    if (rc == PA_OK) g_msg[0] = '\0';
+    return rc;
 }
 
 const char* pa_last_error(void) { return g_msg; }

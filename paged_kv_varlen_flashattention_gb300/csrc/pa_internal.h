@@ -85,6 +85,27 @@ int error_word(unsigned int** ptr);
 // Counts successful kernel launches (pa_kernel_launches).
 void count_launches(int n);
 
+// KV append (pa_kv_append): validated arguments, element strides.
+struct AppendArgs {
+    const void* k_new;
+    const void* v_new;
+    int64_t kn_s0, kn_s1, vn_s0, vn_s1;  // (token, head) strides of k_new / v_new
+    void* k_cache;
+    void* v_cache;
+    int64_t c_s0, c_s1, c_s2;  // (block, slot, head) strides shared by both caches
+    const int32_t* cu_new;
+    const int32_t* cu_k;
+    const int32_t* bt;
+    int64_t bt_s0;
+    int bt_cols;
+    int batch;
+    int64_t total_new;
+    int64_t num_blocks;
+    int P, Hkv, D;
+    cudaStream_t stream;
+};
+int launch_kv_append(const AppendArgs& a, unsigned int* err, char* msg, size_t msg_len);
+
 // Per-kernel timing (pa_kernel_timing): timer_begin before a launch of kernel class `cls`
 // (PA_KC_*) into `stream`, timer_end after it launched successfully.  Both do nothing
 // unless timing is on.

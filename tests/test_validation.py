@@ -187,3 +187,54 @@ def test_alibi_slopes_checks():
     bad_q = list(ds)
     bad_q[0] = desc([8, 4, 64, 1], binding.PA_BF16)
     assert run_check_alibi(bad_q, desc([H + 1], binding.PA_F32), H, Hkv, D, P)[0] == CODES["PA_ERR_RANK"]
+
+
+def _append_descs(**over):
+    """Descriptors of a valid pa_kv_append call: 10 new tokens, 2 sequences, a (6, 32, 2, 64)
+    pool, bf16."""
+    shapes = {"k_new": [10, 2, 64], "v_new": [10, 2, 64], "cu_new": [3], "cu_k": [3], "bt": [2, 3],
+              "k": [6, 32, 2, 64], "v": [6, 32, 2, 64]}
+    dtypes = {"k_new": binding.PA_BF16, "v_new": binding.PA_BF16, "cu_new": binding.PA_I32,
+              "cu_k": binding.PA_I32, "bt": binding.PA_I32, "k": binding.PA_BF16, "v": binding.PA_BF16}
+    strides = {}
+    for key, val in over.items():
+        name, what = key.rsplit("_", 1) if key.endswith(("_shape", "_dtype", "_stride")) else (key, None)
+        {"shape": shapes, "dtype": dtypes, "stride": strides}[what][name] = val
+    order = ["k_new", "v_new", "cu_new", "cu_k", "bt", "k", "v"]
+    return [desc(shapes[n], dtypes[n], strides.get(n)) for n in order]
+
+
+def append_check(P=32, **over):
+    rc = binding.kv_append_check(_append_descs(**over), P)
+    return binding.STATUS[rc], binding.load().pa_last_error().decode()
+
+
+def test_kv_append_checks():
+    """pa_kv_append's host checks reuse the pages' conditions for the paged caches (rank 4,
+    last-dim contiguity, k/v shapes, page size, head size), in the pages' order."""
+    assert append_check() == ("PA_OK", "")
+    st, msg = append_check(k_new_shape=[10, 2, 64, 1])
+    assert st == "PA_ERR_RANK" and "rank 3" in msg
+    st, msg = append_check(k_shape=[6 * 32, 2, 64], v_shape=[6 * 32, 2, 64])
+    assert st == "PA_ERR_RANK_PAGED" and "paged expects k/v tensors of rank 4" in msg
+    st, msg = append_check(k_stride=[32 * 2 * 64, 2 * 64, 64, 2])
+    assert st == "PA_ERR_NONCONTIG" and "contiguous" in msg
+    st, msg = append_check(v_shape=[6, 32, 2, 72])
+    assert st == "PA_ERR_SHAPE" and "shape mismatch k" in msg
+    st, msg = append_check(k_new_shape=[10, 1, 64], v_new_shape=[10, 1, 64])
+    assert st == "PA_ERR_SHAPE" and "k_new" in msg
+    assert append_check(P=0)[0] == "PA_ERR_PAGE_UNSET"
+    st, msg = append_check(P=64)
+    assert st == "PA_ERR_PAGE_MISMATCH" and "does not match k shape" in msg
+    assert append_check(P=48, k_shape=[6, 48, 2, 64], v_shape=[6, 48, 2, 64])[0] == "PA_ERR_PAGE_MULT32"
+    big = [6, 32, 2, 520]
+    assert append_check(k_shape=big, v_shape=big, k_new_shape=[10, 2, 520], v_new_shape=[10, 2, 520])[0] \
+        == "PA_ERR_HEADDIM"
+    assert append_check(cu_k_shape=[4])[0] == "PA_ERR_ARG"
+    assert append_check(bt_shape=[3, 3])[0] == "PA_ERR_ARG"
+    assert append_check(bt_stride=[1, 2])[0] == "PA_ERR_NONCONTIG"
+    assert append_check(v_new_dtype=binding.PA_F16)[0] == "PA_ERR_ARG"
+    assert append_check(cu_new_dtype=binding.PA_F32)[0] == "PA_ERR_ARG"
+    assert append_check(k_new_stride=[2 * 64 + 4, 64, 1])[0] == "PA_ERR_UNSUPPORTED"
+    # a strided view of new tokens (e.g. K rows of a fused projection output) is fine
+    assert append_check(k_new_stride=[3 * 2 * 64, 64, 1])[0] == "PA_OK"
