@@ -472,6 +472,71 @@ def run_ours(args):
         print(json.dumps(result), flush=True)
 
 
+def run_append(args):
+    """--op append: pa_kv_append of each sequence's query tokens (the new tokens of a serving
+    step: whole prompts for prefill, one token per sequence for decode) into a pool laid out
+    like the workload's, timed on the device; GB/s of K and V read plus written."""
+    import torch
+    from paged_kv_varlen_flashattention_gb300 import binding, workloads
+    torch.cuda.set_device(0)
+    lay = workloads.CONFIGS[args.workload]()
+    lay.nan_fill = False
+    g = workloads.materialize(lay, device="cuda")
+    gen = torch.Generator(device="cuda").manual_seed(17)
+    shape = (lay.total_q, lay.num_heads_k, lay.head_dim)
+    kn = torch.randn(shape, generator=gen, device="cuda").to(g.k_cache.dtype)
+    vn = torch.randn(shape, generator=gen, device="cuda").to(g.k_cache.dtype)
+    elt = 2
+    nbytes = 2 * 2 * lay.total_q * lay.num_heads_k * lay.head_dim * elt
+
+    def step():
+        binding.kv_append(kn, vn, g.cu_seqlens_q, g.cu_seqlens_k, g.block_table, g.k_cache, g.v_cache)
+
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0, binding.last_error()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n0 = binding.kernel_launches()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    launches = binding.kernel_launches() - n0
+    ms = e0.elapsed_time(e1) / args.steps
+    binding.kernel_times()
+    binding.kernel_timing(True)
+    for _ in range(max(3, min(args.steps, 20))):
+        step()
+    torch.cuda.synchronize()
+    binding.kernel_timing(False)
+    k_ms, k_n = binding.kernel_times()["append"]
+    hbm, _, _, peak_kind = peaks()
+    value = nbytes / (ms * 1e-3) / 1e9
+    achieved = nbytes / (k_ms / k_n * 1e-3) / 1e9
+    cfg = workload_config(lay, 0, nbytes, 1)
+    cfg.update({"op": "kv_append", "new_tokens": lay.total_q,
+                "l2": "inputs larger than L2 (no flush)" if nbytes > 2 * L2_BYTES else "L2 not flushed; inputs fit"})
+    print(json.dumps({
+        "metric": "KV append GB/s (K and V read + written), % of GB300 HBM roofline", "value": round(value, 2),
+        "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if lay.dtype == "bf16" else "f16", "data": "synthetic", "config": cfg,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None, "kernel": "kv_append_kernel",
+                     "kernel_ms": round(k_ms / k_n, 5), "work_per_launch": nbytes,
+                     "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s",
+                     "timed": "CUDA events around each launch of the kernel, on its stream"},
+        "gpu_launches": int(launches), "clocks": clocks,
+    }), flush=True)
+
+
 def run_reference(args):
     """The oracle on the host cores, timed per step over a bounded sample of the workload."""
     rank = int(os.environ.get("RANK", "0"))
@@ -528,6 +593,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_bf16")
+    ap.add_argument("--op", choices=["attention", "append"], default="attention",
+                    help="attention: the forward call (default); append: pa_kv_append of the step's tokens")
     ap.add_argument("--alibi", action="store_true",
                     help="run every leg with the linear position bias (geometric per-head slopes)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -543,6 +610,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "append":
+        run_append(args)
     else:
         run_ours(args)
 

@@ -6,7 +6,7 @@
 // tensors of rank 4", What it means).
 //
 // HBM-bound byte copy: each warp takes a contiguous run of tokens, finds the first one's
-// sequence by binary search over cu_seqlens_new and walks on from there; the token's
+// sequence by a warp-wide search over cu_seqlens_new and walks on from there; the token's
 // Hkv * D elements are moved in 16-byte units, consecutive lanes on consecutive units of
 // the same (token, head) row, for K and then V.  Streaming loads and stores keep the copy
 // out of L1.
@@ -29,18 +29,19 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(const AppendA
     const int64_t per_warp = (a.total_new + n_warps - 1) / n_warps;
     const int64_t t0 = warp_id * per_warp, t1 = min64(a.total_new, t0 + per_warp);
     if (t0 >= t1) return;
-    // the sequence of token t0: the last b with cu_new[b] <= t0
-    int b = 0;
-    if (lane == 0) {
-        int lo = 0, hi = a.batch - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (a.cu_new[mid] <= t0) lo = mid;
-            else hi = mid - 1;
-        }
-        b = lo;
+    // the sequence of token t0, the last b < batch with cu_new[b] <= t0: a 32-way search,
+    // one probe per lane and round, so a batch of B sequences costs log32(B) dependent loads
+    int lo = 0, span = a.batch;  // the answer is in [lo, lo + span)
+    while (span > 1) {
+        const int step = (span + 31) / 32;
+        const int idx = lo + lane * step;
+        const bool le = idx < lo + span && a.cu_new[idx] <= t0;
+        const unsigned ok = __ballot_sync(0xffffffffu, le);
+        const int last = ok ? 31 - __clz((int)ok) : 0;  // cu_new[lo] <= t0 always holds
+        lo += last * step;
+        span = min(step, span - last * step);
     }
-    b = __shfl_sync(0xffffffffu, b, 0);
+    int b = lo;
     const int units = a.Hkv * (a.D / 8);  // 16-byte units per token
     const int upr = a.D / 8;              // units per (token, head) row
     int nb_end = a.cu_new[b + 1];
@@ -63,15 +64,30 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(const AppendA
         }
         const int64_t slot = pos - page * a.P;
         const int64_t dst_row = (int64_t)blk * a.c_s0 + slot * a.c_s1;
-        for (int u = lane; u < units; u += 32) {
-            const int h = u / upr, c = u - h * upr;
-            const int64_t src_k = t * a.kn_s0 + (int64_t)h * a.kn_s1 + c * 8;
-            const int64_t src_v = t * a.vn_s0 + (int64_t)h * a.vn_s1 + c * 8;
-            const int64_t dst = dst_row + (int64_t)h * a.c_s2 + c * 8;
-            const int4 kv = __ldcs(reinterpret_cast<const int4*>(static_cast<const uint16_t*>(a.k_new) + src_k));
-            const int4 vv = __ldcs(reinterpret_cast<const int4*>(static_cast<const uint16_t*>(a.v_new) + src_v));
-            __stcs(reinterpret_cast<int4*>(static_cast<uint16_t*>(a.k_cache) + dst), kv);
-            __stcs(reinterpret_cast<int4*>(static_cast<uint16_t*>(a.v_cache) + dst), vv);
+        // up to 4 units per lane in flight: every load of the batch before its stores
+        for (int base = 0; base < units; base += 4 * 32) {
+            int4 kr[4], vr[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int u = base + i * 32 + lane;
+                if (u < units) {
+                    const int h = u / upr, c = u - h * upr;
+                    kr[i] = __ldcs(reinterpret_cast<const int4*>(static_cast<const uint16_t*>(a.k_new) + t * a.kn_s0 +
+                                                                 (int64_t)h * a.kn_s1 + c * 8));
+                    vr[i] = __ldcs(reinterpret_cast<const int4*>(static_cast<const uint16_t*>(a.v_new) + t * a.vn_s0 +
+                                                                 (int64_t)h * a.vn_s1 + c * 8));
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int u = base + i * 32 + lane;
+                if (u < units) {
+                    const int h = u / upr, c = u - h * upr;
+                    const int64_t dst = dst_row + (int64_t)h * a.c_s2 + c * 8;
+                    __stcs(reinterpret_cast<int4*>(static_cast<uint16_t*>(a.k_cache) + dst), kr[i]);
+                    __stcs(reinterpret_cast<int4*>(static_cast<uint16_t*>(a.v_cache) + dst), vr[i]);
+                }
+            }
         }
     }
 }
@@ -87,8 +103,9 @@ int launch_kv_append(const AppendArgs& a, unsigned int* err, char* msg, size_t m
         snprintf(msg, msg_len, "kv append: %s", cudaGetErrorString(e));
         return PA_ERR_CUDA;
     }
-    // about four tokens per warp when there are few, else one wave of resident CTAs
-    const int64_t want = (a.total_new + 4 * (kAppendThreads / 32) - 1) / (4 * (kAppendThreads / 32));
+    // one token per warp while that fits in one wave of resident CTAs (each token's
+    // metadata is a chain of dependent loads), else the wave with several tokens per warp
+    const int64_t want = (a.total_new + kAppendThreads / 32 - 1) / (kAppendThreads / 32);
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * kAppendCtasPerSm));
     timer_begin(PA_KC_APPEND, a.stream);
     kv_append_kernel<<<grid, kAppendThreads, 0, a.stream>>>(a, err);

@@ -493,16 +493,33 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             // the rest runs with a unit scale.
             float sl = p.scale_log2;  // softmax_scale > 0 on this path
             if (ALIBI) {
+                if (p.wr == 0) {
+                    // causal: every attended key is at or left of the diagonal, where the
+                    // bias ab * (key - dg) is linear in the key (masked keys stay -inf)
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const float d0 = (float)(st.dg[q] - kt - 2 * tig);  // distance of key kt + 2 tig
+                    for (int q = 0; q < 2; ++q) {
+                        const float base = st.ab[q] * (float)(kt + 2 * tig - st.dg[q]);  // key kt + 2 tig
 #pragma unroll
-                    for (int k = 0; k < 16; ++k)
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            float& v = sv[4 * k + 2 * q + e];
-                            v = fmaf(-st.ab[q], fabsf(d0 - (float)(8 * k + e)), v * sl);
+                        for (int k = 0; k < 16; ++k) {
+                            float b0, b1;
+                            ffma2(b0, b1, st.ab[q], st.ab[q], (float)(8 * k), (float)(8 * k + 1), base, base);
+                            float& v0 = sv[4 * k + 2 * q];
+                            float& v1 = sv[4 * k + 2 * q + 1];
+                            ffma2(v0, v1, v0, v1, sl, sl, b0, b1);
                         }
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const float d0 = (float)(st.dg[q] - kt - 2 * tig);  // distance of key kt + 2 tig
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                float& v = sv[4 * k + 2 * q + e];
+                                v = fmaf(-st.ab[q], fabsf(d0 - (float)(8 * k + e)), v * sl);
+                            }
+                    }
                 }
                 sl = 1.f;
             }
