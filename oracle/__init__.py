@@ -196,3 +196,22 @@ def kv_append(k_new, v_new, cu_seqlens_new, cu_seqlens_k, block_table, k_cache, 
                 raise ValueError(f"sequence {b}: block id {blk} outside the pool")
             k_cache[blk, j % P] = k_new[cu_new[b] + t]
             v_cache[blk, j % P] = v_new[cu_new[b] + t]
+
+
+def attention_padded(dtype, q, k, v, softmax_scale, window_left=-1, window_right=0, alibi_slopes=None, lib=None):
+    """Attention over a padded batch: q (B, Sq, H, D), k and v (B, Sk, Hkv, D), every sequence
+    of length Sq / Sk.  By definition this is the varlen attention of the packed tokens with
+    uniform cumulative lengths (cu_q[b] = b Sq, cu_k[b] = b Sk) in the non-paged mode, so it
+    calls ``attention`` on that packing.  Returns (out float64 (B, Sq, H, D), lse float64
+    (B, H, Sq))."""
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    if qb.ndim != 4 or kb.ndim != 4 or kb.shape != vb.shape:
+        raise ValueError("q must be (B, Sq, H, D) and k, v (B, Sk, Hkv, D) of one shape")
+    B, Sq, H, D = qb.shape
+    Sk, Hkv = kb.shape[1], kb.shape[2]
+    cu_q = np.arange(B + 1, dtype=np.int32) * Sq
+    cu_k = np.arange(B + 1, dtype=np.int32) * Sk
+    out, lse = attention(dtype, qb.reshape(B * Sq, H, D), kb.reshape(B * Sk, Hkv, D), vb.reshape(B * Sk, Hkv, D),
+                         cu_q, cu_k, None, softmax_scale, window_left, window_right, lib=lib,
+                         alibi_slopes=alibi_slopes)
+    return out.reshape(B, Sq, H, D), lse.reshape(B, Sq, H).transpose(0, 2, 1).copy()

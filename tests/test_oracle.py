@@ -83,3 +83,27 @@ def test_alibi_two_key_closed_forms():
 
 def test_alibi_zero_slopes_is_no_bias():
     _pins.pin_alibi_zero_slopes(oracle.attention)
+
+
+def test_padded_equals_batched_sdpa():
+    """The padded-batch oracle equals torch's scaled_dot_product_attention on the batched
+    (B, H, S, D) float64 tensors (full and causal, grouped-query heads), and its lse (B, H,
+    Sq) equals torch.logsumexp of the scaled scores."""
+    import torch
+    import torch.nn.functional as F
+    rng = np.random.default_rng(121)
+    B, S, H, Hkv, D, scale = 3, 23, 4, 2, 16, 0.3
+    q = _pins.f16(rng, (B, S, H, D))
+    k = _pins.f16(rng, (B, S, Hkv, D))
+    v = _pins.f16(rng, (B, S, Hkv, D))
+    tq = torch.from_numpy(q.astype(np.float64)).permute(0, 2, 1, 3)
+    tk = torch.from_numpy(k.astype(np.float64)).permute(0, 2, 1, 3)
+    tv = torch.from_numpy(v.astype(np.float64)).permute(0, 2, 1, 3)
+    for causal in (False, True):
+        out, lse = oracle.attention_padded("f16", q, k, v, scale, -1, 0 if causal else -1)
+        ref = F.scaled_dot_product_attention(tq, tk, tv, is_causal=causal, scale=scale, enable_gqa=True)
+        assert np.allclose(out, ref.permute(0, 2, 1, 3).numpy(), rtol=1e-10, atol=1e-12), causal
+        sc = scale * (tq @ tk.repeat_interleave(H // Hkv, dim=1).transpose(-1, -2))
+        if causal:
+            sc = sc.masked_fill(torch.ones(S, S, dtype=torch.bool).triu(1), float("-inf"))
+        assert np.allclose(lse, torch.logsumexp(sc, dim=-1).numpy(), rtol=1e-12, atol=1e-12), causal
