@@ -241,6 +241,38 @@ int pa_kv_append_check(const pa_tensor* k_new, const pa_tensor* v_new, const pa_
                        const pa_tensor* cu_seqlens_k, const pa_tensor* block_table, const pa_tensor* k_cache,
                        const pa_tensor* v_cache, int32_t page_block_size);
 
+/*
+ * pa_fwd_padded -- attention over a padded batch (every sequence of the batch has seqlen_q
+ * queries and seqlen_k keys), the non-varlen API the pages point to for padded batches
+ * ("flash-attn-varlen expects input tensors of rank 3", Solutions: use FlashAttention
+ * (non-varlen) for padded batch attention).  Same arithmetic, mask (bottom-right
+ * aligned: causal = (-1, 0)), GQA mapping and optional linear position bias as
+ * pa_varlen_fwd_alibi; no paging.
+ *
+ *  q             (batch, seqlen_q, num_heads, head_dim), f16 or bf16, last dim contiguous
+ *  k, v          (batch, seqlen_k, num_heads_k, head_dim), same dtype, same shape
+ *  alibi_slopes  (num_heads,) f32 or NULL
+ *  out           (batch, seqlen_q, num_heads, head_dim), q's dtype, written
+ *  softmax_lse   (batch, num_heads, seqlen_q) f32, last dim contiguous, written
+ *  stream        cudaStream_t; asynchronous, tensors borrowed until it completes.
+ * The batch and sequence dimensions of q, k, v and out must be mergeable (batch stride =
+ * seqlen * sequence stride, as for contiguous tensors), else PA_ERR_UNSUPPORTED.  Status
+ * codes: PA_ERR_RANK for a rank other than 4, PA_ERR_NONCONTIG, PA_ERR_SHAPE (k vs v, q vs
+ * k, alibi_slopes), then the checks of pa_varlen_fwd on the packed view.  The library
+ * keeps a small per-(device, stream) device buffer for the uniform cumulative lengths
+ * (grown outside stream capture only, PA_ERR_WORKSPACE otherwise).
+ */
+int pa_fwd_padded(const pa_tensor* q, const pa_tensor* k, const pa_tensor* v, int32_t num_heads,
+                  int32_t num_heads_k, int32_t head_dim, float softmax_scale, int32_t window_left,
+                  int32_t window_right, const pa_tensor* alibi_slopes, const pa_tensor* out,
+                  const pa_tensor* softmax_lse, void* stream);
+
+/* The host-side checks of pa_fwd_padded alone: no device-residency check, no CUDA call. */
+int pa_check_padded(const pa_tensor* q, const pa_tensor* k, const pa_tensor* v, int32_t num_heads,
+                    int32_t num_heads_k, int32_t head_dim, float softmax_scale, int32_t window_left,
+                    int32_t window_right, const pa_tensor* alibi_slopes, const pa_tensor* out,
+                    const pa_tensor* softmax_lse);
+
 /* Message of the calling thread's last failed call ("" after a success).  The string
  * stays valid until that thread's next call into the library. */
 const char* pa_last_error(void);

@@ -84,6 +84,12 @@ def load():
         lib.pa_kv_append.argtypes = [_TP] * 7 + [ctypes.c_int32, ctypes.c_void_p]
         lib.pa_kv_append_check.restype = ctypes.c_int
         lib.pa_kv_append_check.argtypes = [_TP] * 7 + [ctypes.c_int32]
+        _PAD = [_TP, _TP, _TP, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_int32,
+                ctypes.c_int32, _TP, _TP, _TP]
+        lib.pa_fwd_padded.restype = ctypes.c_int
+        lib.pa_fwd_padded.argtypes = _PAD + [ctypes.c_void_p]
+        lib.pa_check_padded.restype = ctypes.c_int
+        lib.pa_check_padded.argtypes = list(_PAD)
         lib.pa_kernel_timing.restype = None
         lib.pa_kernel_timing.argtypes = [ctypes.c_int]
         lib.pa_kernel_times.restype = ctypes.c_int
@@ -240,3 +246,33 @@ def kv_append(k_new, v_new, cu_seqlens_new, cu_seqlens_k, block_table, k_cache, 
 def kv_append_check(descriptors, page_block_size) -> int:
     """Host-only checks of pa_kv_append on seven descriptors (PaTensor or None)."""
     return load().pa_kv_append_check(*[_ref(d) for d in descriptors], int(page_block_size))
+
+
+def fwd_padded(q, k, v, softmax_scale=None, window_left=-1, window_right=0, alibi_slopes=None, out=None,
+               softmax_lse=None, stream=None) -> Tuple[object, object]:
+    """pa_fwd_padded on torch CUDA tensors: q (B, Sq, H, D), k and v (B, Sk, Hkv, D); returns
+    (out (B, Sq, H, D), softmax_lse (B, H, Sq) fp32), allocated with torch when not given."""
+    import torch
+    lib = load()
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(q.shape[-1])
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    if softmax_lse is None:
+        softmax_lse = torch.empty((q.shape[0], q.shape[2], q.shape[1]), dtype=torch.float32, device=q.device)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    ds = [describe(t) for t in (q, k, v, alibi_slopes, out, softmax_lse)]
+    rc = lib.pa_fwd_padded(_ref(ds[0]), _ref(ds[1]), _ref(ds[2]), int(q.shape[2]), int(k.shape[2]), int(q.shape[3]),
+                           float(softmax_scale), int(window_left), int(window_right), _ref(ds[3]), _ref(ds[4]),
+                           _ref(ds[5]), ctypes.c_void_p(s.cuda_stream))
+    if rc != 0:
+        raise PaError(rc, lib.pa_last_error().decode())
+    return out, softmax_lse
+
+
+def check_padded(descriptors, num_heads, num_heads_k, head_dim, softmax_scale=0.125, window_left=-1,
+                 window_right=0) -> int:
+    """Host-only checks of pa_fwd_padded on (q, k, v, alibi_slopes, out, softmax_lse) descriptors."""
+    d = [_ref(x) for x in descriptors]
+    return load().pa_check_padded(d[0], d[1], d[2], int(num_heads), int(num_heads_k), int(head_dim),
+                                  float(softmax_scale), int(window_left), int(window_right), d[3], d[4], d[5])

@@ -10,6 +10,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -375,20 +376,23 @@ int validate_append(const pa_tensor* kn, const pa_tensor* vn, const pa_tensor* c
 // ---- per-(device, stream) split-KV workspace ------------------------------------------------
 std::mutex g_ws_mu;
 std::map<std::pair<int, cudaStream_t>, pa::Workspace> g_ws;
+// uniform cu_seqlens of the padded entry point, per (device, stream) like the workspace
+std::map<std::pair<int, cudaStream_t>, pa::Workspace> g_cu;
 
-int workspace_for(cudaStream_t stream, size_t bytes, void** ptr) {
+int grow_buffer(std::map<std::pair<int, cudaStream_t>, pa::Workspace>& buffers, cudaStream_t stream, size_t bytes,
+                void** ptr) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(PA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
     std::lock_guard<std::mutex> lock(g_ws_mu);
-    pa::Workspace& w = g_ws[{dev, stream}];
+    pa::Workspace& w = buffers[{dev, stream}];
     if (w.bytes < bytes) {
         cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
         e = cudaStreamIsCapturing(stream, &st);
         if (e != cudaSuccess) return fail(PA_ERR_CUDA, "cudaStreamIsCapturing: %s", cudaGetErrorString(e));
         if (st != cudaStreamCaptureStatusNone)
             return fail(PA_ERR_WORKSPACE,
-                        "split-KV workspace must grow to %zu bytes while the stream is capturing; run one call "
+                        "a library buffer must grow to %zu bytes while the stream is capturing; run one call "
                         "of the largest shape before capture",
                         bytes);
         if (w.ptr) {
@@ -408,6 +412,8 @@ int workspace_for(cudaStream_t stream, size_t bytes, void** ptr) {
     *ptr = w.ptr;
     return PA_OK;
 }
+
+int workspace_for(cudaStream_t stream, size_t bytes, void** ptr) { return grow_buffer(g_ws, stream, bytes, ptr); }
 
 // A second stream per device on which the tensor-core prefill kernel runs beside the
 // split-KV kernel (forked from and joined back to the caller's stream with events, so
@@ -634,6 +640,13 @@ int forward_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
                       num_heads, num_heads_k, head_dim, page_block_size, softmax_scale, window_left, window_right,
                       alibi_slopes, out, softmax_lse, true, &a);
     if (rc != PA_OK) return rc;
+    return launch_forward(a, stream, scratch, scratch_ctx);
+}
+
+// Everything after the host checks: split plan, scratch, and the launches (prefill on the
+// side stream beside the split-KV pass on the caller's stream).
+int launch_forward(pa::Args& a, void* stream, ScratchFn scratch, void* scratch_ctx) {
+    int rc = PA_OK;
     a.stream = static_cast<cudaStream_t>(stream);
     a.wait_ns = pa::g_wait_ns.load(std::memory_order_relaxed);
     a.withhold_loads = pa::g_withhold.load(std::memory_order_relaxed);
@@ -677,6 +690,75 @@ int forward_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
 }
 
 }  // namespace pa
+
+// ---- padded (non-varlen) entry point ---------------------------------------------------------
+namespace {
+
+// A rank-3 descriptor of a rank-4 (batch, seq, heads, dim) tensor whose batch and sequence
+// dimensions can be merged (batch stride = seq * seq stride).
+pa_tensor merged(const pa_tensor* t) {
+    pa_tensor m = *t;
+    m.ndim = 3;
+    m.shape[0] = t->shape[0] * t->shape[1];
+    m.shape[1] = t->shape[2];
+    m.shape[2] = t->shape[3];
+    m.stride[0] = t->stride[1];
+    m.stride[1] = t->stride[2];
+    m.stride[2] = t->stride[3];
+    m.shape[3] = m.stride[3] = 0;
+    return m;
+}
+
+bool mergeable(const pa_tensor* t) { return t->shape[0] <= 1 || t->shape[1] <= 1 || t->stride[0] == t->shape[1] * t->stride[1]; }
+
+int padded_common(const pa_tensor* q, const pa_tensor* k, const pa_tensor* v, int32_t num_heads, int32_t num_heads_k,
+                  int32_t head_dim, float softmax_scale, int32_t wl, int32_t wr, const pa_tensor* alibi,
+                  const pa_tensor* out, const pa_tensor* lse, bool check_device, void* cu_storage, pa::Args* a) {
+    if (!q || !k || !v || !out || !lse) return fail(PA_ERR_ARG, "a tensor descriptor is NULL (only alibi_slopes may be)");
+    if (q->ndim != 4 || k->ndim != 4 || v->ndim != 4)
+        return fail(PA_ERR_RANK, "flash-attn expects input tensors of rank 4 (q: %d, k: %d, v: %d)", q->ndim, k->ndim,
+                    v->ndim);
+    for (const pa_tensor* t : {q, k, v})
+        if (t->stride[3] != 1)
+            return fail(PA_ERR_NONCONTIG, "the last dim of %s must be contiguous %s", t == q ? "q" : t == k ? "k" : "v",
+                        strides(t).c_str());
+    if (!same_shape(k, v)) return fail(PA_ERR_SHAPE, "shape mismatch k %s and v %s", dims(k).c_str(), dims(v).c_str());
+    if (k->shape[0] != q->shape[0] || k->shape[3] != q->shape[3])
+        return fail(PA_ERR_SHAPE, "shape mismatch q %s and k %s", dims(q).c_str(), dims(k).c_str());
+    if (out->ndim != 4 || !same_shape(out, q))
+        return fail(PA_ERR_ARG, "out must have q's shape %s, got %s", dims(q).c_str(), dims(out).c_str());
+    const int64_t B = q->shape[0], Sq = q->shape[1], Sk = k->shape[1], H = q->shape[2];
+    if (lse->ndim != 3 || lse->shape[0] != B || lse->shape[1] != H || lse->shape[2] != Sq || lse->stride[2] != 1)
+        return fail(PA_ERR_ARG, "softmax_lse must be (batch, num_heads, seqlen_q) = (%lld, %lld, %lld) with a contiguous "
+                    "last dim", (long long)B, (long long)H, (long long)Sq);
+    for (const pa_tensor* t : {q, k, v, out})
+        if (!mergeable(t))
+            return fail(PA_ERR_UNSUPPORTED, "batch stride must equal seqlen * sequence stride %s", strides(t).c_str());
+    if (Sq > INT32_MAX / (B > 0 ? B : 1) || Sk > INT32_MAX / (B > 0 ? B : 1))
+        return fail(PA_ERR_UNSUPPORTED, "batch * seqlen beyond 2^31 is not supported");
+    const pa_tensor q3 = merged(q), k3 = merged(k), v3 = merged(v), o3 = merged(out);
+    pa_tensor l2 = *lse;  // (H, B Sq) view for the shared checks; the batch offset is set below
+    l2.ndim = 2;
+    l2.shape[0] = H;
+    l2.shape[1] = B * Sq;
+    l2.stride[0] = lse->stride[1];
+    l2.stride[1] = 1;
+    pa_tensor cq{}, ck{};
+    cq.data = cu_storage;
+    ck.data = cu_storage ? static_cast<int32_t*>(cu_storage) + (B + 1) : nullptr;
+    cq.dtype = ck.dtype = PA_I32;
+    cq.ndim = ck.ndim = 1;
+    cq.shape[0] = ck.shape[0] = B + 1;
+    cq.stride[0] = ck.stride[0] = 1;
+    int rc = validate(&q3, &k3, &v3, &cq, &ck, nullptr, (int32_t)Sq, (int32_t)Sk, num_heads, num_heads_k, head_dim, 0,
+                      softmax_scale, wl, wr, alibi, &o3, &l2, check_device, a);
+    if (rc != PA_OK) return rc;
+    // token t = b Sq + i of head h lands at b lse.stride[0] + h lse.stride[1] + i
+    a->lse_sb = lse->stride[0] - Sq;
+    return PA_OK;
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -723,6 +805,41 @@ int pa_varlen_fwd_alibi(const pa_tensor* q, const pa_tensor* k_cache, const pa_t
                             max_seqlen_k, num_heads, num_heads_k, head_dim, page_block_size, softmax_scale,
                             window_left, window_right, alibi_slopes, out, softmax_lse, stream, library_workspace,
                             nullptr);
+}
+
+// ---- padded (non-varlen) entry points ----
+int pa_check_padded(const pa_tensor* q, const pa_tensor* k, const pa_tensor* v, int32_t num_heads, int32_t num_heads_k,
+                    int32_t head_dim, float softmax_scale, int32_t window_left, int32_t window_right,
+                    const pa_tensor* alibi_slopes, const pa_tensor* out, const pa_tensor* softmax_lse) {
+    pa::Args a{};
+    static int32_t fake_cu[1];  // never dereferenced by the host checks
+    return padded_common(q, k, v, num_heads, num_heads_k, head_dim, softmax_scale, window_left, window_right,
+                         alibi_slopes, out, softmax_lse, false, fake_cu, &a);
+}
+
+int pa_fwd_padded(const pa_tensor* q, const pa_tensor* k, const pa_tensor* v, int32_t num_heads, int32_t num_heads_k,
+                  int32_t head_dim, float softmax_scale, int32_t window_left, int32_t window_right,
+                  const pa_tensor* alibi_slopes, const pa_tensor* out, const pa_tensor* softmax_lse, void* stream) {
+    if (!q || q->ndim != 4)
+        return pa_check_padded(q, k, v, num_heads, num_heads_k, head_dim, softmax_scale, window_left, window_right,
+                               alibi_slopes, out, softmax_lse);
+    const int64_t B = q->shape[0];
+    void* cu = nullptr;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the host checks first, so that a bad call allocates nothing
+    int rc = pa_check_padded(q, k, v, num_heads, num_heads_k, head_dim, softmax_scale, window_left, window_right,
+                             alibi_slopes, out, softmax_lse);
+    if (rc != PA_OK) return rc;
+    if ((rc = grow_buffer(g_cu, s, (size_t)(2 * (B + 1)) * sizeof(int32_t), &cu)) != PA_OK) return rc;
+    pa::Args a{};
+    rc = padded_common(q, k, v, num_heads, num_heads_k, head_dim, softmax_scale, window_left, window_right,
+                       alibi_slopes, out, softmax_lse, true, cu, &a);
+    if (rc != PA_OK) return rc;
+    if (a.total_q == 0 || a.batch == 0) return PA_OK;
+    rc = pa::launch_uniform_cu(static_cast<int32_t*>(cu), static_cast<int32_t*>(cu) + (B + 1), (int)B,
+                               (int)q->shape[1], (int)k->shape[1], s, g_msg, sizeof g_msg);
+    if (rc != PA_OK) return rc;
+    return pa::launch_forward(a, stream, library_workspace, nullptr);
 }
 
 int pa_kv_append_check(const pa_tensor* k_new, const pa_tensor* v_new, const pa_tensor* cu_seqlens_new,

@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(160) decode_kernel(const __grid_constant__ CUt
         if (d == 0) {
             const float lse = L > 0.f ? (mm + log2f(L)) * 0.69314718055994531f : -INFINITY;
             if (single)
-                p.lse[(int64_t)h * p.lse_s0 + t] = lse;
+                p.lse[(int64_t)h * p.lse_s0 + t + (int64_t)b * p.lse_sb] = lse;
             else
                 p.part_lse[(int64_t)split * p.part_stride + t * p.H + h] = lse;
         }

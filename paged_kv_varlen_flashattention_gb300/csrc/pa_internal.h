@@ -39,6 +39,7 @@ struct Args {
     int64_t o_s0, o_s1;
     float* lse;
     int64_t lse_s0;
+    int64_t lse_sb;  // per-sequence lse offset: 0 for (H, total_q); H Sq - Sq for (B, H, Sq)
     int64_t total_q;
     cudaStream_t stream;
     uint64_t wait_ns;    // bound on every in-kernel wait
@@ -117,6 +118,9 @@ void timer_end(int cls, cudaStream_t stream);
 using ScratchFn = int (*)(void* ctx, cudaStream_t stream, size_t bytes, void** ptr, char* msg, size_t msg_len);
 
 // Validation and dispatch shared by the C entry points (api.cpp).
+int launch_forward(Args& a, void* stream, ScratchFn scratch, void* scratch_ctx);
+int launch_uniform_cu(int32_t* cu_q, int32_t* cu_k, int batch, int sq, int sk, cudaStream_t stream, char* msg,
+                      size_t msg_len);
 int forward_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
                  const pa_tensor* cu_seqlens_q, const pa_tensor* cu_seqlens_k, const pa_tensor* block_table,
                  int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_heads, int32_t num_heads_k,

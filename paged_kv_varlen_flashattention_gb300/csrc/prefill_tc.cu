@@ -44,7 +44,7 @@ struct PrefillParams {
     void* out;
     int64_t o_s0, o_s1;
     float* lse;
-    int64_t lse_s0;
+    int64_t lse_s0, lse_sb;  // lse of (head h, token t, sequence b) at h lse_s0 + t + b lse_sb
     const int32_t* cu_q;
     const int32_t* cu_k;
     const int32_t* bt;
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 const int h = hk * p.G + g;
                 for (int d = 0; d < p.D; d += 8)
                     *reinterpret_cast<int4*>(out + t * p.o_s0 + (int64_t)h * p.o_s1 + d) = make_int4(0, 0, 0, 0);
-                p.lse[(int64_t)h * p.lse_s0 + t] = -INFINITY;
+                p.lse[(int64_t)h * p.lse_s0 + t + (int64_t)b * p.lse_sb] = -INFINITY;
             }
         }
         leave();
@@ -618,7 +618,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 const int h = hk * p.G + g;
                 orow[q] = out + t * p.o_s0 + (int64_t)h * p.o_s1;
                 if (valid[q] && tig == 0)
-                    p.lse[(int64_t)h * p.lse_s0 + t] =
+                    p.lse[(int64_t)h * p.lse_s0 + t + (int64_t)b * p.lse_sb] =
                         l > 0.f ? (st.m[q] + log2f(l)) * 0.69314718055994531f : -INFINITY;
             }
 #pragma unroll 1
@@ -739,6 +739,7 @@ int launch_prefill(const Args& a, unsigned int* err, char* msg, size_t msg_len) 
     pp.o_s1 = a.o_s1;
     pp.lse = a.lse;
     pp.lse_s0 = a.lse_s0;
+    pp.lse_sb = a.lse_sb;
     pp.cu_q = a.cu_q;
     pp.cu_k = a.cu_k;
     pp.bt = a.block_table;

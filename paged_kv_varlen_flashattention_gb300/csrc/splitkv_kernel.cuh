@@ -27,7 +27,7 @@ struct SplitParams {
     void* out;
     int64_t o_s0, o_s1;
     float* lse;
-    int64_t lse_s0;
+    int64_t lse_s0, lse_sb;  // lse of (head h, token t, sequence b) at h lse_s0 + t + b lse_sb
     const int32_t* cu_q;
     const int32_t* cu_k;
     const int32_t* bt;
@@ -450,7 +450,7 @@ __global__ void __launch_bounds__(128) splitkv_kernel(const __grid_constant__ CU
         const float l = l_sm[r];
         const float lse = l > 0.f ? (m_sm[r] + log2f(l)) * 0.69314718055994531f : -INFINITY;
         if (single)
-            p.lse[(int64_t)h * p.lse_s0 + t] = lse;
+            p.lse[(int64_t)h * p.lse_s0 + t + (int64_t)b * p.lse_sb] = lse;
         else
             p.part_lse[(int64_t)split * p.part_stride + t * p.H + h] = lse;
     }
@@ -512,7 +512,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const SplitParams p) {
         }
         *reinterpret_cast<uint32_t*>(out + t * p.o_s0 + (int64_t)h * p.o_s1 + d) = pack2<T>(a0 * inv, a1 * inv);
     }
-    if (lane == 0) p.lse[(int64_t)h * p.lse_s0 + t] = sum > 0.f ? m_use + logf(sum) : -INFINITY;
+    if (lane == 0) p.lse[(int64_t)h * p.lse_s0 + t + (int64_t)b * p.lse_sb] = sum > 0.f ? m_use + logf(sum) : -INFINITY;
 }
 
 }  // namespace pa

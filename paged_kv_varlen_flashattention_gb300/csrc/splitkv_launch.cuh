@@ -168,6 +168,7 @@ static int launch_splitkv_t(const Args& a, const SplitPlan& plan, void* workspac
     sp.o_s1 = a.o_s1;
     sp.lse = a.lse;
     sp.lse_s0 = a.lse_s0;
+    sp.lse_sb = a.lse_sb;
     sp.cu_q = a.cu_q;
     sp.cu_k = a.cu_k;
     sp.bt = a.block_table;

@@ -5,6 +5,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from paged_kv_varlen_flashattention_gb300 import binding, workloads
 from tests import _gpu
 
@@ -231,3 +232,73 @@ def test_alibi_slopes_on_host_are_rejected():
                            max_seqlen_q=lay.max_seqlen_q, max_seqlen_k=lay.max_seqlen_k,
                            alibi_slopes=torch.zeros(lay.num_heads, dtype=torch.float32))
     assert ei.value.name == "PA_ERR_NOT_DEVICE"
+
+
+# ---- padded (non-varlen) batches ------------------------------------------------------------
+
+def _padded_check(B, Sq, Sk, H=8, Hkv=2, D=128, dtype=torch.bfloat16, wl=-1, wr=0, alibi=None, seed=31):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    q = torch.randn((B, Sq, H, D), generator=g, device="cuda").to(dtype)
+    k = torch.randn((B, Sk, Hkv, D), generator=g, device="cuda").to(dtype)
+    v = torch.randn((B, Sk, Hkv, D), generator=g, device="cuda").to(dtype)
+    sl = None if alibi is None else torch.from_numpy(alibi).cuda()
+    out, lse = binding.fwd_padded(q, k, v, 1.0 / D ** 0.5, wl, wr, alibi_slopes=sl)
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0, binding.last_error()
+    name = "bf16" if dtype == torch.bfloat16 else "f16"
+    ref_o, ref_l = oracle.attention_padded(name, q.cpu(), k.cpu(), v.cpu(), 1.0 / D ** 0.5, wl, wr,
+                                           alibi_slopes=None if alibi is None else alibi.astype(np.float64))
+    lay = workloads.Layout.__new__(workloads.Layout)
+    lay.name, lay.num_heads, lay.head_dim, lay.dtype = "padded", H, D, name
+    _gpu.compare(lay, out.reshape(B * Sq, H, D), lse.permute(1, 0, 2).reshape(H, B * Sq),
+                 ref_o.reshape(B * Sq * H, D), ref_l.transpose(0, 2, 1).reshape(-1))
+
+
+@pytest.mark.parametrize("B,Sq,Sk", [(3, 100, 100), (4, 1, 300), (2, 5, 40), (2, 300, 700), (1, 1, 1)])
+def test_padded_causal(B, Sq, Sk):
+    _padded_check(B, Sq, Sk)
+
+
+def test_padded_full_window_fp16_alibi():
+    _padded_check(2, 150, 150, H=4, Hkv=4, D=64, dtype=torch.float16, wl=-1, wr=-1,
+                  alibi=_gpu.alibi_slopes(4))
+
+
+@pytest.mark.parametrize("D", [256, 512])
+def test_padded_large_head_dims(D):
+    _padded_check(2, 40, 90, H=4, Hkv=1, D=D)
+
+
+def test_padded_noncontiguous_lse_and_out():
+    """out and lse as views with strides of larger tensors (batch strides honoured)."""
+    B, S, H, Hkv, D = 2, 64, 4, 2, 64
+    q = torch.randn((B, S, H, D), device="cuda").bfloat16()
+    k = torch.randn((B, S, Hkv, D), device="cuda").bfloat16()
+    v = torch.randn((B, S, Hkv, D), device="cuda").bfloat16()
+    lse_big = torch.full((B, H + 2, S + 16), 7.0, device="cuda")
+    lse = lse_big[:, 1:H + 1, 8:S + 8]
+    out, _ = binding.fwd_padded(q, k, v, 0.125, -1, 0, softmax_lse=lse)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.attention_padded("bf16", q.cpu(), k.cpu(), v.cpu(), 0.125, -1, 0)
+    assert np.allclose(lse.cpu().numpy(), ref_l, atol=1e-3)
+    assert torch.all(lse_big[:, 0] == 7.0) and torch.all(lse_big[:, :, :8] == 7.0)
+    assert np.allclose(out.float().cpu().numpy(), ref_o, atol=1.6e-2, rtol=2e-2)
+
+
+def test_padded_full_size_sampled():
+    """8 x 2048 causal, H=32, Hkv=8, D=128 (the tensor-core path), sampled rows."""
+    B, S, H, Hkv, D = 8, 2048, 32, 8, 128
+    g = torch.Generator(device="cuda").manual_seed(41)
+    q = torch.randn((B, S, H, D), generator=g, device="cuda").bfloat16()
+    k = torch.randn((B, S, Hkv, D), generator=g, device="cuda").bfloat16()
+    v = torch.randn((B, S, Hkv, D), generator=g, device="cuda").bfloat16()
+    out, lse = binding.fwd_padded(q, k, v, 1.0 / D ** 0.5, -1, 0)
+    torch.cuda.synchronize()
+    rows = np.random.default_rng(0).choice(B * S * H, size=512, replace=False)
+    rows = np.unique(np.concatenate([rows, [0, B * S * H - 1]]))
+    cu = np.arange(B + 1, dtype=np.int32) * S
+    ref_o, ref_l = oracle.attention("bf16", q.cpu().reshape(B * S, H, D), k.cpu().reshape(B * S, Hkv, D),
+                                    v.cpu().reshape(B * S, Hkv, D), cu, cu, None, 1.0 / D ** 0.5, -1, 0, rows=rows)
+    lay = workloads.Layout.__new__(workloads.Layout)
+    lay.name, lay.num_heads, lay.head_dim, lay.dtype = "padded_full", H, D, "bf16"
+    _gpu.compare(lay, out.reshape(B * S, H, D), lse.permute(1, 0, 2).reshape(H, B * S), ref_o, ref_l, rows)

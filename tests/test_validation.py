@@ -238,3 +238,38 @@ def test_kv_append_checks():
     assert append_check(k_new_stride=[2 * 64 + 4, 64, 1])[0] == "PA_ERR_UNSUPPORTED"
     # a strided view of new tokens (e.g. K rows of a fused projection output) is fine
     assert append_check(k_new_stride=[3 * 2 * 64, 64, 1])[0] == "PA_OK"
+
+
+
+def _padded(q=(2, 7, 4, 64), k=(2, 9, 2, 64), v=None, out=None, lse=None, alibi=None, q_stride=None,
+            dtype=binding.PA_BF16):
+    v = v or k
+    out = out or q
+    lse = lse or (q[0], q[2], q[1])
+    return [desc(list(q), dtype, q_stride), desc(list(k), dtype), desc(list(v), dtype),
+            None if alibi is None else desc(list(alibi), binding.PA_F32), desc(list(out), dtype),
+            desc(list(lse), binding.PA_F32)]
+
+
+def padded_status(ds, H=4, Hkv=2, D=64):
+    rc = binding.check_padded(ds, H, Hkv, D)
+    return binding.STATUS[rc], binding.load().pa_last_error().decode()
+
+
+def test_padded_checks():
+    """pa_check_padded: rank 4 inputs ("use FlashAttention (non-varlen) for padded batch
+    attention", the Solutions of "flash-attn-varlen expects input tensors of rank 3"), then
+    the varlen call's checks on the packed view."""
+    assert padded_status(_padded()) == ("PA_OK", "")
+    assert padded_status(_padded(alibi=(4,)))[0] == "PA_OK"
+    st, msg = padded_status(_padded(q=(14, 4, 64), out=(14, 4, 64), lse=(2, 4, 7)))
+    assert st == "PA_ERR_RANK" and "rank 4" in msg
+    st, msg = padded_status(_padded(v=(2, 9, 2, 72)))
+    assert st == "PA_ERR_SHAPE" and "shape mismatch k" in msg
+    st, msg = padded_status(_padded(k=(3, 9, 2, 64)))
+    assert st == "PA_ERR_SHAPE" and "shape mismatch q" in msg
+    assert padded_status(_padded(alibi=(5,)))[0] == "PA_ERR_SHAPE"
+    assert padded_status(_padded(lse=(2, 7, 4)))[0] == "PA_ERR_ARG"
+    assert padded_status(_padded(q_stride=[7 * 4 * 64 + 8, 4 * 64, 64, 1]))[0] == "PA_ERR_UNSUPPORTED"
+    assert padded_status(_padded(), H=5)[0] == "PA_ERR_ARG"
+    assert padded_status(_padded(q_stride=[7 * 4 * 64, 4 * 64, 64, 2]))[0] == "PA_ERR_NONCONTIG"
