@@ -537,6 +537,71 @@ def run_append(args):
     }), flush=True)
 
 
+def run_padded(args):
+    """--op padded: pa_fwd_padded on a padded causal batch of 8 x 4096 tokens (H=32, Hkv=8,
+    D=128, bf16; the prefill shape at a uniform length), timed on the device; TFLOP/s."""
+    import torch
+    from paged_kv_varlen_flashattention_gb300 import binding
+    torch.cuda.set_device(0)
+    B, S, H, Hkv, D = 8, 4096, 32, 8, 128
+    g = torch.Generator(device="cuda").manual_seed(19)
+    q = torch.randn((B, S, H, D), generator=g, device="cuda").bfloat16()
+    k = torch.randn((B, S, Hkv, D), generator=g, device="cuda").bfloat16()
+    v = torch.randn((B, S, Hkv, D), generator=g, device="cuda").bfloat16()
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device="cuda")
+    sl = torch.from_numpy(alibi_slopes(H)).cuda() if args.alibi else None
+    flops = 4 * D * H * B * (S * (S + 1) // 2)
+    nbytes = 2 * B * S * Hkv * D * 2 + 2 * B * S * H * D * 2 + 4 * B * H * S
+
+    def step():
+        binding.fwd_padded(q, k, v, 1.0 / D ** 0.5, -1, 0, alibi_slopes=sl, out=out, softmax_lse=lse)
+
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0, binding.last_error()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n0 = binding.kernel_launches()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    launches = binding.kernel_launches() - n0
+    ms = e0.elapsed_time(e1) / args.steps
+    binding.kernel_times()
+    binding.kernel_timing(True)
+    for _ in range(max(3, min(args.steps, 10))):
+        step()
+    torch.cuda.synchronize()
+    binding.kernel_timing(False)
+    k_ms, k_n = binding.kernel_times()["prefill"]
+    _, bf16, _, peak_kind = peaks()
+    value = flops / (ms * 1e-3) / 1e12
+    achieved = flops / (k_ms / k_n * 1e-3) / 1e12
+    print(json.dumps({
+        "metric": "paged-attn TFLOP/s (prefill) and KV GB/s (decode), % of GB300 roofline", "value": round(value, 2),
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "padded_causal_bf16", "op": "fwd_padded", "batch": B, "seqlen": S, "num_heads": H,
+                   "num_heads_k": Hkv, "head_dim": D, "algorithmic_flops": flops, "algorithmic_bytes": nbytes,
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas1",
+                   **({"alibi_slopes": "2^(-8 (h + 1) / H)"} if args.alibi else {})},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16, "unit": "TFLOP/s",
+                     "frac": round(achieved / bf16, 4), "traffic": None, "kernel": "prefill_kernel",
+                     "kernel_ms": round(k_ms / k_n, 5), "work_per_launch": flops,
+                     "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops)" if peak_kind == "measured"
+                     else "fallback 1.9 PFLOP/s",
+                     "timed": "CUDA events around each launch of the kernel, on its stream"},
+        "gpu_launches": int(launches), "clocks": clocks,
+    }), flush=True)
+
+
 def run_reference(args):
     """The oracle on the host cores, timed per step over a bounded sample of the workload."""
     rank = int(os.environ.get("RANK", "0"))
@@ -593,8 +658,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_bf16")
-    ap.add_argument("--op", choices=["attention", "append"], default="attention",
-                    help="attention: the forward call (default); append: pa_kv_append of the step's tokens")
+    ap.add_argument("--op", choices=["attention", "append", "padded"], default="attention",
+                    help="attention: the forward call (default); append: pa_kv_append of the step's tokens; "
+                         "padded: pa_fwd_padded on an 8 x 4096 causal batch")
     ap.add_argument("--alibi", action="store_true",
                     help="run every leg with the linear position bias (geometric per-head slopes)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -612,6 +678,8 @@ def main():
         run_reference(args)
     elif args.op == "append":
         run_append(args)
+    elif args.op == "padded":
+        run_padded(args)
     else:
         run_ours(args)
 
