@@ -466,14 +466,18 @@ constexpr int kCombineMaxSplits = 1024;  // weights kept in shared memory per wa
 
 template <typename T, int M, int NT>
 __global__ void __launch_bounds__(128) combine_kernel(const SplitParams p) {
+    // grid.x = row blocks x 64-column chunks: one warp per (row, 64 output columns), so a
+    // handful of long rows with many splits still spreads over many warps
     __shared__ float wsm[kCombineRows][kCombineMaxSplits];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.z, hk = blockIdx.y % p.Hkv, rt = blockIdx.y / p.Hkv;
+    const int n_chunks = (p.D + 63) / 64;
+    const int chunk = blockIdx.x % n_chunks;
     TileView tv;
     if (!tile_view<M, NT>(p, b, rt, tv, false)) return;
     if (tv.nsplit <= 1) return;
     const int ns = min(tv.nsplit, kCombineMaxSplits);
-    const int r = blockIdx.x * kCombineRows + warp;
+    const int r = (blockIdx.x / n_chunks) * kCombineRows + warp;
     if (r >= tv.rows) return;
     T* out = static_cast<T*>(p.out);
     const int rho = tv.row0 + r;
@@ -501,18 +505,38 @@ __global__ void __launch_bounds__(128) combine_kernel(const SplitParams p) {
     for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
     __syncwarp();
     const float inv = sum > 0.f ? 1.f / sum : 0.f;
-    const float* po = p.part_o + row * p.D;
-    const int64_t split_stride = p.part_stride * p.D;
-    for (int d = lane * 2; d < p.D; d += 64) {
-        float a0 = 0.f, a1 = 0.f;
-        for (int s = 0; s < ns; ++s) {
-            const float2 o = *reinterpret_cast<const float2*>(po + s * split_stride + d);
-            a0 = fmaf(w[s], o.x, a0);
-            a1 = fmaf(w[s], o.y, a1);
+    const int d = chunk * 64 + lane * 2;
+    if (d < p.D) {
+        const float* po = p.part_o + row * p.D + d;
+        const int64_t split_stride = p.part_stride * p.D;
+        // eight splits per step with independent accumulators: eight loads in flight
+        float a0[8], a1[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) a0[u] = a1[u] = 0.f;
+        int s = 0;
+        for (; s + 8 <= ns; s += 8) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float2 o = *reinterpret_cast<const float2*>(po + (int64_t)(s + u) * split_stride);
+                a0[u] = fmaf(w[s + u], o.x, a0[u]);
+                a1[u] = fmaf(w[s + u], o.y, a1[u]);
+            }
         }
-        *reinterpret_cast<uint32_t*>(out + t * p.o_s0 + (int64_t)h * p.o_s1 + d) = pack2<T>(a0 * inv, a1 * inv);
+        for (; s < ns; ++s) {
+            const float2 o = *reinterpret_cast<const float2*>(po + (int64_t)s * split_stride);
+            a0[0] = fmaf(w[s], o.x, a0[0]);
+            a1[0] = fmaf(w[s], o.y, a1[0]);
+        }
+        float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            x0 += a0[u];
+            x1 += a1[u];
+        }
+        *reinterpret_cast<uint32_t*>(out + t * p.o_s0 + (int64_t)h * p.o_s1 + d) = pack2<T>(x0 * inv, x1 * inv);
     }
-    if (lane == 0) p.lse[(int64_t)h * p.lse_s0 + t + (int64_t)b * p.lse_sb] = sum > 0.f ? m_use + logf(sum) : -INFINITY;
+    if (chunk == 0 && lane == 0)
+        p.lse[(int64_t)h * p.lse_s0 + t + (int64_t)b * p.lse_sb] = sum > 0.f ? m_use + logf(sum) : -INFINITY;
 }
 
 }  // namespace pa

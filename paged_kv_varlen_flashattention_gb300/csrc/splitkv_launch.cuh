@@ -56,7 +56,8 @@ static int run_splitkv(const CUtensorMap& tk, const CUtensorMap& tv, const Split
     timer_end(PA_KC_SPLITKV, stream);
     count_launches(1);
     if (plan.max_splits > 1) {
-        dim3 g2((plan.tile_rows + kCombineRows - 1) / kCombineRows, sp.Hkv * plan.row_tiles, sp.batch);
+        dim3 g2(((plan.tile_rows + kCombineRows - 1) / kCombineRows) * ((sp.D + 63) / 64), sp.Hkv * plan.row_tiles,
+                sp.batch);
         timer_begin(PA_KC_COMBINE, stream);
         combine_kernel<T, C::M, NT><<<g2, 128, 0, stream>>>(sp);
         e = cudaGetLastError();
@@ -111,7 +112,7 @@ static int run_decode(const CUtensorMap& tk, const CUtensorMap& tv, const SplitP
     timer_end(PA_KC_SPLITKV, stream);
     count_launches(1);
     if (plan.max_splits > 1) {
-        dim3 g2((plan.tile_rows + kCombineRows - 1) / kCombineRows, sp.Hkv, sp.batch);
+        dim3 g2(((plan.tile_rows + kCombineRows - 1) / kCombineRows) * ((sp.D + 63) / 64), sp.Hkv, sp.batch);
         timer_begin(PA_KC_COMBINE, stream);
         combine_kernel<T, C::M, NT><<<g2, 128, 0, stream>>>(sp);
         e = cudaGetLastError();
