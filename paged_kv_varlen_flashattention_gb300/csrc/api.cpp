@@ -595,11 +595,15 @@ SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, int num_sms)
     if (const char* env = std::getenv("PA_SPLIT_TILES")) {
         split_tiles = std::max<int64_t>(1, std::atoll(env));
     } else if (pl.row_tiles == 1) {
-        // Aim at about four CTAs of work per SM.  A split is never shorter than 4 tiles, nor
-        // than 8 M keys: its fp32 partial result (M rows x D x 4 bytes, written and read back)
-        // then costs at most ~1/8 of the K/V bytes it reads (8 M keys x 2 D x 2 bytes).
-        const int64_t target = 4ll * num_sms;
-        int64_t splits = (target + units - 1) / units;
+        // Fewer (sequence, kv head) units than resident CTA slots: one wave, every unit's keys
+        // split evenly over slots / units CTAs (each further wave would add a pipeline ramp,
+        // a merge and a partial result per CTA).  Otherwise about four CTAs per SM, which
+        // balances sequences of different lengths (unknown on the host).  A split is never
+        // shorter than 4 tiles, nor than 8 M keys: its fp32 partial result (M rows x D x 4
+        // bytes, written and read back) then costs at most ~1/8 of the K/V bytes it reads.
+        const int64_t slots =
+            (int64_t)num_sms * (a.dtype == PA_BF16 ? splitkv_occupancy_bf16(pl) : splitkv_occupancy_f16(pl));
+        int64_t splits = units < slots ? slots / units : (4ll * num_sms + units - 1) / units;
         splits = std::max<int64_t>(1, std::min(splits, tiles_max));
         const int64_t min_tiles = std::max<int64_t>(4, (8ll * M + pl.nt - 1) / pl.nt);
         split_tiles = std::max<int64_t>(min_tiles, (tiles_max + splits - 1) / splits);

@@ -76,6 +76,9 @@ int launch_splitkv(const Args& a, const SplitPlan& plan, void* workspace, unsign
                    size_t msg_len);
 int launch_splitkv_bf16(const Args& a, const SplitPlan& plan, void* workspace, unsigned int* err, char* msg,
                         size_t msg_len);
+// Resident CTAs per SM of the split-KV kernel `plan` dispatches to (dp, mt, row_tiles set).
+int splitkv_occupancy_bf16(const SplitPlan& plan);
+int splitkv_occupancy_f16(const SplitPlan& plan);
 int launch_splitkv_f16(const Args& a, const SplitPlan& plan, void* workspace, unsigned int* err, char* msg,
                        size_t msg_len);
 

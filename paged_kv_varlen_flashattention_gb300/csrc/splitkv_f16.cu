@@ -6,4 +6,5 @@ int launch_splitkv_f16(const Args& a, const SplitPlan& plan, void* workspace, un
                        size_t msg_len) {
     return launch_splitkv_t<__half>(a, plan, workspace, err, msg, msg_len);
 }
+int splitkv_occupancy_f16(const SplitPlan& plan) { return splitkv_occupancy_t<__half>(plan); }
 }  // namespace pa

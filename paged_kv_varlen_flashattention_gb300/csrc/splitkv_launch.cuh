@@ -126,6 +126,53 @@ static int run_decode(const CUtensorMap& tk, const CUtensorMap& tv, const SplitP
     return PA_OK;
 }
 
+// Resident CTAs per SM of the kernel a plan dispatches to (occupancy API, once per
+// instantiation), for sizing the split count to whole waves.
+template <typename KernelT>
+static int resident_ctas(KernelT kern, int threads, int smem) {
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 1;
+    }
+    return n > 0 ? n : 1;
+}
+
+template <typename T, int DP, int MG>
+static int decode_occupancy() {
+    constexpr int NT = 64, STAGES = DecShape<DP>::STAGES;
+    static const int n = resident_ctas(decode_kernel<T, DP, MG, NT, STAGES>, 160, DecCfg<DP, MG, NT, STAGES>::SMEM);
+    return n;
+}
+
+template <typename T, int DP, int MT>
+static int generic_occupancy() {
+    constexpr int NT = SplitShape<DP>::NT, STAGES = SplitShape<DP>::STAGES;
+    static const int n = resident_ctas(splitkv_kernel<T, DP, MT, NT, STAGES>, 128, SplitCfg<DP, MT, NT, STAGES>::SMEM);
+    return n;
+}
+
+template <typename T>
+static int splitkv_occupancy_t(const SplitPlan& plan) {
+    static const bool force_generic = std::getenv("PA_FORCE_GENERIC") != nullptr;
+    if (plan.row_tiles == 1 && plan.dp <= 256 && !force_generic) {  // the same choice as launch_splitkv_t
+        if (plan.dp == 64) return plan.mt == 1 ? decode_occupancy<T, 64, 1>() : decode_occupancy<T, 64, 2>();
+        if (plan.dp == 128) return plan.mt == 1 ? decode_occupancy<T, 128, 1>() : decode_occupancy<T, 128, 2>();
+        return plan.mt == 1 ? decode_occupancy<T, 256, 1>() : decode_occupancy<T, 256, 2>();
+    }
+    switch (plan.dp * 4 + plan.mt) {
+        case 64 * 4 + 1: return generic_occupancy<T, 64, 1>();
+        case 64 * 4 + 2: return generic_occupancy<T, 64, 2>();
+        case 128 * 4 + 1: return generic_occupancy<T, 128, 1>();
+        case 128 * 4 + 2: return generic_occupancy<T, 128, 2>();
+        case 256 * 4 + 1: return generic_occupancy<T, 256, 1>();
+        case 256 * 4 + 2: return generic_occupancy<T, 256, 2>();
+        case 512 * 4 + 1: return generic_occupancy<T, 512, 1>();
+        default: return generic_occupancy<T, 512, 2>();
+    }
+}
+
 template <typename T>
 static int launch_splitkv_t(const Args& a, const SplitPlan& plan, void* workspace, unsigned int* err, char* msg,
                             size_t msg_len) {

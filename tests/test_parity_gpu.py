@@ -302,3 +302,50 @@ def test_padded_full_size_sampled():
     lay = workloads.Layout.__new__(workloads.Layout)
     lay.name, lay.num_heads, lay.head_dim, lay.dtype = "padded_full", H, D, "bf16"
     _gpu.compare(lay, out.reshape(B * S, H, D), lse.permute(1, 0, 2).reshape(H, B * S), ref_o, ref_l, rows)
+
+
+def test_cuda_graph_capture_and_replay():
+    """A serving step (KV append, then the forward call with a mixed batch) captured in a
+    CUDA graph after one warm-up call on the capture stream (which sizes the library's
+    per-stream workspace) replays to the
+    same result as the direct calls, and a new q written into the captured input buffer is
+    picked up by the replay."""
+    lay = workloads.small("mixed")
+    lay.nan_fill = False
+    g = workloads.materialize(lay, device="cuda")
+    out = torch.empty_like(g.q)
+    lse = torch.empty((lay.num_heads, lay.total_q), dtype=torch.float32, device="cuda")
+    kw = dict(max_seqlen_q=lay.max_seqlen_q, max_seqlen_k=lay.max_seqlen_k, softmax_scale=lay.softmax_scale,
+              window_left=lay.window_left, window_right=lay.window_right, out=out, softmax_lse=lse)
+    kn = torch.randn((lay.total_q, lay.num_heads_k, lay.head_dim), device="cuda").to(g.k_cache.dtype)
+    vn = torch.randn_like(kn)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        binding.kv_append(kn, vn, g.cu_seqlens_q, g.cu_seqlens_k, g.block_table, g.k_cache, g.v_cache, stream=s)
+        binding.varlen_fwd(g.q, g.k_cache, g.v_cache, g.cu_seqlens_q, g.cu_seqlens_k, g.block_table, stream=s, **kw)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = out.clone(), lse.clone()
+    graph = torch.cuda.CUDAGraph()
+    # the split-KV workspace is per (device, stream): capture on the stream that was warmed up
+    with torch.cuda.graph(graph, stream=s):
+        stream = torch.cuda.current_stream()
+        binding.kv_append(kn, vn, g.cu_seqlens_q, g.cu_seqlens_k, g.block_table, g.k_cache, g.v_cache,
+                          stream=stream)
+        binding.varlen_fwd(g.q, g.k_cache, g.v_cache, g.cu_seqlens_q, g.cu_seqlens_k, g.block_table,
+                           stream=stream, **kw)
+    out.zero_()
+    lse.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0, binding.last_error()
+    assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
+    # new queries through the same captured buffers
+    g.q.copy_(torch.randn_like(g.q.float()).to(g.q.dtype))
+    graph.replay()
+    torch.cuda.synchronize()
+    inp_cpu = workloads.Inputs(lay, g.q.cpu(), g.k_cache.cpu(), g.v_cache.cpu(), g.cu_seqlens_q.cpu(),
+                               g.cu_seqlens_k.cpu(), g.block_table.cpu())
+    ref_o, ref_l = _gpu.oracle_for(inp_cpu)
+    _gpu.compare(lay, out, lse, ref_o, ref_l)
