@@ -615,10 +615,18 @@ SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, int num_sms)
         pl.split_tiles = (int)((tiles_max + 1023) / 1024);
         pl.max_splits = (int)((tiles_max + pl.split_tiles - 1) / pl.split_tiles);
     }
-    pl.ws_bytes = 0;
+    // the decode kernel launches sequences longest first (a one-CTA ranking pass) for
+    // batches it can rank; the order sits at the start of the scratch
+    static const bool force_generic = std::getenv("PA_FORCE_GENERIC") != nullptr;
+    const bool decode_kernel = pl.row_tiles == 1 && pl.dp <= 256 && !force_generic;
+    pl.rank_in_cta = decode_kernel && a.batch >= 2 && a.batch <= kRankInCta;
+    pl.order_bytes = decode_kernel && a.batch > kRankInCta && a.batch <= kMaxOrderBatch
+                         ? ((size_t)a.batch * sizeof(int) + 255) / 256 * 256
+                         : 0;
+    pl.ws_bytes = pl.order_bytes;
     if (pl.max_splits > 1) {
         const size_t rows = (size_t)a.total_q * a.H;
-        pl.ws_bytes = (size_t)pl.max_splits * rows * ((size_t)a.D + 1) * sizeof(float) + 256;
+        pl.ws_bytes += (size_t)pl.max_splits * rows * ((size_t)a.D + 1) * sizeof(float) + 256;
     }
     return pl;
 }

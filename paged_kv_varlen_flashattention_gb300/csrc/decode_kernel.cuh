@@ -15,6 +15,8 @@
 
 namespace pa {
 
+constexpr int kDecodeThreads = 160;  // 4 consumer warps + 1 producer warp
+
 template <int DP, int MG, int NT, int STAGES>
 struct DecCfg {
     static constexpr int M = 16 * MG;        // rows per CTA
@@ -55,7 +57,7 @@ __device__ __forceinline__ bool dec_wait(uint64_t* bar, uint32_t parity, volatil
 }
 
 template <typename T, int DP, int MG, int NT, int STAGES>
-__global__ void __launch_bounds__(160) decode_kernel(const __grid_constant__ CUtensorMap tm_k,
+__global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                      const __grid_constant__ CUtensorMap tm_v,
                                                      const SplitParams p) {
     using C = DecCfg<DP, MG, NT, STAGES>;
@@ -63,7 +65,31 @@ __global__ void __launch_bounds__(160) decode_kernel(const __grid_constant__ CUt
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int b = blockIdx.z, hk = blockIdx.y % p.Hkv, split = blockIdx.x;
+    // Sequences longest first (ties by index): their CTAs start first and the short ones
+    // fill the tail of the grid.  Small batches are ranked here, one sequence per thread;
+    // larger ones come with an order from a ranking pass.
+    __shared__ int rank_len[kDecodeThreads];
+    __shared__ int rank_pick;
+    int b = (int)blockIdx.z;
+    if (p.order) {
+        b = p.order[blockIdx.z];
+    } else if (p.rank_in_cta) {
+        if (tid < p.batch) rank_len[tid] = p.cu_k[tid + 1] - p.cu_k[tid];
+        if (tid == 0) rank_pick = (int)blockIdx.z;
+        __syncthreads();
+        if (tid < p.batch) {
+            const int ls = rank_len[tid];
+            int rank = 0;
+            for (int t = 0; t < p.batch; ++t) {
+                const int lt = rank_len[t];
+                rank += (lt > ls) || (lt == ls && t < tid);
+            }
+            if (rank == (int)blockIdx.z) rank_pick = tid;
+        }
+        __syncthreads();
+        b = rank_pick;
+    }
+    const int hk = blockIdx.y % p.Hkv, split = blockIdx.x;
 
     TileView tv;
     if (!tile_view<M, NT>(p, b, 0, tv, split == 0)) return;

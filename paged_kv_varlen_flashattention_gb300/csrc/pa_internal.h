@@ -63,8 +63,17 @@ struct SplitPlan {
     int tile_rows;    // most rows a row tile can hold: min(16 * mt, max_seqlen_q * G)
     int split_tiles;  // key tiles per split
     int max_splits;   // grid.x
-    size_t ws_bytes;  // partial-result scratch needed (0 when max_splits == 1)
+    size_t ws_bytes;     // scratch needed: the longest-first order, then the partial results
+    size_t order_bytes;  // bytes of the order at the start of the scratch (0: none)
+    int rank_in_cta;     // decode kernel CTAs rank the batch themselves (small batches)
 };
+
+// The decode kernel launches sequences longest first: batches of at most kRankInCta
+// sequences are ranked inside every CTA, larger ones up to kMaxOrderBatch by a one-CTA pass.
+constexpr int kRankInCta = 160;
+constexpr int kMaxOrderBatch = 1024;
+int launch_longest_first(const int32_t* cu_k, int batch, int* order, cudaStream_t stream, char* msg,
+                         size_t msg_len);
 
 // Dense-prefill (tcgen05) launch availability for these arguments.
 bool prefill_supported(const Args& a);

@@ -42,6 +42,8 @@ struct SplitParams {
     float scale_log2;
     int wl, wr;
     const float* alibi;  // per-query-head slopes of the linear position bias, or nullptr
+    const int* order;    // decode kernel: sequence of grid z index (longest first), or nullptr
+    int rank_in_cta;     // decode kernel: each CTA ranks the (<= kDecodeThreads) sequences itself
     int rows_cap, row_tiles, split_tiles, max_splits;
     float* part_o;
     float* part_lse;

@@ -101,9 +101,13 @@ static int run_decode(const CUtensorMap& tk, const CUtensorMap& tv, const SplitP
         }
         configured = true;
     }
+    if (sp.order) {
+        const int rc = launch_longest_first(sp.cu_k, sp.batch, const_cast<int*>(sp.order), stream, msg, msg_len);
+        if (rc != PA_OK) return rc;
+    }
     dim3 grid(plan.max_splits, sp.Hkv, sp.batch);
     timer_begin(PA_KC_SPLITKV, stream);
-    kern<<<grid, 160, C::SMEM, stream>>>(tk, tv, sp);
+    kern<<<grid, kDecodeThreads, C::SMEM, stream>>>(tk, tv, sp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "decode launch: %s", cudaGetErrorString(e));
@@ -139,10 +143,13 @@ static int resident_ctas(KernelT kern, int threads, int smem) {
     return n > 0 ? n : 1;
 }
 
+static_assert(kRankInCta <= kDecodeThreads, "in-CTA ranking: one sequence per thread");
+
 template <typename T, int DP, int MG>
 static int decode_occupancy() {
     constexpr int NT = 64, STAGES = DecShape<DP>::STAGES;
-    static const int n = resident_ctas(decode_kernel<T, DP, MG, NT, STAGES>, 160, DecCfg<DP, MG, NT, STAGES>::SMEM);
+    static const int n =
+        resident_ctas(decode_kernel<T, DP, MG, NT, STAGES>, kDecodeThreads, DecCfg<DP, MG, NT, STAGES>::SMEM);
     return n;
 }
 
@@ -244,8 +251,10 @@ static int launch_splitkv_t(const Args& a, const SplitPlan& plan, void* workspac
     sp.split_tiles = plan.split_tiles;
     sp.max_splits = plan.max_splits;
     sp.part_stride = a.total_q * a.H;
+    if (plan.order_bytes) sp.order = static_cast<const int*>(workspace);
+    sp.rank_in_cta = plan.rank_in_cta;
     if (plan.max_splits > 1) {
-        sp.part_o = static_cast<float*>(workspace);
+        sp.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.order_bytes);
         sp.part_lse = sp.part_o + (size_t)plan.max_splits * sp.part_stride * a.D;
     }
     sp.err = err;
