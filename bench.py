@@ -89,6 +89,23 @@ def headline_unit(flops, nbytes):
     return "GB/s", nbytes / 1e9
 
 
+def max_over_ranks(value, dist, device):
+    """The largest of every rank's value (the slowest rank's time); `dist` None on one GPU."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(work_per_rank, world, ms_max):
+    """Whole-job throughput of N replicas: every rank runs the same step on its own GPU (the
+    path has no exchange between (sequence, kv head) units), so the job does `world` times
+    the per-rank work in the slowest rank's time."""
+    return world * work_per_rank / (ms_max * 1e-3)
+
+
 def kernel_class_seqs(lay):
     """Sequences per kernel class, mirroring the library's dispatch: sequences with more
     than 32 rows (sq * G) go to the tensor-core prefill kernel when it takes the call
@@ -381,16 +398,13 @@ def run_ours(args):
         torch.cuda.synchronize()
     ms, launches = time_device(binding, g, lay, args.steps, args.warmup, dist)
     clocks = sampler.stop()
-    ms_t = torch.tensor([ms], device="cuda")
-    if dist:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms = float(ms_t.item())
+    ms = max_over_ranks(ms, dist, "cuda")
     tensor_bound = flops / nbytes > (bf16 * 1e12) / (hbm * 1e9)
     if tensor_bound:
         unit, peak, scale_w = "TFLOP/s", bf16, flops / 1e12
     else:
         unit, peak, scale_w = "GB/s", hbm, nbytes / 1e9
-    value = world * scale_w / (ms * 1e-3)
+    value = replica_throughput(scale_w, world, ms)
 
     # roofline of the dominant kernel: its algorithmic work per launch over its own average
     # launch duration (CUDA events around each launch, on the stream it runs on)
