@@ -34,7 +34,7 @@ def _rank(rank, world, port, results):
 
 def test_two_gloo_ranks_take_the_slowest_time():
     world = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         results = m.dict()
         mp.spawn(_rank, args=(world, _free_port(), results), nprocs=world, join=True)
         got = dict(results)
