@@ -112,8 +112,11 @@ enum {
  * Checks run in the pages' order: ranks, last-dim contiguity, k/v shapes, page size set,
  * page size == k shape, page size % 32, head size <= 512; then device residency, then the
  * library's own argument checks.  Returns PA_OK or a status (message: pa_last_error()).
- * Memory: the library keeps one grow-only split-KV workspace per device; it is allocated
- * on first need with cudaMalloc and never while `stream` is capturing (PA_ERR_WORKSPACE).
+ * Memory: the library keeps one grow-only scratch per (device, stream) for the split-KV
+ * partial results and the decode kernel's launch order (longest sequence first); it is
+ * allocated on first need with cudaMalloc and never while `stream` is capturing
+ * (PA_ERR_WORKSPACE): before capturing a call into a CUDA graph, make one call of the
+ * largest shape on the capture stream.
  * Thread safety: calls from several host threads are safe.
  */
 int pa_varlen_fwd(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
@@ -134,7 +137,8 @@ int pa_varlen_fwd(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor*
  * let a plug-in use the buffers they pass in.  Same arguments, checks and results as
  * pa_varlen_fwd; the caller still provides every input and output.
  *
- * Scratch: split-KV partial results go to one fixed 32 MiB array compiled into the library
+ * Scratch: split-KV partial results (and the decode launch order of batches of more than
+ * 160 sequences) go to one fixed 32 MiB array compiled into the library
  * (a static device array: every GPU that loads the library holds it until the process
  * exits) instead of the library's growable workspace.  A call whose split plan needs more
  * than 32 MiB is rejected with PA_ERR_WORKSPACE and a message giving both sizes.  The
