@@ -474,6 +474,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const SplitParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.z, hk = blockIdx.y % p.Hkv, rt = blockIdx.y / p.Hkv;
     const int n_chunks = (p.D + 63) / 64;
+    // launched as a programmatic dependent of the split kernel (its launch overlaps that
+    // kernel's tail): the partial results are read only after it has completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int chunk = blockIdx.x % n_chunks;
     TileView tv;
     if (!tile_view<M, NT>(p, b, rt, tv, false)) return;

@@ -30,6 +30,25 @@ struct SplitShape<512> {
     static constexpr int NT = 32, STAGES = 2;  // 3 stages would exceed 227 KB with a 32-row Q tile
 };
 
+// The combine as a programmatic dependent launch of the split kernel before it on the
+// stream: its launch and prologue overlap that kernel's tail (it waits in griddepcontrol
+// before touching the partial results).
+template <typename T, int M, int NT>
+static cudaError_t launch_combine(dim3 grid, const SplitParams& sp, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, combine_kernel<T, M, NT>, sp);
+    return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
 template <typename T, int DP, int MT>
 static int run_splitkv(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& sp, const SplitPlan& plan,
                        cudaStream_t stream, char* msg, size_t msg_len) {
@@ -59,8 +78,7 @@ static int run_splitkv(const CUtensorMap& tk, const CUtensorMap& tv, const Split
         dim3 g2(((plan.tile_rows + kCombineRows - 1) / kCombineRows) * ((sp.D + 63) / 64), sp.Hkv * plan.row_tiles,
                 sp.batch);
         timer_begin(PA_KC_COMBINE, stream);
-        combine_kernel<T, C::M, NT><<<g2, 128, 0, stream>>>(sp);
-        e = cudaGetLastError();
+        e = launch_combine<T, C::M, NT>(g2, sp, stream);
         if (e != cudaSuccess) {
             snprintf(msg, msg_len, "split-KV combine launch: %s", cudaGetErrorString(e));
             return PA_ERR_CUDA;
@@ -118,8 +136,7 @@ static int run_decode(const CUtensorMap& tk, const CUtensorMap& tv, const SplitP
     if (plan.max_splits > 1) {
         dim3 g2(((plan.tile_rows + kCombineRows - 1) / kCombineRows) * ((sp.D + 63) / 64), sp.Hkv, sp.batch);
         timer_begin(PA_KC_COMBINE, stream);
-        combine_kernel<T, C::M, NT><<<g2, 128, 0, stream>>>(sp);
-        e = cudaGetLastError();
+        e = launch_combine<T, C::M, NT>(g2, sp, stream);
         if (e != cudaSuccess) {
             snprintf(msg, msg_len, "decode combine launch: %s", cudaGetErrorString(e));
             return PA_ERR_CUDA;
