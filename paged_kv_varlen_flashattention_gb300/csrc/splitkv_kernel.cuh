@@ -106,8 +106,14 @@ __device__ __forceinline__ bool tile_view(const SplitParams& p, int b, int rt, T
     return true;
 }
 
-template <int DP, int MT, int NT, int STAGES>
+// NW warps: 4, or 8 for the widest heads, where two warps share each key slice of
+// Q.K^T (one half of the head dim each, partial scores summed by the softmax) and each
+// warp owns DP / 8 output columns of P.V -- two warps per scheduler hide the latency of
+// the long MMA chains.
+template <int DP, int MT, int NT, int STAGES, int NW = 4>
 struct SplitCfg {
+    static constexpr int NTHR = NW * 32;
+    static constexpr int KSPLIT = NW / 4;           // head-dim parts of Q.K^T
     static constexpr int M = 16 * MT;               // query rows per CTA
     static constexpr int CH = DP / 64;              // 64-element (128-byte) column chunks of a row
     static constexpr int TILE_BYTES = CH * NT * 128;  // one K (or V) tile of NT keys
@@ -115,7 +121,7 @@ struct SplitCfg {
     static constexpr int Q_BYTES = CH * M * 128;
     static constexpr int P_BYTES = M * 128;         // P rows padded to 128 bytes
     static constexpr int S_STRIDE = NT + 4;         // fp32 score row stride
-    static constexpr int S_BYTES = M * S_STRIDE * 4;
+    static constexpr int S_BYTES = KSPLIT * M * S_STRIDE * 4;  // one partial score buffer per part
     static constexpr int OFF_Q = STAGES * STAGE_BYTES;
     static constexpr int OFF_P = OFF_Q + Q_BYTES;
     static constexpr int OFF_S = OFF_P + P_BYTES;
@@ -124,19 +130,20 @@ struct SplitCfg {
     static constexpr int OFF_BAR = (OFF_ROW + 7 * M * 4 + 15) & ~15;
     static constexpr int SMEM = OFF_BAR + STAGES * 8 + 1024;  // + slack for 1024-byte alignment
     static constexpr int KW = NT / 4;               // keys per warp in Q.K^T
-    static constexpr int DW = DP / 4;               // output columns per warp in P.V
+    static constexpr int DW = DP / NW;              // output columns per warp in P.V
+    static_assert(NW == 4 || NW == 8, "warps");
     static_assert(NT == 64 || NT == 32, "tile width");
     static_assert(DW % 16 == 0, "P.V column slice");
     static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
 
-template <typename T, int DP, int MT, int NT, int STAGES>
-__global__ void __launch_bounds__(128) splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
+template <typename T, int DP, int MT, int NT, int STAGES, int NW>
+__global__ void __launch_bounds__(NW * 32) splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                       const __grid_constant__ CUtensorMap tm_v,
                                                       const SplitParams p) {
-    using C = SplitCfg<DP, MT, NT, STAGES>;
+    using C = SplitCfg<DP, MT, NT, STAGES, NW>;
     constexpr int M = C::M;
-    constexpr int RPW = M / 4;  // softmax rows owned by each warp
+    constexpr int RPW = M / NW;  // softmax rows owned by each warp
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -187,7 +194,7 @@ __global__ void __launch_bounds__(128) splitkv_kernel(const __grid_constant__ CU
         const T* q = static_cast<const T*>(p.q);
         constexpr int UNITS = DP / 8;
         uint8_t* qs = smem + C::OFF_Q;
-        for (int idx = tid; idx < M * UNITS; idx += 128) {
+        for (int idx = tid; idx < M * UNITS; idx += C::NTHR) {
             const int r = idx / UNITS, u = idx - r * UNITS;
             int4 val = make_int4(0, 0, 0, 0);
             if (r < tv.rows && u * 8 < p.D) {
@@ -278,7 +285,7 @@ __global__ void __launch_bounds__(128) splitkv_kernel(const __grid_constant__ CU
         const int valid_rows = min(NT, tv.sk - kt);
         if (valid_rows < NT) {
             const int zr = NT - valid_rows;
-            for (int idx = tid; idx < C::CH * zr * 8; idx += 128) {
+            for (int idx = tid; idx < C::CH * zr * 8; idx += C::NTHR) {
                 const int c = idx / (zr * 8), rem = idx - c * zr * 8;
                 *reinterpret_cast<int4*>(vst + (c * NT + valid_rows + (rem >> 3)) * 128 + ((rem & 7) << 4)) =
                     make_int4(0, 0, 0, 0);
@@ -286,7 +293,8 @@ __global__ void __launch_bounds__(128) splitkv_kernel(const __grid_constant__ CU
             fence_proxy_async_smem();  // this stage is rewritten by TMA later
         }
 
-        // S = Q K^T for keys [warp*KW, warp*KW + KW) of the tile.
+        // S = Q K^T for keys [ws*KW, ws*KW + KW) of the tile, over head-dim part kp
+        const int ws = warp & 3, kp = warp >> 2;
         float s_acc[MT][C::KW / 8][4];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
@@ -296,14 +304,15 @@ __global__ void __launch_bounds__(128) splitkv_kernel(const __grid_constant__ CU
                 for (int e = 0; e < 4; ++e) s_acc[mt][n][e] = 0.f;
         const uint32_t k_base = smem_addr(kst);
 #pragma unroll
-        for (int ks = 0; ks < DP / 16; ++ks) {
+        for (int kq = 0; kq < DP / 16 / C::KSPLIT; ++kq) {
+            const int ks = kp * (DP / 16 / C::KSPLIT) + kq;
             const int c = ks >> 2, u0 = (ks & 3) * 2;
             uint32_t bf[C::KW / 8][2];
             if constexpr (C::KW == 16) {
-                const int key = warp * 16 + rr + ((mi >> 1) << 3);
+                const int key = ws * 16 + rr + ((mi >> 1) << 3);
                 ldsm_x4(k_base + c * NT * 128 + swz128(key, u0 + (mi & 1)), bf[0][0], bf[0][1], bf[1][0], bf[1][1]);
             } else {
-                const int key = warp * 8 + rr;
+                const int key = ws * 8 + rr;
                 ldsm_x2(k_base + c * NT * 128 + swz128(key, u0 + (mi & 1)), bf[0][0], bf[0][1]);
             }
 #pragma unroll
@@ -315,7 +324,8 @@ __global__ void __launch_bounds__(128) splitkv_kernel(const __grid_constant__ CU
                 for (int n = 0; n < C::KW / 8; ++n) MmaOp<T>::run(s_acc[mt][n], af, bf[n][0], bf[n][1]);
             }
         }
-        // scale into the log2 domain and mask by select (NaN-safe) -> shared scores
+        // raw partial scores -> shared memory (part kp)
+        float* Sp = S + kp * (M * C::S_STRIDE);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -323,17 +333,9 @@ __global__ void __launch_bounds__(128) splitkv_kernel(const __grid_constant__ CU
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
                     const int r = mt * 16 + (lane >> 2) + h2 * 8;
-                    const int col = warp * C::KW + n * 8 + (lane & 3) * 2;
-                    const int j = kt + col;
-                    const int lo = row_lo[r], hi = row_hi[r], dg = row_dg[r];
-                    const float ab = row_ab[r];
-                    float2 sv;
-                    sv.x = (j >= lo && j <= hi) ? biased_log2(s_acc[mt][n][h2 * 2], p.scale_log2, ab, dg, j)
-                                                : -INFINITY;
-                    sv.y = (j + 1 >= lo && j + 1 <= hi)
-                               ? biased_log2(s_acc[mt][n][h2 * 2 + 1], p.scale_log2, ab, dg, j + 1)
-                               : -INFINITY;
-                    *reinterpret_cast<float2*>(S + r * C::S_STRIDE + col) = sv;
+                    const int col = ws * C::KW + n * 8 + (lane & 3) * 2;
+                    *reinterpret_cast<float2*>(Sp + r * C::S_STRIDE + col) =
+                        make_float2(s_acc[mt][n][h2 * 2], s_acc[mt][n][h2 * 2 + 1]);
                 }
         if (__syncthreads_or(!ok)) {
             if (tid == 0) flag_error(p.err, PA_ERR_DEVICE_TIMEOUT);
@@ -345,12 +347,21 @@ __global__ void __launch_bounds__(128) splitkv_kernel(const __grid_constant__ CU
             issue(it + STAGES - 1);
         }
 
-        // online softmax: warp w owns rows w, w+4, ...
+        // online softmax: warp w owns rows w, w+NW, ...; the score is scaled into the log2
+        // domain (plus the position bias) and masked by select (NaN-safe)
 #pragma unroll
         for (int k = 0; k < RPW; ++k) {
-            const int r = warp + 4 * k;
-            const float v0 = S[r * C::S_STRIDE + lane];
-            const float v1 = (NT == 64) ? S[r * C::S_STRIDE + lane + 32] : -INFINITY;
+            const int r = warp + NW * k;
+            const int lo = row_lo[r], hi = row_hi[r], dg = row_dg[r];
+            const float ab = row_ab[r];
+            auto score = [&](int col) {
+                float sv = S[r * C::S_STRIDE + col];
+                if (C::KSPLIT == 2) sv += S[(M + r) * C::S_STRIDE + col];
+                const int j = kt + col;
+                return (j >= lo && j <= hi) ? biased_log2(sv, p.scale_log2, ab, dg, j) : -INFINITY;
+            };
+            const float v0 = score(lane);
+            const float v1 = (NT == 64) ? score(lane + 32) : -INFINITY;
             float mx = fmaxf(v0, v1);
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
@@ -412,8 +423,8 @@ __global__ void __launch_bounds__(128) splitkv_kernel(const __grid_constant__ CU
 #pragma unroll
     for (int k = 0; k < RPW; ++k) {
         if (lane == 0) {
-            m_sm[warp + 4 * k] = m_run[k];
-            l_sm[warp + 4 * k] = l_run[k];
+            m_sm[warp + NW * k] = m_run[k];
+            l_sm[warp + NW * k] = l_run[k];
         }
     }
     __syncthreads();

@@ -12,22 +12,24 @@
 namespace pa {
 
 template <int DP>
-struct SplitShape;  // tile width and pipeline depth per padded head dim
+struct SplitShape;  // tile width, pipeline depth and warps per padded head dim
 template <>
 struct SplitShape<64> {
-    static constexpr int NT = 64, STAGES = 4;
+    static constexpr int NT = 64, STAGES = 4, NW = 4;
 };
 template <>
 struct SplitShape<128> {
-    static constexpr int NT = 64, STAGES = 3;
+    static constexpr int NT = 64, STAGES = 3, NW = 4;
 };
 template <>
 struct SplitShape<256> {
-    static constexpr int NT = 64, STAGES = 3;
+    static constexpr int NT = 64, STAGES = 3, NW = 4;
 };
 template <>
 struct SplitShape<512> {
-    static constexpr int NT = 32, STAGES = 2;  // 3 stages would exceed 227 KB with a 32-row Q tile
+    // 3 stages would exceed 227 KB with a 32-row Q tile; 8 warps (253 registers a thread
+    // with 4: the issue latency of the MMA chains, not the loads, bounded the kernel)
+    static constexpr int NT = 32, STAGES = 2, NW = 8;
 };
 
 // The combine as a programmatic dependent launch of the split kernel before it on the
@@ -52,9 +54,9 @@ static cudaError_t launch_combine(dim3 grid, const SplitParams& sp, cudaStream_t
 template <typename T, int DP, int MT>
 static int run_splitkv(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& sp, const SplitPlan& plan,
                        cudaStream_t stream, char* msg, size_t msg_len) {
-    constexpr int NT = SplitShape<DP>::NT, STAGES = SplitShape<DP>::STAGES;
-    using C = SplitCfg<DP, MT, NT, STAGES>;
-    auto kern = splitkv_kernel<T, DP, MT, NT, STAGES>;
+    constexpr int NT = SplitShape<DP>::NT, STAGES = SplitShape<DP>::STAGES, NW = SplitShape<DP>::NW;
+    using C = SplitCfg<DP, MT, NT, STAGES, NW>;
+    auto kern = splitkv_kernel<T, DP, MT, NT, STAGES, NW>;
     static bool configured = false;  // attribute set once per process (per instantiation)
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -66,7 +68,7 @@ static int run_splitkv(const CUtensorMap& tk, const CUtensorMap& tv, const Split
     }
     dim3 grid(plan.max_splits, sp.Hkv * plan.row_tiles, sp.batch);
     timer_begin(PA_KC_SPLITKV, stream);
-    kern<<<grid, 128, C::SMEM, stream>>>(tk, tv, sp);
+    kern<<<grid, C::NTHR, C::SMEM, stream>>>(tk, tv, sp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "split-KV launch: %s", cudaGetErrorString(e));
@@ -172,8 +174,9 @@ static int decode_occupancy() {
 
 template <typename T, int DP, int MT>
 static int generic_occupancy() {
-    constexpr int NT = SplitShape<DP>::NT, STAGES = SplitShape<DP>::STAGES;
-    static const int n = resident_ctas(splitkv_kernel<T, DP, MT, NT, STAGES>, 128, SplitCfg<DP, MT, NT, STAGES>::SMEM);
+    constexpr int NT = SplitShape<DP>::NT, STAGES = SplitShape<DP>::STAGES, NW = SplitShape<DP>::NW;
+    using C = SplitCfg<DP, MT, NT, STAGES, NW>;
+    static const int n = resident_ctas(splitkv_kernel<T, DP, MT, NT, STAGES, NW>, C::NTHR, C::SMEM);
     return n;
 }
 
