@@ -69,13 +69,35 @@ def algorithmic(lay, seqs=None):
     return flops, kv + qo + lse
 
 
+def l2_label(nbytes):
+    return ("inputs larger than L2 (no flush)" if nbytes > 2 * L2_BYTES
+            else "inputs fit in L2: flushed before every timed call (outside the timed events)")
+
+
+class L2Flush:
+    """Writes a buffer three times the size of L2 before each timed call when the step's
+    inputs are small enough to stay resident in L2 between calls; a no-op otherwise."""
+
+    def __init__(self, nbytes):
+        import torch
+        self.buf = (torch.empty(3 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+                    if nbytes <= 2 * L2_BYTES else None)
+
+    def __bool__(self):
+        return self.buf is not None
+
+    def __call__(self):
+        if self.buf is not None:
+            self.buf.zero_()
+
+
 def workload_config(lay, flops, nbytes, world):
     """The `config` object of the JSON line (both arms)."""
     return {"workload": lay.name, "batch": lay.batch, "num_heads": lay.num_heads,
             "num_heads_k": lay.num_heads_k, "head_dim": lay.head_dim,
             "page_block_size": lay.page_block_size, "max_seqlen_k": lay.max_seqlen_k,
             "total_keys": lay.total_k, "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
-            "l2": "inputs larger than L2 (no flush)" if nbytes > 2 * L2_BYTES else "L2 not flushed; inputs fit",
+            "l2": l2_label(nbytes),
             "parallelism": f"replicas{world}",
             **({"alibi_slopes": "2^(-8 (h + 1) / H)"} if ALIBI["slopes"] is not None else {})}
 
@@ -118,7 +140,7 @@ def kernel_class_seqs(lay):
     return {"prefill": pre, "splitkv": split}
 
 
-def time_kernels(binding, g, lay, steps):
+def time_kernels(binding, g, lay, steps, flush=None):
     """Per-kernel device time: the library brackets each launch with CUDA events on the
     stream it is launched on.  Returns {class: (ms per launch, launches per step)}."""
     import torch
@@ -129,6 +151,8 @@ def time_kernels(binding, g, lay, steps):
     binding.kernel_timing(True)
     try:
         for _ in range(steps):
+            if flush:
+                flush()
             _call(binding, g, lay, out, lse)
         torch.cuda.synchronize()
     finally:
@@ -255,7 +279,7 @@ def _call(binding, g, lay, out, lse, stream=None):
                        alibi_slopes=_slopes_on(g.q.device))
 
 
-def time_device(binding, g, lay, steps, warmup, dist):
+def time_device(binding, g, lay, steps, warmup, dist, flush=None):
     import torch
     out = torch.empty_like(g.q)
     lse = torch.empty((lay.num_heads, lay.total_q), dtype=torch.float32, device=g.q.device)
@@ -271,15 +295,29 @@ def time_device(binding, g, lay, steps, warmup, dist):
         dist.barrier()
     torch.cuda.synchronize()
     n0 = binding.kernel_launches()
-    e0.record(stream)
-    for _ in range(steps):
-        _call(binding, g, lay, out, lse)
-    e1.record(stream)
-    torch.cuda.synchronize()
+    if flush:
+        # each call timed on its own, the L2 flush before it outside the events
+        pairs = []
+        for _ in range(steps):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            _call(binding, g, lay, out, lse)
+            b.record(stream)
+            pairs.append((a, b))
+        torch.cuda.synchronize()
+        total = sum(a.elapsed_time(b) for a, b in pairs)
+    else:
+        e0.record(stream)
+        for _ in range(steps):
+            _call(binding, g, lay, out, lse)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        total = e0.elapsed_time(e1)
     if dist:
         dist.barrier()
     launches = binding.kernel_launches() - n0
-    return e0.elapsed_time(e1) / steps, launches
+    return total / steps, launches
 
 
 def time_e2e(binding, g, lay, steps, warmup):
@@ -396,7 +434,8 @@ def run_ours(args):
         for _ in range(20):
             _call(binding, g, lay, out, lse)
         torch.cuda.synchronize()
-    ms, launches = time_device(binding, g, lay, args.steps, args.warmup, dist)
+    flush = L2Flush(nbytes)
+    ms, launches = time_device(binding, g, lay, args.steps, args.warmup, dist, flush)
     clocks = sampler.stop()
     ms = max_over_ranks(ms, dist, "cuda")
     tensor_bound = flops / nbytes > (bf16 * 1e12) / (hbm * 1e9)
@@ -408,7 +447,7 @@ def run_ours(args):
 
     # roofline of the dominant kernel: its algorithmic work per launch over its own average
     # launch duration (CUDA events around each launch, on the stream it runs on)
-    per_kernel = time_kernels(binding, g, lay, max(3, min(args.steps, 20)))
+    per_kernel = time_kernels(binding, g, lay, max(3, min(args.steps, 20)), flush)
     # a class without sequences of its own (e.g. the split-KV pass of a prefill-only batch)
     # launches CTAs that exit at once; its events then mostly time the wait for SMs
     with_work = {k: v for k, v in per_kernel.items()
@@ -513,19 +552,32 @@ def run_append(args):
     torch.cuda.synchronize()
     assert binding.device_status() == 0, binding.last_error()
     stream = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush = L2Flush(nbytes)
     n0 = binding.kernel_launches()
-    e0.record(stream)
+    pairs = []
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if not flush:
+        e0.record(stream)
     for _ in range(args.steps):
-        step()
-    e1.record(stream)
+        if flush:  # each call timed on its own, the L2 flush before it outside the events
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            step()
+            b.record(stream)
+            pairs.append((a, b))
+        else:
+            step()
+    if not flush:
+        e1.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
     launches = binding.kernel_launches() - n0
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = (sum(a.elapsed_time(b) for a, b in pairs) if flush else e0.elapsed_time(e1)) / args.steps
     binding.kernel_times()
     binding.kernel_timing(True)
     for _ in range(max(3, min(args.steps, 20))):
+        flush()
         step()
     torch.cuda.synchronize()
     binding.kernel_timing(False)
@@ -535,7 +587,7 @@ def run_append(args):
     achieved = nbytes / (k_ms / k_n * 1e-3) / 1e9
     cfg = workload_config(lay, 0, nbytes, 1)
     cfg.update({"op": "kv_append", "new_tokens": lay.total_q,
-                "l2": "inputs larger than L2 (no flush)" if nbytes > 2 * L2_BYTES else "L2 not flushed; inputs fit"})
+                "l2": l2_label(nbytes)})
     print(json.dumps({
         "metric": "KV append GB/s (K and V read + written), % of GB300 HBM roofline", "value": round(value, 2),
         "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
