@@ -69,19 +69,24 @@ def algorithmic(lay, seqs=None):
     return flops, kv + qo + lse
 
 
-def l2_label(nbytes):
-    return ("inputs larger than L2 (no flush)" if nbytes > 2 * L2_BYTES
-            else "inputs fit in L2: flushed before every timed call (outside the timed events)")
+def pool_bytes(lay):
+    """Bytes of the K and V pools (the data a step re-reads from one call to the next)."""
+    return 2 * lay.num_blocks * lay.page_block_size * lay.num_heads_k * lay.head_dim * 2
+
+
+def l2_label(nbytes, what="K/V"):
+    return (f"{what} larger than twice L2 (no flush)" if nbytes > 2 * L2_BYTES
+            else f"{what} within twice L2: L2 flushed before every timed call (outside the timed events)")
 
 
 class L2Flush:
-    """Writes a buffer three times the size of L2 before each timed call when the step's
-    inputs are small enough to stay resident in L2 between calls; a no-op otherwise."""
+    """Writes a buffer three times the size of L2 before each timed call when the K/V a
+    step reads is small enough to stay resident in L2 between calls; a no-op otherwise."""
 
-    def __init__(self, nbytes):
+    def __init__(self, kv_bytes):
         import torch
         self.buf = (torch.empty(3 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
-                    if nbytes <= 2 * L2_BYTES else None)
+                    if kv_bytes <= 2 * L2_BYTES else None)
 
     def __bool__(self):
         return self.buf is not None
@@ -91,13 +96,39 @@ class L2Flush:
             self.buf.zero_()
 
 
+def timed_calls(step, steps, flush):
+    """Average device time (ms) of `steps` calls of `step` on the current stream: one event
+    pair around all of them, or, when L2 is flushed, one pair around each call with the
+    flush before it outside the events."""
+    import torch
+    stream = torch.cuda.current_stream()
+    if not flush:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+    pairs = []
+    for _ in range(steps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        pairs.append((a, b))
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in pairs) / steps
+
+
 def workload_config(lay, flops, nbytes, world):
     """The `config` object of the JSON line (both arms)."""
     return {"workload": lay.name, "batch": lay.batch, "num_heads": lay.num_heads,
             "num_heads_k": lay.num_heads_k, "head_dim": lay.head_dim,
             "page_block_size": lay.page_block_size, "max_seqlen_k": lay.max_seqlen_k,
             "total_keys": lay.total_k, "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
-            "l2": l2_label(nbytes),
+            "l2": l2_label(pool_bytes(lay)),
             "parallelism": f"replicas{world}",
             **({"alibi_slopes": "2^(-8 (h + 1) / H)"} if ALIBI["slopes"] is not None else {})}
 
@@ -289,35 +320,15 @@ def time_device(binding, g, lay, steps, warmup, dist, flush=None):
     st = binding.device_status()
     if st != 0:
         raise RuntimeError(f"device status {st}: {binding.last_error()}")
-    stream = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     n0 = binding.kernel_launches()
-    if flush:
-        # each call timed on its own, the L2 flush before it outside the events
-        pairs = []
-        for _ in range(steps):
-            flush()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            _call(binding, g, lay, out, lse)
-            b.record(stream)
-            pairs.append((a, b))
-        torch.cuda.synchronize()
-        total = sum(a.elapsed_time(b) for a, b in pairs)
-    else:
-        e0.record(stream)
-        for _ in range(steps):
-            _call(binding, g, lay, out, lse)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        total = e0.elapsed_time(e1)
+    ms = timed_calls(lambda: _call(binding, g, lay, out, lse), steps, flush)
     if dist:
         dist.barrier()
     launches = binding.kernel_launches() - n0
-    return total / steps, launches
+    return ms, launches
 
 
 def time_e2e(binding, g, lay, steps, warmup):
@@ -434,7 +445,7 @@ def run_ours(args):
         for _ in range(20):
             _call(binding, g, lay, out, lse)
         torch.cuda.synchronize()
-    flush = L2Flush(nbytes)
+    flush = L2Flush(pool_bytes(lay))
     ms, launches = time_device(binding, g, lay, args.steps, args.warmup, dist, flush)
     clocks = sampler.stop()
     ms = max_over_ranks(ms, dist, "cuda")
@@ -496,9 +507,10 @@ def run_ours(args):
             set_alibi(args, lay2)
             g2 = workloads.materialize(lay2, device="cuda")
             f2, b2 = algorithmic(lay2)
-            ms2, l2 = time_device(binding, g2, lay2, 3, 2, None)
+            flush2 = L2Flush(pool_bytes(lay2))
+            ms2, l2 = time_device(binding, g2, lay2, 3, 2, None, flush2)
             tf = f2 / (ms2 * 1e-3) / 1e12
-            pk = time_kernels(binding, g2, lay2, 3).get("prefill")
+            pk = time_kernels(binding, g2, lay2, 3, flush2).get("prefill")
             f_pre = algorithmic(lay2, kernel_class_seqs(lay2)["prefill"])[0]
             tf_k = f_pre / pk[1] / (pk[0] * 1e-3) / 1e12 if pk else None
             result["secondary"] = {"workload": lay2.name, "value": round(tf, 2), "unit": "TFLOP/s",
@@ -508,6 +520,7 @@ def run_ours(args):
                                                 "unit": "TFLOP/s", "frac": round(tf_k / bf16, 4) if tf_k else None,
                                                 "kernel_ms": round(pk[0], 5) if pk else None,
                                                 "traffic": profiled_traffic(lay2.name)},
+                                   "l2": l2_label(pool_bytes(lay2)),
                                    "gpu_launches": int(l2)}
             del g2
         except Exception as e:  # reported, not hidden
@@ -551,29 +564,11 @@ def run_append(args):
         step()
     torch.cuda.synchronize()
     assert binding.device_status() == 0, binding.last_error()
-    stream = torch.cuda.current_stream()
-    flush = L2Flush(nbytes)
+    flush = L2Flush(nbytes)  # the bytes an append step touches (new rows in, their slots out)
     n0 = binding.kernel_launches()
-    pairs = []
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if not flush:
-        e0.record(stream)
-    for _ in range(args.steps):
-        if flush:  # each call timed on its own, the L2 flush before it outside the events
-            flush()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            step()
-            b.record(stream)
-            pairs.append((a, b))
-        else:
-            step()
-    if not flush:
-        e1.record(stream)
-    torch.cuda.synchronize()
+    ms = timed_calls(step, args.steps, flush)
     clocks = sampler.stop()
     launches = binding.kernel_launches() - n0
-    ms = (sum(a.elapsed_time(b) for a, b in pairs) if flush else e0.elapsed_time(e1)) / args.steps
     binding.kernel_times()
     binding.kernel_timing(True)
     for _ in range(max(3, min(args.steps, 20))):
@@ -587,7 +582,7 @@ def run_append(args):
     achieved = nbytes / (k_ms / k_n * 1e-3) / 1e9
     cfg = workload_config(lay, 0, nbytes, 1)
     cfg.update({"op": "kv_append", "new_tokens": lay.total_q,
-                "l2": l2_label(nbytes)})
+                "l2": l2_label(nbytes, "bytes moved")})
     print(json.dumps({
         "metric": "KV append GB/s (K and V read + written), % of GB300 HBM roofline", "value": round(value, 2),
         "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
@@ -629,20 +624,16 @@ def run_padded(args):
         step()
     torch.cuda.synchronize()
     assert binding.device_status() == 0, binding.last_error()
-    stream = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    kv_bytes = 2 * B * S * Hkv * D * 2
+    flush = L2Flush(kv_bytes)
     n0 = binding.kernel_launches()
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    ms = timed_calls(step, args.steps, flush)
     clocks = sampler.stop()
     launches = binding.kernel_launches() - n0
-    ms = e0.elapsed_time(e1) / args.steps
     binding.kernel_times()
     binding.kernel_timing(True)
     for _ in range(max(3, min(args.steps, 10))):
+        flush()
         step()
     torch.cuda.synchronize()
     binding.kernel_timing(False)
@@ -656,7 +647,7 @@ def run_padded(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "padded_causal_bf16", "op": "fwd_padded", "batch": B, "seqlen": S, "num_heads": H,
                    "num_heads_k": Hkv, "head_dim": D, "algorithmic_flops": flops, "algorithmic_bytes": nbytes,
-                   "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas1",
+                   "l2": l2_label(kv_bytes), "parallelism": "replicas1",
                    **({"alibi_slopes": "2^(-8 (h + 1) / H)"} if args.alibi else {})},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16, "unit": "TFLOP/s",
                      "frac": round(achieved / bf16, 4), "traffic": None, "kernel": "prefill_kernel",
