@@ -597,13 +597,15 @@ SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, int num_sms)
     } else if (pl.row_tiles == 1) {
         // Fewer (sequence, kv head) units than resident CTA slots: one wave, every unit's keys
         // split evenly over slots / units CTAs (each further wave would add a pipeline ramp,
-        // a merge and a partial result per CTA).  Otherwise about four CTAs per SM, which
-        // balances sequences of different lengths (unknown on the host).  A split is never
-        // shorter than 4 tiles, nor than 8 M keys: its fp32 partial result (M rows x D x 4
-        // bytes, written and read back) then costs at most ~1/8 of the K/V bytes it reads.
+        // a merge and a partial result per CTA).  Otherwise one CTA per unit, no split and no
+        // combine: launched longest first, the units themselves even out the waves (on 64
+        // decode sequences of U[512, 4096] keys, 512 units over 304 slots: 6.37 TB/s, against
+        // 5.72 with two splits per unit and 5.61 with three).  A split is never shorter than
+        // 4 tiles, nor than 8 M keys: its fp32 partial result (M rows x D x 4 bytes, written
+        // and read back) then costs at most ~1/8 of the K/V bytes it reads.
         const int64_t slots =
             (int64_t)num_sms * (a.dtype == PA_BF16 ? splitkv_occupancy_bf16(pl) : splitkv_occupancy_f16(pl));
-        int64_t splits = units < slots ? slots / units : (4ll * num_sms + units - 1) / units;
+        int64_t splits = units < slots ? slots / units : 1;
         splits = std::max<int64_t>(1, std::min(splits, tiles_max));
         const int64_t min_tiles = std::max<int64_t>(4, (8ll * M + pl.nt - 1) / pl.nt);
         split_tiles = std::max<int64_t>(min_tiles, (tiles_max + splits - 1) / splits);
