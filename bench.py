@@ -4,9 +4,11 @@
 A step is one pa_varlen_fwd call over one synthetic serving batch (default: the
 decode batch -- 64 sequences, q_len 1, sk ~ U[512, 4096], H=32, Hkv=8, D=128,
 page 32, bf16).  The headline value is the algorithmic KV GB/s of that step; the
-roofline object compares it with the measured HBM copy bandwidth.  A secondary
-measurement reports the causal-prefill workload in TFLOP/s against the measured
-dense bf16 peak.
+roofline object compares its dominant kernel with the measured HBM copy bandwidth (and,
+labelled apart, with the nominal ~7.9 TB/s).  Beside it: `secondary`, the causal-prefill
+workload in TFLOP/s against the measured (and nominal) dense bf16 peak, and `workloads`,
+the chunked-prefill + decode batch with a sliding window and the long-context split-KV
+batches at head_dim 256 and 512, each with its own roofline.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -19,7 +21,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -34,7 +35,14 @@ import numpy as np  # noqa: E402
 METRIC = "paged-attn TFLOP/s (prefill) and KV GB/s (decode), % of GB300 roofline"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+# nominal GB300 figures: HBM3e ~7.9 TB/s, dense bf16 tensor 2.25 PFLOP/s (the targets' "~8 TB/s"
+# and "dense bf16 peak"); reported beside the measured copy / matmul rates, labelled as such
+NOMINAL_HBM_GBS = 7900.0
+NOMINAL_BF16_TFLOPS = 2250.0
 L2_BYTES = 129 * 1024 * 1024
+# the serving workloads measured beside the headline (chunked prefill + decode with a window,
+# long-context split-KV decode at head_dim 256 and 512)
+EXTRA_WORKLOADS = ("mixed_bf16", "long_bf16", "long_d512_bf16")
 
 
 # ---- algorithmic work (closed form per query row) -----------------------------------------
@@ -216,18 +224,38 @@ def csrc_hash():
     return h.hexdigest()[:16]
 
 
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
+
+
 def profiled_traffic(workload):
-    """DRAM bytes per launch from the committed ncu summary of this workload, or None if
-    the summary is missing or was taken on different kernel sources."""
-    path = os.path.join(ROOT, "profiles", f"{workload}.md")
-    if not os.path.exists(path):
+    """DRAM bytes per launch of the workload's dominant kernel from the committed ncu capture
+    (profiles/traffic.json: dram__bytes_read.sum + dram__bytes_write.sum, with the hash of the
+    kernel sources it was taken on), or None if there is none for the current sources."""
+    try:
+        entry = json.load(open(TRAFFIC_JSON))["captures"][workload]
+    except Exception:
         return None
-    text = open(path).read()
-    m_bytes = re.search(r"dram_bytes_per_call:\s*([0-9.eE+]+)", text)
-    m_hash = re.search(r"csrc_sha256_16:\s*([0-9a-f]+)", text)
-    if not m_bytes or not m_hash or m_hash.group(1) != csrc_hash():
+    if entry.get("csrc_sha256_16") != csrc_hash():
         return None
-    return float(m_bytes.group(1))
+    return float(entry["dram_read_bytes"]) + float(entry["dram_write_bytes"])
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or None."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return None
 
 
 class ClockSampler:
@@ -411,6 +439,74 @@ def cpu_baseline(lay, inp_cpu, budget_s=20.0):
     return work / t_total, unit, t_total, oracle.threads(), sample
 
 
+def kernel_names(lay):
+    """Kernel class -> kernel name for a workload (the split-KV class is the warp-sliced
+    decode kernel for rows of at most 32 and head_dim up to 256, else the general kernel)."""
+    G = lay.num_heads // lay.num_heads_k
+    rows = max(q for q in lay.seqlens_q) * G if not kernel_class_seqs(lay)["prefill"] else 32
+    dec = "decode_kernel" if rows <= 32 and lay.head_dim <= 256 else "splitkv_kernel"
+    return {"prefill": "prefill_kernel", "combine": "combine_kernel", "splitkv": dec}
+
+
+def roofline_of(binding, g, lay, steps, flush):
+    """The roofline object of a workload's dominant kernel: its algorithmic work per launch
+    (bytes of its sequences for the split-KV pass, FLOPs for the prefill kernel) over its own
+    average launch duration (CUDA events around each launch, on the stream it runs on),
+    against the measured peak, and beside it against the nominal GB300 peak."""
+    hbm, bf16, _, peak_kind = peaks()
+    per_kernel = time_kernels(binding, g, lay, steps, flush)
+    # a class without sequences of its own (e.g. the split-KV pass of a prefill-only batch)
+    # launches CTAs that exit at once; its events then mostly time the wait for SMs
+    classes = kernel_class_seqs(lay)
+    with_work = {k: v for k, v in per_kernel.items() if k == "combine" or classes.get(k)}
+    dom = max((k for k in with_work if k != "combine"), key=lambda k: with_work[k][0] * with_work[k][1],
+              default="combine")
+    dom_ms, dom_launches = per_kernel[dom]
+    f_d, b_d = algorithmic(lay, classes[dom]) if dom != "combine" else algorithmic(lay)
+    dom_tensor = dom == "prefill" or (f_d / max(b_d, 1) > (bf16 * 1e12) / (hbm * 1e9))
+    if dom_tensor:
+        unit, peak, nominal, work = "TFLOP/s", bf16, NOMINAL_BF16_TFLOPS, f_d / 1e12 / dom_launches
+    else:
+        unit, peak, nominal, work = "GB/s", hbm, NOMINAL_HBM_GBS, b_d / 1e9 / dom_launches
+    achieved = work / (dom_ms * 1e-3)
+    total_ms = sum(v[0] * v[1] for v in with_work.values())
+    src = ("bf16_tflops" if dom_tensor else "hbm_gbs")
+    return {"bound": "tensor" if dom_tensor else "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": profiled_traffic(lay.name),
+            "kernel": kernel_names(lay)[dom], "kernel_ms": round(dom_ms, 5),
+            "kernel_share": round(dom_ms * dom_launches / total_ms, 4) if total_ms > 0 else None,
+            "work_per_launch": work * (1e12 if dom_tensor else 1e9),
+            "peak_source": (f"measured (MEASURED_PEAKS.json {src})" if peak_kind == "measured" else
+                            ("fallback 1.9 PFLOP/s" if dom_tensor else "fallback 6.8 TB/s")),
+            "peak_nominal": nominal, "frac_nominal": round(achieved / nominal, 4),
+            "timed": "CUDA events around each launch of the kernel, on its stream"}
+
+
+def measure(binding, lay, steps, warmup, dist, world):
+    """Whole-call device time of one workload (inputs resident in HBM, L2 flushed before every
+    call when the K/V pools fit in it), its value in the workload's unit, and its roofline."""
+    import torch
+    g = workloads_mod().materialize(lay, device="cuda")
+    flops, nbytes = algorithmic(lay)
+    hbm, bf16, _, _ = peaks()
+    flush = L2Flush(pool_bytes(lay))
+    ms, launches = time_device(binding, g, lay, steps, warmup, dist, flush)
+    ms = max_over_ranks(ms, dist, "cuda")
+    tensor_bound = flops / nbytes > (bf16 * 1e12) / (hbm * 1e9)
+    unit, work = ("TFLOP/s", flops / 1e12) if tensor_bound else ("GB/s", nbytes / 1e9)
+    value = replica_throughput(work, world, ms)
+    roof = roofline_of(binding, g, lay, max(3, min(steps, 20)), flush)
+    out = {"g": g, "flops": flops, "nbytes": nbytes, "ms": ms, "launches": launches, "unit": unit,
+           "value": value, "roofline": roof, "flush": flush}
+    torch.cuda.synchronize()
+    return out
+
+
+def workloads_mod():
+    from paged_kv_varlen_flashattention_gb300 import workloads
+    return workloads
+
+
 def run_ours(args):
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -429,70 +525,33 @@ def run_ours(args):
     lay = workloads.CONFIGS[args.workload]()
     lay.nan_fill = False
     set_alibi(args, lay)
-    g = workloads.materialize(lay, device="cuda")
-    flops, nbytes = algorithmic(lay)
-    hbm, bf16, bf16_sus, peak_kind = peaks()
+    _, bf16, _, _ = peaks()
 
-    # a sustained run of the same step while the clock sampler warms up
     if args.profile:
-        args.no_e2e = args.no_secondary = args.no_cpu_baseline = True
+        args.no_e2e = args.no_secondary = args.no_cpu_baseline = args.no_workloads = True
     sampler = ClockSampler(torch.cuda.current_device() if world == 1 else local)
     sampler.start()
-    t_end = time.time() + (0.0 if args.profile else 1.0)
-    out = torch.empty_like(g.q)
+    # a sustained run of the same step while the clock sampler warms up
+    g0 = workloads.materialize(lay, device="cuda")
+    out = torch.empty_like(g0.q)
     lse = torch.empty((lay.num_heads, lay.total_q), dtype=torch.float32, device="cuda")
+    t_end = time.time() + (0.0 if args.profile else 1.0)
     while time.time() < t_end:
         for _ in range(20):
-            _call(binding, g, lay, out, lse)
+            _call(binding, g0, lay, out, lse)
         torch.cuda.synchronize()
-    flush = L2Flush(pool_bytes(lay))
-    ms, launches = time_device(binding, g, lay, args.steps, args.warmup, dist, flush)
+    del g0, out, lse
+    m = measure(binding, lay, args.steps, args.warmup, dist, world)
     clocks = sampler.stop()
-    ms = max_over_ranks(ms, dist, "cuda")
-    tensor_bound = flops / nbytes > (bf16 * 1e12) / (hbm * 1e9)
-    if tensor_bound:
-        unit, peak, scale_w = "TFLOP/s", bf16, flops / 1e12
-    else:
-        unit, peak, scale_w = "GB/s", hbm, nbytes / 1e9
-    value = replica_throughput(scale_w, world, ms)
-
-    # roofline of the dominant kernel: its algorithmic work per launch over its own average
-    # launch duration (CUDA events around each launch, on the stream it runs on)
-    per_kernel = time_kernels(binding, g, lay, max(3, min(args.steps, 20)), flush)
-    # a class without sequences of its own (e.g. the split-KV pass of a prefill-only batch)
-    # launches CTAs that exit at once; its events then mostly time the wait for SMs
-    with_work = {k: v for k, v in per_kernel.items()
-                 if k == "combine" or kernel_class_seqs(lay).get(k)}
-    dom = max((k for k in with_work if k != "combine"),
-              key=lambda k: with_work[k][0] * with_work[k][1], default="combine")
-    dom_ms, dom_launches = per_kernel[dom]
-    f_d, b_d = algorithmic(lay, kernel_class_seqs(lay)[dom]) if dom != "combine" else (flops, nbytes)
-    dom_tensor = dom == "prefill" or (f_d / max(b_d, 1) > (bf16 * 1e12) / (hbm * 1e9))
-    if dom_tensor:
-        r_unit, r_peak, r_work = "TFLOP/s", bf16, f_d / 1e12 / dom_launches
-    else:
-        r_unit, r_peak, r_work = "GB/s", hbm, b_d / 1e9 / dom_launches
-    achieved = r_work / (dom_ms * 1e-3)
-    total_ms = sum(v[0] * v[1] for v in with_work.values())
-    kernel_names = {"prefill": "prefill_kernel", "combine": "combine_kernel",
-                    "splitkv": "decode_kernel" if max(lay.seqlens_q) * lay.num_heads // lay.num_heads_k <= 32
-                    and lay.head_dim <= 256 else "decode_kernel/splitkv_kernel"}
+    g, flops, nbytes = m["g"], m["flops"], m["nbytes"]
 
     result = {
-        "metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": round(m["value"], 2), "unit": m["unit"], "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(m["ms"], 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if lay.dtype == "bf16" else "f16", "data": "synthetic",
         "config": workload_config(lay, flops, nbytes, world),
-        "roofline": {"bound": "tensor" if dom_tensor else "hbm", "achieved": round(achieved, 1), "peak": r_peak,
-                     "unit": r_unit, "frac": round(achieved / r_peak, 4), "traffic": profiled_traffic(lay.name),
-                     "kernel": kernel_names[dom], "kernel_ms": round(dom_ms, 5),
-                     "kernel_share": round(dom_ms * dom_launches / total_ms, 4),
-                     "work_per_launch": r_work * (1e12 if dom_tensor else 1e9),
-                     "peak_source": (f"measured (MEASURED_PEAKS.json {'bf16_tflops' if dom_tensor else 'hbm_gbs'})"
-                                     if peak_kind == "measured" else
-                                     ("fallback 1.9 PFLOP/s" if dom_tensor else "fallback 6.8 TB/s")),
-                     "timed": "CUDA events around each launch of the kernel, on its stream"},
-        "gpu_launches": int(launches),
+        "roofline": m["roofline"],
+        "gpu_launches": int(m["launches"]),
         "clocks": clocks,
     }
     if rank == 0 and not args.no_e2e:
@@ -500,37 +559,46 @@ def run_ours(args):
         result["e2e"] = {"value": round(nbytes / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
                          "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                          "ms_per_step": round(ms_e2e, 4)}
+    if rank == 0 and not args.no_cpu_baseline:
+        inp_cpu = g.to("cpu")
+        val, cunit, secs, cores, sample = cpu_baseline(lay, inp_cpu, budget_s=args.cpu_budget)
+        result["cpu_baseline"] = {"value": round(val, 4), "unit": cunit, "cores": cores, "cpu_model": cpu_model(),
+                                  "kind": "oracle", "sample": sample}
+        del inp_cpu
+    del g, m
     if rank == 0 and not args.no_secondary and lay.name != "prefill_bf16":
         try:
             lay2 = workloads.CONFIGS["prefill_bf16"]()
             lay2.nan_fill = False
             set_alibi(args, lay2)
-            g2 = workloads.materialize(lay2, device="cuda")
-            f2, b2 = algorithmic(lay2)
-            flush2 = L2Flush(pool_bytes(lay2))
-            ms2, l2 = time_device(binding, g2, lay2, 3, 2, None, flush2)
-            tf = f2 / (ms2 * 1e-3) / 1e12
-            pk = time_kernels(binding, g2, lay2, 3, flush2).get("prefill")
-            f_pre = algorithmic(lay2, kernel_class_seqs(lay2)["prefill"])[0]
-            tf_k = f_pre / pk[1] / (pk[0] * 1e-3) / 1e12 if pk else None
-            result["secondary"] = {"workload": lay2.name, "value": round(tf, 2), "unit": "TFLOP/s",
-                                   "ms_per_step": round(ms2, 4), "algorithmic_flops": f2,
-                                   "roofline": {"bound": "tensor", "kernel": "prefill_kernel",
-                                                "achieved": round(tf_k, 2) if tf_k else None, "peak": bf16,
-                                                "unit": "TFLOP/s", "frac": round(tf_k / bf16, 4) if tf_k else None,
-                                                "kernel_ms": round(pk[0], 5) if pk else None,
-                                                "traffic": profiled_traffic(lay2.name)},
-                                   "l2": l2_label(pool_bytes(lay2)),
-                                   "gpu_launches": int(l2)}
-            del g2
+            m2 = measure(binding, lay2, 3, 3, None, 1)
+            roof = m2["roofline"]
+            result["secondary"] = {"workload": lay2.name, "value": round(m2["flops"] / (m2["ms"] * 1e-3) / 1e12, 2),
+                                   "unit": "TFLOP/s", "ms_per_step": round(m2["ms"], 4),
+                                   "algorithmic_flops": m2["flops"], "roofline": roof,
+                                   "l2": l2_label(pool_bytes(lay2)), "gpu_launches": int(m2["launches"])}
+            del m2
         except Exception as e:  # reported, not hidden
             result["secondary"] = {"error": str(e)[:300]}
         set_alibi(args, lay)
-    if rank == 0 and not args.no_cpu_baseline:
-        inp_cpu = g.to("cpu")
-        val, cunit, secs, cores, sample = cpu_baseline(lay, inp_cpu, budget_s=args.cpu_budget)
-        result["cpu_baseline"] = {"value": round(val, 4), "unit": cunit, "cores": cores, "kind": "oracle",
-                                  "sample": sample}
+    if rank == 0 and not args.no_workloads:
+        result["workloads"] = {}
+        for name in EXTRA_WORKLOADS:
+            if name == lay.name:
+                continue
+            try:
+                lw = workloads.CONFIGS[name]()
+                lw.nan_fill = False
+                set_alibi(args, lw)
+                mw = measure(binding, lw, 10, 3, None, 1)
+                result["workloads"][name] = {
+                    "value": round(mw["value"], 2), "unit": mw["unit"], "ms_per_step": round(mw["ms"], 5),
+                    "algorithmic_bytes": mw["nbytes"], "algorithmic_flops": mw["flops"],
+                    "roofline": mw["roofline"], "l2": l2_label(pool_bytes(lw)), "gpu_launches": int(mw["launches"])}
+                del mw
+            except Exception as e:  # reported, not hidden
+                result["workloads"][name] = {"error": str(e)[:300]}
+        set_alibi(args, lay)
     if dist:
         dist.barrier()
         dist.destroy_process_group()
@@ -702,8 +770,8 @@ def run_reference(args):
         "ms_per_step": round(secs * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
         "config": workload_config(lay, flops_all, bytes_all, world),
-        "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": oracle.threads(), "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": oracle.threads(), "cpu_model": cpu_model(),
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
@@ -722,6 +790,8 @@ def main():
                     help="run every leg with the linear position bias (geometric per-head slopes)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the mixed / long-context workloads measured beside the headline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-sequences", type=int, default=16)

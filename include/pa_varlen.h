@@ -117,6 +117,12 @@ enum {
  * allocated on first need with cudaMalloc and never while `stream` is capturing
  * (PA_ERR_WORKSPACE): before capturing a call into a CUDA graph, make one call of the
  * largest shape on the capture stream.
+ * Streams: a batch that holds prefill-class sequences (more than 32 rows of q_len x the
+ * GQA group) runs the tensor-core prefill kernel on a second stream forked from `stream`
+ * and joined back to it with events, beside the decode-class pass on `stream`.  The
+ * library keeps one such side stream (with its two events) per (device, caller stream),
+ * created by the first such call on that stream: make it before capturing `stream` into a
+ * graph.  Two caller streams never share a side stream, so their prefill work can overlap.
  * Thread safety: calls from several host threads are safe.
  */
 int pa_varlen_fwd(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
@@ -147,7 +153,9 @@ int pa_varlen_fwd(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor*
  * race and give undefined results, so serialise them (one stream, or events).
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, which allocates nothing); make that first call before any stream
- * capture.  It calls no cudaMalloc, cudaFree or allocating library routine.
+ * capture.  It calls no cudaMalloc, cudaFree or allocating library routine, and creates no
+ * stream or event: a batch with prefill-class sequences runs its prefill kernel and its
+ * decode-class pass one after the other on `stream` (pa_varlen_fwd overlaps them).
  */
 int pa_varlen_fwd_noalloc(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
                           const pa_tensor* cu_seqlens_q, const pa_tensor* cu_seqlens_k,

@@ -265,6 +265,19 @@ int validate(const pa_tensor* q, const pa_tensor* k, const pa_tensor* v, const p
     a->lse_s0 = lse->stride[0];
     a->total_q = total_q;
     a->alibi = alibi ? static_cast<const float*>(alibi->data) : nullptr;
+    // grid limits of the launches: the split-KV pass puts (kv head, row tile) in grid.y.
+    // Long rows go to the tensor-core prefill kernel when it takes the call (one row tile
+    // left for the split-KV pass); otherwise every 32 rows of the longest sequence are a tile.
+    if (hkv > 65535) return fail(PA_ERR_UNSUPPORTED, "num_heads_k %lld exceeds 65535", (long long)hkv);
+    if (!pa::prefill_supported(*a)) {
+        const int64_t rows = std::max<int64_t>(1, (int64_t)max_sq * (hq / hkv));
+        const int64_t row_tiles = rows <= 16 ? 1 : (rows + 31) / 32;
+        if (hkv * row_tiles > 65535)
+            return fail(PA_ERR_UNSUPPORTED,
+                        "num_heads_k (%lld) x row tiles of max_seqlen_q x group (%lld) exceeds 65535 CTAs per "
+                        "sequence for this head_dim / group size; split the call into shorter query chunks",
+                        (long long)hkv, (long long)row_tiles);
+    }
     g_msg[0] = '\0';
     return PA_OK;
 }
@@ -415,21 +428,25 @@ int grow_buffer(std::map<std::pair<int, cudaStream_t>, pa::Workspace>& buffers, 
 
 int workspace_for(cudaStream_t stream, size_t bytes, void** ptr) { return grow_buffer(g_ws, stream, bytes, ptr); }
 
-// A second stream per device on which the tensor-core prefill kernel runs beside the
-// split-KV kernel (forked from and joined back to the caller's stream with events, so
-// stream ordering and graph capture behave as for a single launch).
+// A second stream per (device, caller stream) on which the tensor-core prefill kernel runs
+// beside the split-KV kernel (forked from and joined back to the caller's stream with
+// events, so stream ordering and graph capture behave as for a single launch).  Each caller
+// stream has its own, so the prefill work of two serving streams does not queue behind one
+// another; the entry's mutex orders the fork/launch/join of callers sharing one stream.
 struct SideStream {
     cudaStream_t stream = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
+    std::mutex mu;
 };
-std::mutex g_side_mu;  // also orders the fork/launch/join sequence of concurrent callers
-SideStream g_side[256];
+std::mutex g_side_mu;  // guards the map only
+std::map<std::pair<int, cudaStream_t>, SideStream> g_side;
 
-int side_stream(SideStream** out) {
+int side_stream(cudaStream_t caller, SideStream** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= 256) return fail(PA_ERR_CUDA, "cudaGetDevice failed");
-    SideStream& ss = g_side[dev];
+    if (e != cudaSuccess) return fail(PA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    std::lock_guard<std::mutex> lock(g_side_mu);
+    SideStream& ss = g_side[{dev, caller}];  // std::map: the entry's address never changes
     if (!ss.stream) {
         if ((e = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking)) != cudaSuccess ||
             (e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess ||
@@ -648,18 +665,21 @@ int forward_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
                  int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_heads, int32_t num_heads_k,
                  int32_t head_dim, int32_t page_block_size, float softmax_scale, int32_t window_left,
                  int32_t window_right, const pa_tensor* alibi_slopes, const pa_tensor* out,
-                 const pa_tensor* softmax_lse, void* stream, ScratchFn scratch, void* scratch_ctx) {
+                 const pa_tensor* softmax_lse, void* stream, ScratchFn scratch, void* scratch_ctx,
+                 bool side_stream_ok) {
+    NvtxRange range("pa_varlen_fwd");
     pa::Args a{};
     int rc = validate(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, max_seqlen_q, max_seqlen_k,
                       num_heads, num_heads_k, head_dim, page_block_size, softmax_scale, window_left, window_right,
                       alibi_slopes, out, softmax_lse, true, &a);
     if (rc != PA_OK) return rc;
-    return launch_forward(a, stream, scratch, scratch_ctx);
+    return launch_forward(a, stream, scratch, scratch_ctx, side_stream_ok);
 }
 
 // Everything after the host checks: split plan, scratch, and the launches (prefill on the
-// side stream beside the split-KV pass on the caller's stream).
-int launch_forward(pa::Args& a, void* stream, ScratchFn scratch, void* scratch_ctx) {
+// caller stream's side stream beside the split-KV pass on the caller's stream, or both on
+// the caller's stream one after the other when `side_stream_ok` is false).
+int launch_forward(pa::Args& a, void* stream, ScratchFn scratch, void* scratch_ctx, bool side_stream_ok) {
     int rc = PA_OK;
     a.stream = static_cast<cudaStream_t>(stream);
     a.wait_ns = pa::g_wait_ns.load(std::memory_order_relaxed);
@@ -677,16 +697,17 @@ int launch_forward(pa::Args& a, void* stream, ScratchFn scratch, void* scratch_c
         rc = scratch(scratch_ctx, a.stream, plan.ws_bytes, &ws, g_msg, sizeof g_msg);
         if (rc != PA_OK) return rc;
     }
-    if (!use_prefill) {
+    if (!use_prefill || !side_stream_ok) {
+        if (use_prefill && (rc = pa::launch_prefill(a, err, g_msg, sizeof g_msg)) != PA_OK) return rc;
         rc = pa::launch_splitkv(a, plan, ws, err, g_msg, sizeof g_msg);
         if (rc != PA_OK) return rc;
         g_msg[0] = '\0';
         return PA_OK;
     }
     // prefill-class sequences on the side stream, decode-class ones on the caller's stream
-    std::lock_guard<std::mutex> lock(g_side_mu);
     SideStream* ss = nullptr;
-    if ((rc = side_stream(&ss)) != PA_OK) return rc;
+    if ((rc = side_stream(a.stream, &ss)) != PA_OK) return rc;
+    std::lock_guard<std::mutex> lock(ss->mu);
     cudaError_t e = cudaEventRecord(ss->fork, a.stream);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->stream, ss->fork, 0);
     if (e != cudaSuccess) return fail(PA_ERR_CUDA, "forking the prefill stream: %s", cudaGetErrorString(e));
@@ -806,7 +827,7 @@ int pa_varlen_fwd(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor*
     return pa::forward_impl(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, max_seqlen_q,
                             max_seqlen_k, num_heads, num_heads_k, head_dim, page_block_size, softmax_scale,
                             window_left, window_right, nullptr, out, softmax_lse, stream, library_workspace,
-                            nullptr);
+                            nullptr, true);
 }
 
 int pa_varlen_fwd_alibi(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
@@ -818,7 +839,7 @@ int pa_varlen_fwd_alibi(const pa_tensor* q, const pa_tensor* k_cache, const pa_t
     return pa::forward_impl(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, max_seqlen_q,
                             max_seqlen_k, num_heads, num_heads_k, head_dim, page_block_size, softmax_scale,
                             window_left, window_right, alibi_slopes, out, softmax_lse, stream, library_workspace,
-                            nullptr);
+                            nullptr, true);
 }
 
 // ---- padded (non-varlen) entry points ----
@@ -837,6 +858,7 @@ int pa_fwd_padded(const pa_tensor* q, const pa_tensor* k, const pa_tensor* v, in
     if (!q || q->ndim != 4)
         return pa_check_padded(q, k, v, num_heads, num_heads_k, head_dim, softmax_scale, window_left, window_right,
                                alibi_slopes, out, softmax_lse);
+    pa::NvtxRange range("pa_fwd_padded");
     const int64_t B = q->shape[0];
     void* cu = nullptr;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -853,7 +875,7 @@ int pa_fwd_padded(const pa_tensor* q, const pa_tensor* k, const pa_tensor* v, in
     rc = pa::launch_uniform_cu(static_cast<int32_t*>(cu), static_cast<int32_t*>(cu) + (B + 1), (int)B,
                                (int)q->shape[1], (int)k->shape[1], s, g_msg, sizeof g_msg);
     if (rc != PA_OK) return rc;
-    return pa::launch_forward(a, stream, library_workspace, nullptr);
+    return pa::launch_forward(a, stream, library_workspace, nullptr, true);
 }
 
 int pa_kv_append_check(const pa_tensor* k_new, const pa_tensor* v_new, const pa_tensor* cu_seqlens_new,
@@ -867,6 +889,7 @@ int pa_kv_append_check(const pa_tensor* k_new, const pa_tensor* v_new, const pa_
 int pa_kv_append(const pa_tensor* k_new, const pa_tensor* v_new, const pa_tensor* cu_seqlens_new,
                  const pa_tensor* cu_seqlens_k, const pa_tensor* block_table, const pa_tensor* k_cache,
                  const pa_tensor* v_cache, int32_t page_block_size, void* stream) {
+    pa::NvtxRange range("pa_kv_append");
     pa::AppendArgs a{};
     int rc = validate_append(k_new, v_new, cu_seqlens_new, cu_seqlens_k, block_table, k_cache, v_cache,
                              page_block_size, true, &a);

@@ -107,6 +107,7 @@ int launch_kv_append(const AppendArgs& a, unsigned int* err, char* msg, size_t m
     // metadata is a chain of dependent loads), else the wave with several tokens per warp
     const int64_t want = (a.total_new + kAppendThreads / 32 - 1) / (kAppendThreads / 32);
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * kAppendCtasPerSm));
+    NvtxRange nv("pa::kv_append_kernel");
     timer_begin(PA_KC_APPEND, a.stream);
     kv_append_kernel<<<grid, kAppendThreads, 0, a.stream>>>(a, err);
     e = cudaGetLastError();

@@ -2,7 +2,9 @@
 // memory.  The split-KV path needs scratch for per-split partial results; instead of
 // the library's cudaMalloc'd workspace, this entry point uses one fixed array that is
 // part of the library's device image, so every device that loads the library holds it
-// (PA_NOALLOC_SCRATCH_BYTES) until the process exits.
+// (PA_NOALLOC_SCRATCH_BYTES) until the process exits.  It creates no stream or event
+// either: a batch with prefill-class sequences runs its prefill kernel and its split-KV
+// pass one after the other on the caller's stream.
 #include <cstdio>
 #include <mutex>
 
@@ -72,5 +74,5 @@ extern "C" int pa_varlen_fwd_noalloc(const pa_tensor* q, const pa_tensor* k_cach
     return pa::forward_impl(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, max_seqlen_q,
                             max_seqlen_k, num_heads, num_heads_k, head_dim, page_block_size, softmax_scale,
                             window_left, window_right, nullptr, out, softmax_lse, stream, pa::static_scratch,
-                            nullptr);
+                            nullptr, false);
 }

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "pa_varlen.h"
@@ -129,8 +130,20 @@ void timer_end(int cls, cudaStream_t stream);
 // device memory usable on `stream`, or returns a status with a message in msg.
 using ScratchFn = int (*)(void* ctx, cudaStream_t stream, size_t bytes, void** ptr, char* msg, size_t msg_len);
 
-// Validation and dispatch shared by the C entry points (api.cpp).
-int launch_forward(Args& a, void* stream, ScratchFn scratch, void* scratch_ctx);
+// NVTX range around a scope (a call, a launch), visible to profilers that record NVTX;
+// costs a function-pointer check when no tool is attached.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
+// Validation and dispatch shared by the C entry points (api.cpp).  `side_stream_ok`: a
+// batch with prefill-class sequences may fork its prefill kernel onto a side stream of the
+// caller's stream (created on first use); when false, both kernels run on `stream`, one
+// after the other, and nothing is created.
+int launch_forward(Args& a, void* stream, ScratchFn scratch, void* scratch_ctx, bool side_stream_ok);
 int launch_uniform_cu(int32_t* cu_q, int32_t* cu_k, int batch, int sq, int sk, cudaStream_t stream, char* msg,
                       size_t msg_len);
 int forward_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
@@ -138,7 +151,8 @@ int forward_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
                  int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_heads, int32_t num_heads_k,
                  int32_t head_dim, int32_t page_block_size, float softmax_scale, int32_t window_left,
                  int32_t window_right, const pa_tensor* alibi_slopes, const pa_tensor* out,
-                 const pa_tensor* softmax_lse, void* stream, ScratchFn scratch, void* scratch_ctx);
+                 const pa_tensor* softmax_lse, void* stream, ScratchFn scratch, void* scratch_ctx,
+                 bool side_stream_ok);
 
 // Tensor-map encoding through the driver entry point (no libcuda link needed).
 // Rank-4 bf16/f16 map over (d0 fastest .. d3), strides in bytes for dims 1..3.

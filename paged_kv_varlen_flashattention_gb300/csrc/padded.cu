@@ -44,6 +44,7 @@ int launch_longest_first(const int32_t* cu_k, int batch, int* order, cudaStream_
         snprintf(msg, msg_len, "longest-first order: batch %d outside [1, %d]", batch, kMaxOrderBatch);
         return PA_ERR_UNSUPPORTED;
     }
+    NvtxRange nv("pa::longest_first_kernel");
     longest_first_kernel<<<1, kOrderThreads, 0, stream>>>(cu_k, batch, order);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
@@ -57,6 +58,7 @@ int launch_longest_first(const int32_t* cu_k, int batch, int* order, cudaStream_
 int launch_uniform_cu(int32_t* cu_q, int32_t* cu_k, int batch, int sq, int sk, cudaStream_t stream, char* msg,
                       size_t msg_len) {
     const int threads = 256, blocks = (batch + 1 + threads - 1) / threads;
+    NvtxRange nv("pa::uniform_cu_kernel");
     uniform_cu_kernel<<<blocks, threads, 0, stream>>>(cu_q, cu_k, batch, sq, sk);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {

@@ -705,6 +705,7 @@ int run_prefill(const Args& a, const PrefillParams& pp, cudaStream_t stream, cha
         configured = true;
     }
     dim3 grid(pp.pairs, a.Hkv, 1);
+    NvtxRange nv("pa::prefill_kernel");
     timer_begin(PA_KC_PREFILL, stream);
     kern<<<grid, kPrefillThreads, C::SMEM, stream>>>(tq, tk, tv, pp);
     cudaError_t e = cudaGetLastError();

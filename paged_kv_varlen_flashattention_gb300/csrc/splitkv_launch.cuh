@@ -37,6 +37,7 @@ struct SplitShape<512> {
 // before touching the partial results).
 template <typename T, int M, int NT>
 static cudaError_t launch_combine(dim3 grid, const SplitParams& sp, cudaStream_t stream) {
+    NvtxRange nv("pa::combine_kernel");
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(128);
@@ -67,6 +68,7 @@ static int run_splitkv(const CUtensorMap& tk, const CUtensorMap& tv, const Split
         configured = true;
     }
     dim3 grid(plan.max_splits, sp.Hkv * plan.row_tiles, sp.batch);
+    NvtxRange nv("pa::splitkv_kernel");
     timer_begin(PA_KC_SPLITKV, stream);
     kern<<<grid, C::NTHR, C::SMEM, stream>>>(tk, tv, sp);
     cudaError_t e = cudaGetLastError();
@@ -126,6 +128,7 @@ static int run_decode(const CUtensorMap& tk, const CUtensorMap& tv, const SplitP
         if (rc != PA_OK) return rc;
     }
     dim3 grid(plan.max_splits, sp.Hkv, sp.batch);
+    NvtxRange nv("pa::decode_kernel");
     timer_begin(PA_KC_SPLITKV, stream);
     kern<<<grid, kDecodeThreads, C::SMEM, stream>>>(tk, tv, sp);
     cudaError_t e = cudaGetLastError();

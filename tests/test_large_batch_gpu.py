@@ -1,0 +1,72 @@
+"""Decode batches of serving size against the oracle (GPU).
+
+The decode kernel launches sequences longest first.  It ranks batches of up to 160
+sequences inside every CTA, batches of 161 to 1,024 through a separate one-CTA ranking
+pass whose order sits at the start of the call's scratch (the split partial results
+follow it), and keeps the index order above 1,024.  These cases reach each branch on
+both sides of its bounds, with skewed lengths (a few sequences far longer than the rest),
+q_len 1 and 4 mixed in one batch, sequences with fewer keys than queries (rows that attend
+nothing), a few prefill-class sequences in the same batch, and NaN in every cache slot
+no sequence owns.  Sampled rows always include the first and last query of every
+sequence (first and last head); all compared element by element at the stated tolerances.
+
+The block table is the per-sequence map of "flash-attn-varlen paged expects k/v tensors
+of rank 4" (What it means): one shared pool, one row of physical blocks per sequence.
+"""
+import numpy as np
+import pytest
+
+from paged_kv_varlen_flashattention_gb300 import workloads
+from tests import _gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def skewed_layout(batch, seed, *, H=8, Hkv=2, D=128, P=32, long_n=3, long_k=20000, q4_frac=0.3,
+                  prefill_n=0, short_hi=600, dtype="bf16"):
+    """`batch` sequences: sk ~ U[1, short_hi] except `long_n` of about `long_k` keys; q_len 4
+    for a fraction of them (else 1); `prefill_n` of them get 64 queries (prefill class)."""
+    rng = np.random.default_rng(seed)
+    sk = rng.integers(1, short_hi, size=batch, endpoint=True)
+    longs = rng.choice(batch, size=long_n, replace=False)
+    sk[longs] = long_k - rng.integers(0, 100, size=long_n)
+    sq = np.where(rng.random(batch) < q4_frac, 4, 1)
+    if prefill_n:
+        pre = rng.choice(np.setdiff1d(np.arange(batch), longs), size=prefill_n, replace=False)
+        sq[pre] = 64
+        sk[pre] = np.maximum(sk[pre], 64 + rng.integers(0, 300, size=prefill_n))
+    return workloads.make_layout(f"skewed_{batch}", dtype, sq.tolist(), sk.tolist(), num_heads=H, num_heads_k=Hkv,
+                                 head_dim=D, page_block_size=P, seed=seed, spare=0.05)
+
+
+@pytest.mark.parametrize("batch", [160, 161])
+def test_in_cta_ranking_bound(batch):
+    """160 sequences: ranked inside every CTA; 161: the first batch ranked by the separate pass."""
+    _gpu.check_layout(skewed_layout(batch, seed=31), limit=2048)
+
+
+def test_ranking_pass_group_of_eight_with_prefill_rows():
+    """300 sequences, G = 8 (q_len 4 -> 32 rows), a few prefill-class sequences beside them."""
+    _gpu.check_layout(skewed_layout(300, seed=32, H=16, Hkv=2, prefill_n=3), limit=2048)
+
+
+def test_ranking_pass_upper_bound_head_dim_64():
+    """1,024 sequences, the largest batch the ranking pass orders."""
+    _gpu.check_layout(skewed_layout(1024, seed=33, D=64, long_n=5), limit=4096)
+
+
+def test_index_order_above_1024_head_dim_256():
+    """1,500 sequences: launched in index order (no ranking)."""
+    _gpu.check_layout(skewed_layout(1500, seed=34, D=256, P=64, long_n=4, long_k=12000, short_hi=300),
+                      limit=6000)
+
+
+@pytest.mark.parametrize("tiles", ["1", "3"])
+def test_ranking_pass_with_forced_splits(tiles, monkeypatch):
+    """The order and the split partials share the scratch: order first, partials after it."""
+    monkeypatch.setenv("PA_SPLIT_TILES", tiles)
+    _gpu.check_layout(skewed_layout(400, seed=35, long_k=3000), limit=2048)
+
+
+def test_fp16_large_batch():
+    _gpu.check_layout(skewed_layout(200, seed=36, dtype="f16"), limit=2048)

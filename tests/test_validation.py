@@ -142,6 +142,19 @@ def test_implementation_limits():
     assert run_check(ds, H, Hkv, D, P)[0] == CODES["PA_ERR_UNSUPPORTED"]
 
 
+def test_grid_limit_of_long_rows():
+    """Long query rows the tensor-core prefill kernel does not take (head_dim 512 here) are
+    split-KV row tiles of 32 rows: num_heads_k x tiles must fit the 65,535 CTAs of grid.y."""
+    shp = {"q": [8, 4, 512], "k": [6, 32, 2, 512], "v": [6, 32, 2, 512], "out": [8, 4, 512]}
+    ds, H, Hkv, D, P = build(shp)
+    rc, msg = run_check(ds, H, Hkv, D, P, max_sq=300000)  # 600,000 rows -> 18,750 tiles x 2 kv heads
+    assert rc == 0, msg
+    rc, msg = run_check(ds, H, Hkv, D, P, max_sq=600000)  # 37,500 tiles x 2 kv heads > 65,535
+    assert rc == CODES["PA_ERR_UNSUPPORTED"] and "65535" in msg, msg
+    ds, H, Hkv, D, P = _base()  # head_dim 64, G = 2: the tensor-core prefill takes the long rows
+    assert run_check(ds, H, Hkv, D, P, max_sq=600000)[0] == 0
+
+
 def test_non_finite_scale():
     ds, H, Hkv, D, P = _base()
     assert run_check(ds, H, Hkv, D, P, scale=float("nan"))[0] == CODES["PA_ERR_ARG"]
