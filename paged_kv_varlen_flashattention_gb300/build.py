@@ -14,8 +14,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpa_varlen.so")
 
-SOURCES = ["api.cpp", "errword.cu", "splitkv_bf16.cu", "splitkv_f16.cu", "prefill_tc.cu", "noalloc.cu", "kv_append.cu",
-           "padded.cu"]
+SOURCES = ["api.cpp", "errword.cu", "splitkv_bf16.cu", "splitkv_f16.cu", "prefill_tc.cu", "decode_tc.cu", "noalloc.cu",
+           "kv_append.cu", "padded.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

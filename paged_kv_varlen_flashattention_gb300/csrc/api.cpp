@@ -591,6 +591,14 @@ int encode_tmap_4d(void* map, int dtype, const void* base, const uint64_t dims_[
     return PA_OK;
 }
 
+bool decode_tc_wanted(int dp) {
+    // Opt-in (PA_DECODE_TC=1, read per call): on GB300 it measured below the warp-sliced
+    // kernel at head dims 128 and 256 (0.50 / 0.73 of the copy peak against 0.93 / 0.91) and
+    // level with the general kernel at 512 (0.30 against 0.31).
+    const char* env = std::getenv("PA_DECODE_TC");
+    return dp >= 128 && env && env[0] == '1';
+}
+
 SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, int num_sms) {
     SplitPlan pl{};
     pl.dp = a.D <= 64 ? 64 : a.D <= 128 ? 128 : a.D <= 256 ? 256 : 512;
@@ -603,6 +611,9 @@ SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, int num_sms)
     const int M = 16 * pl.mt;
     pl.row_tiles = (int)((rows_here + M - 1) / M);
     pl.tile_rows = (int)std::min<int64_t>(M, rows_here);
+    static const bool force_generic = std::getenv("PA_FORCE_GENERIC") != nullptr;
+    pl.tc = pl.row_tiles == 1 && !force_generic && decode_tc_wanted(pl.dp);
+    if (pl.tc) pl.nt = 128;
     // keys one row tile can touch: its queries span at most M / G + 1 positions
     int64_t kspan = a.max_sk;
     if (a.wl >= 0) kspan = std::min<int64_t>(kspan, (int64_t)a.wl + M / G + 1 + std::max(a.wr, 0) + 1);
@@ -621,7 +632,8 @@ SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, int num_sms)
         // 4 tiles, nor than 8 M keys: its fp32 partial result (M rows x D x 4 bytes, written
         // and read back) then costs at most ~1/8 of the K/V bytes it reads.
         const int64_t slots =
-            (int64_t)num_sms * (a.dtype == PA_BF16 ? splitkv_occupancy_bf16(pl) : splitkv_occupancy_f16(pl));
+            (int64_t)num_sms * (pl.tc ? decode_tc_occupancy(a.dtype, pl.dp, M)
+                                : a.dtype == PA_BF16 ? splitkv_occupancy_bf16(pl) : splitkv_occupancy_f16(pl));
         int64_t splits = units < slots ? slots / units : 1;
         splits = std::max<int64_t>(1, std::min(splits, tiles_max));
         const int64_t min_tiles = std::max<int64_t>(4, (8ll * M + pl.nt - 1) / pl.nt);
@@ -634,10 +646,9 @@ SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, int num_sms)
         pl.split_tiles = (int)((tiles_max + 1023) / 1024);
         pl.max_splits = (int)((tiles_max + pl.split_tiles - 1) / pl.split_tiles);
     }
-    // the decode kernel launches sequences longest first (a one-CTA ranking pass) for
-    // batches it can rank; the order sits at the start of the scratch
-    static const bool force_generic = std::getenv("PA_FORCE_GENERIC") != nullptr;
-    const bool decode_kernel = pl.row_tiles == 1 && pl.dp <= 256 && !force_generic;
+    // the decode kernels launch sequences longest first (a one-CTA ranking pass) for
+    // batches they can rank; the order sits at the start of the scratch
+    const bool decode_kernel = pl.tc || (pl.row_tiles == 1 && pl.dp <= 256 && !force_generic);
     pl.rank_in_cta = decode_kernel && a.batch >= 2 && a.batch <= kRankInCta;
     pl.order_bytes = decode_kernel && a.batch > kRankInCta && a.batch <= kMaxOrderBatch
                          ? ((size_t)a.batch * sizeof(int) + 255) / 256 * 256

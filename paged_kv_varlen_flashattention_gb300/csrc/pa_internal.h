@@ -67,6 +67,7 @@ struct SplitPlan {
     size_t ws_bytes;     // scratch needed: the longest-first order, then the partial results
     size_t order_bytes;  // bytes of the order at the start of the scratch (0: none)
     int rank_in_cta;     // decode kernel CTAs rank the batch themselves (small batches)
+    int tc;              // decode class on the tensor-core decode kernel (128-key tiles)
 };
 
 // The decode kernel launches sequences longest first: batches of at most kRankInCta
@@ -89,6 +90,12 @@ int launch_splitkv_bf16(const Args& a, const SplitPlan& plan, void* workspace, u
 // Resident CTAs per SM of the split-KV kernel `plan` dispatches to (dp, mt, row_tiles set).
 int splitkv_occupancy_bf16(const SplitPlan& plan);
 int splitkv_occupancy_f16(const SplitPlan& plan);
+// Resident CTAs per SM of the tensor-core decode kernel (padded head dim dp, nr rows).
+int decode_tc_occupancy(int dtype, int dp, int nr);
+// Whether decode-class rows (one row tile of at most 32 rows) of padded head dim `dp` >= 128
+// go to the tensor-core decode kernel: when the PA_DECODE_TC environment variable is 1 (a
+// switch between two complete kernels; off by default, where the other kernels measured faster).
+bool decode_tc_wanted(int dp);
 int launch_splitkv_f16(const Args& a, const SplitPlan& plan, void* workspace, unsigned int* err, char* msg,
                        size_t msg_len);
 

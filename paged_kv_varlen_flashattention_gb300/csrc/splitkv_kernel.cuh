@@ -469,6 +469,10 @@ __global__ void __launch_bounds__(NW * 32) splitkv_kernel(const __grid_constant_
     }
 }
 
+// Launch of the tensor-core decode kernel (decode_tc.cu) for a plan with plan.tc set.
+int launch_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& sp, const SplitPlan& plan,
+                     int dtype, cudaStream_t stream, char* msg, size_t msg_len);
+
 // lse = ln sum_s exp(lse_s); out = sum_s exp(lse_s - lse) * O_s, for the tiles that
 // were split.  Grid: (row groups of 4, kv head x row tile, sequence); one warp per output
 // row: the split weights are computed once per row into shared memory, then each lane

@@ -206,11 +206,12 @@ static int splitkv_occupancy_t(const SplitPlan& plan) {
 template <typename T>
 static int launch_splitkv_t(const Args& a, const SplitPlan& plan, void* workspace, unsigned int* err, char* msg,
                             size_t msg_len) {
-    const int NT = plan.dp == 512 ? 32 : 64;
-    // Box rows: the largest of {NT, 32} that divides the page, so that a box never
+    const int NT = plan.nt;
+    // Box rows: the largest of {NT, 64, 32} that divides the page, so that a box never
     // straddles two pages (page sizes are multiples of 32).
     int box_rows = NT;
-    if (a.paged && (a.page % NT) != 0) box_rows = 32;
+    if (a.paged)
+        box_rows = (a.page % NT) == 0 ? NT : (NT > 64 && a.page % 64 == 0) ? 64 : 32;
     CUtensorMap tk, tv;
     uint64_t dims[4];
     uint64_t strides[3];
@@ -284,6 +285,25 @@ static int launch_splitkv_t(const Args& a, const SplitPlan& plan, void* workspac
     sp.wait_ns = a.wait_ns;
     sp.withhold = a.withhold_loads;
 
+    if (plan.tc) {  // decode class on the tensor cores
+        if (plan.max_splits > 1) {
+            const int rc = launch_decode_tc(tk, tv, sp, plan, a.dtype, a.stream, msg, msg_len);
+            if (rc != PA_OK) return rc;
+            const int M = 16 * plan.mt;
+            dim3 g2(((plan.tile_rows + kCombineRows - 1) / kCombineRows) * ((sp.D + 63) / 64), sp.Hkv, sp.batch);
+            timer_begin(PA_KC_COMBINE, a.stream);
+            const cudaError_t e = M == 16 ? launch_combine<T, 16, 128>(g2, sp, a.stream)
+                                          : launch_combine<T, 32, 128>(g2, sp, a.stream);
+            if (e != cudaSuccess) {
+                snprintf(msg, msg_len, "decode_tc combine launch: %s", cudaGetErrorString(e));
+                return PA_ERR_CUDA;
+            }
+            timer_end(PA_KC_COMBINE, a.stream);
+            count_launches(1);
+            return PA_OK;
+        }
+        return launch_decode_tc(tk, tv, sp, plan, a.dtype, a.stream, msg, msg_len);
+    }
     // decode class (one row tile of at most 32 rows, head dim <= 256): warp-sliced kernel
     static const bool force_generic = std::getenv("PA_FORCE_GENERIC") != nullptr;
     if (plan.row_tiles == 1 && plan.dp <= 256 && !force_generic) {
