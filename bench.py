@@ -41,8 +41,9 @@ NOMINAL_HBM_GBS = 7900.0
 NOMINAL_BF16_TFLOPS = 2250.0
 L2_BYTES = 129 * 1024 * 1024
 # the serving workloads measured beside the headline (chunked prefill + decode with a window,
-# long-context split-KV decode at head_dim 256 and 512)
-EXTRA_WORKLOADS = ("mixed_bf16", "long_bf16", "long_d512_bf16")
+# long-context split-KV decode at head_dim 256 and 512, and the decode batch with one sequence
+# far longer than the rest)
+EXTRA_WORKLOADS = ("mixed_bf16", "long_bf16", "long_d512_bf16", "skewed_decode_bf16")
 
 
 # ---- algorithmic work (closed form per query row) -----------------------------------------
@@ -170,9 +171,9 @@ def replica_throughput(work_per_rank, world, ms_max):
 def kernel_class_seqs(lay):
     """Sequences per kernel class, mirroring the library's dispatch: sequences with more
     than 32 rows (sq * G) go to the tensor-core prefill kernel when it takes the call
-    (head_dim <= 128, G divides 128, softmax_scale > 0), the rest to the split-KV pass."""
+    (head_dim <= 128, G <= 128, softmax_scale > 0), the rest to the split-KV pass."""
     G = lay.num_heads // lay.num_heads_k
-    tc = (lay.head_dim <= 128 and 128 % G == 0 and lay.softmax_scale > 0
+    tc = (lay.head_dim <= 128 and G <= 128 and lay.softmax_scale > 0
           and max(lay.seqlens_q) * G > 32 and not os.environ.get("PA_DISABLE_TC_PREFILL"))
     pre = [b for b in range(lay.batch) if tc and lay.seqlens_q[b] * G > 32]
     split = [b for b in range(lay.batch) if b not in set(pre)]

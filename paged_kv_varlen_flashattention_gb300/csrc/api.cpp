@@ -638,6 +638,12 @@ SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, int num_sms)
         splits = std::max<int64_t>(1, std::min(splits, tiles_max));
         const int64_t min_tiles = std::max<int64_t>(4, (8ll * M + pl.nt - 1) / pl.nt);
         split_tiles = std::max<int64_t>(min_tiles, (tiles_max + splits - 1) / splits);
+        // Nor does a split hold more than kMaxSplitKeys keys.  The host does not read the
+        // lengths, so a batch where one sequence is far longer than the rest (a 131,072-key
+        // sequence among 4,096-key ones) would otherwise leave that sequence's one CTA per kv
+        // head as the tail of the grid; with the cap its keys spread over many CTAs, while
+        // sequences below the cap keep one CTA (their further split indices exit at once).
+        split_tiles = std::min(split_tiles, std::max(min_tiles, kMaxSplitKeys / pl.nt));
     }
     split_tiles = std::min(split_tiles, tiles_max);
     pl.split_tiles = (int)split_tiles;

@@ -74,6 +74,8 @@ struct SplitPlan {
 // sequences are ranked inside every CTA, larger ones up to kMaxOrderBatch by a one-CTA pass.
 constexpr int kRankInCta = 160;
 constexpr int kMaxOrderBatch = 1024;
+// Most keys one split-KV CTA of the decode class takes (the plan's cap for skewed batches).
+constexpr int64_t kMaxSplitKeys = 8192;
 int launch_longest_first(const int32_t* cu_k, int batch, int* order, cudaStream_t stream, char* msg,
                          size_t msg_len);
 

@@ -2,7 +2,9 @@
 //
 // One CTA owns two 128-row query tiles (A and B, consecutive) of one (sequence, kv head);
 // a tile's rows are the (query i, head g) pairs of the kv head's GQA group, ordered
-// i * G + g, so each K/V tile feeds all G query heads and both query tiles.
+// i * G + g, so each K/V tile feeds all G query heads and both query tiles.  A tile holds
+// floor(128 / G) whole queries; when G does not divide 128 its last 128 mod G rows are
+// padding (masked, never written).
 // Roles (384 threads, three warpgroups):
 //   warps 0, 2  TMA producers (warp 0: both q tiles once, then K tiles; warp 2: V tiles),
 //               128 keys per tile through the block table (one box per page piece; the
@@ -188,14 +190,16 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     // sequence's last pair (the longest under a causal mask) first.  Warp 0 scans
     // cu_seqlens_q 32 sequences at a time with a prefix sum of pair counts.
     int* pick = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
+    const int qpt = 128 / p.G;     // whole queries per 128-row tile
+    const int trows = qpt * p.G;   // rows of a tile that hold queries (the rest are padding)
     if (warp == 0) {
         int remaining = (int)blockIdx.x, found_b = -1, found_u = 0;
         for (int base = 0; base < p.batch && found_b < 0; base += 32) {
             const int bb = base + lane;
             int pairs = 0;
             if (bb < p.batch) {
-                const int64_t rows = (int64_t)(p.cu_q[bb + 1] - p.cu_q[bb]) * p.G;
-                pairs = rows > p.rows_cap ? (int)((rows + 255) / 256) : 0;
+                const int sqb = p.cu_q[bb + 1] - p.cu_q[bb];
+                pairs = (int64_t)sqb * p.G > p.rows_cap ? (sqb + 2 * qpt - 1) / (2 * qpt) : 0;
             }
             int incl = pairs;
 #pragma unroll
@@ -244,10 +248,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         return;
     }
     const int64_t rows_total = (int64_t)sq * p.G;
-    const int row0 = u * 256;                             // first row of tile A
-    const bool has_b = (int64_t)row0 + 128 < rows_total;  // tile B holds at least one row
-    const int qpt = 128 / p.G;                            // queries per tile
-    const int i0 = row0 / p.G;
+    const int i0 = u * 2 * qpt;         // first query of tile A
+    const bool has_b = i0 + qpt < sq;   // tile B holds at least one query
+    // row (i * G + g) of row r of tile x, and whether that row holds a query of the sequence
+    auto tile_rho = [&](int x, int r) -> int64_t { return (int64_t)(i0 + x * qpt) * p.G + r; };
+    auto row_live = [&](int x, int r) { return r < trows && tile_rho(x, r) < rows_total; };
     const int i_last = min(sq - 1, i0 + (has_b ? 2 : 1) * qpt - 1);
     const int64_t cdiag = (int64_t)sk - sq;
     const int64_t lo = p.wl >= 0 ? max64(0, i0 + cdiag - p.wl) : 0;
@@ -258,9 +263,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     T* out = static_cast<T*>(p.out);
     if (n_tiles == 0) {  // no row of the pair attends any key: out = 0, lse = -inf
         if (warp >= 4) {
-            const int r = ((warp - 4) >> 2) * 128 + (warp & 3) * 32 + lane;
-            const int64_t rho = row0 + r;
-            if (rho < rows_total) {
+            const int x = (warp - 4) >> 2, r = (warp & 3) * 32 + lane;
+            const int64_t rho = tile_rho(x, r);
+            if (row_live(x, r)) {
                 const int i = (int)(rho / p.G), g = (int)(rho - (int64_t)i * p.G);
                 const int64_t t = q0 + i;
                 const int h = hk * p.G + g;
@@ -284,7 +289,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         if (warp == 0) {
             if (lane == 0 && !p.withhold) {  // the q tiles first: their latency overlaps the id lookups
                 prefetch_tmap(&tm_q);
-                mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::Q_TILE);
+                mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::CH * trows * 128);
                 for (int x = 0; x < (has_b ? 2 : 1); ++x)
                     for (int c = 0; c < C::CH; ++c)
                         tma_load_4d(smem + C::OFF_Q + x * C::Q_TILE + c * 128 * 128, &tm_q, q_full, c * 64,
@@ -434,12 +439,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         auto init_rows = [&](int x, TileRows& st) {
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
-                const int64_t rho = row0 + x * 128 + lb + gid + 8 * q;
+                const int64_t rho = tile_rho(x, lb + gid + 8 * q);
                 st.lo[q] = 0;
                 st.hi[q] = -1;
                 st.dg[q] = 0;
                 st.ab[q] = 0.f;
-                if (rho < rows_total) {
+                if (row_live(x, lb + gid + 8 * q)) {
                     const int64_t diag = rho / p.G + cdiag;
                     st.lo[q] = p.wl >= 0 ? (int)max64(0, diag - p.wl) : 0;
                     st.hi[q] = p.wr >= 0 ? (int)max64(-1, min64((int64_t)sk - 1, diag + p.wr)) : sk - 1;
@@ -611,8 +616,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 l += __shfl_xor_sync(0xffffffffu, l, 1);
                 l += __shfl_xor_sync(0xffffffffu, l, 2);
                 inv[q] = l > 0.f ? 1.f / l : 0.f;
-                const int64_t rho = row0 + x * 128 + lb + gid + 8 * q;
-                valid[q] = rho < rows_total;
+                const int64_t rho = tile_rho(x, lb + gid + 8 * q);
+                valid[q] = row_live(x, lb + gid + 8 * q);
                 const int i = (int)(rho / p.G), g = (int)(rho - (int64_t)i * p.G);
                 const int64_t t = q0 + i;
                 const int h = hk * p.G + g;
@@ -726,7 +731,7 @@ bool prefill_supported(const Args& a) {
     static const bool disabled = std::getenv("PA_DISABLE_TC_PREFILL") != nullptr;
     if (disabled) return false;
     const int G = a.H / a.Hkv;
-    if (a.D > 128 || 128 % G != 0) return false;
+    if (a.D > 128 || G > 128) return false;
     if (!(a.scale > 0.f)) return false;
     if ((int64_t)a.max_sq * G <= prefill_rows_threshold()) return false;  // nothing for it to do
     if (a.total_q <= 0 || a.q_s1 * 2 % 16 != 0 || a.q_s0 * 2 % 16 != 0) return false;
@@ -768,9 +773,11 @@ int launch_prefill(const Args& a, unsigned int* err, char* msg, size_t msg_len) 
     pp.wl = a.wl;
     pp.wr = a.wr;
     pp.rows_cap = prefill_rows_threshold();
-    // upper bound of the number of 256-row pairs: sum_b ceil(sq_b G / 256) <= ceil(total_q G / 256) + batch
-    pp.pairs = (int)std::min<int64_t>(((int64_t)a.total_q * pp.G + 255) / 256 + a.batch,
-                                      (int64_t)a.batch * (((int64_t)a.max_sq * pp.G + 255) / 256));
+    // upper bound of the number of tile pairs (2 qpt queries each, qpt = floor(128 / G)):
+    // sum_b ceil(sq_b / (2 qpt)) <= ceil(total_q / (2 qpt)) + batch
+    const int64_t pq = 2 * (128 / pp.G);
+    pp.pairs = (int)std::min<int64_t>(((int64_t)a.total_q + pq - 1) / pq + a.batch,
+                                      (int64_t)a.batch * (((int64_t)a.max_sq + pq - 1) / pq));
     pp.err = err;
     pp.wait_ns = a.wait_ns;
     pp.withhold = a.withhold_loads;

@@ -164,6 +164,17 @@ def long_d512_bf16(seed=6) -> Layout:
                        std=0.5)
 
 
+def skewed_decode_bf16(batch=64, lo=512, hi=4096, long_k=131072, seed=7) -> Layout:
+    """The decode batch with one sequence far longer than the rest: 63 sequences with
+    sk ~ U[512, 4096] and one (at a seeded position) with 131,072 keys; H=32, Hkv=8, D=128,
+    P=32, q_len 1, pool +10 %."""
+    rng = np.random.default_rng(seed)
+    sk = rng.integers(lo, hi, size=batch, endpoint=True)
+    sk[int(rng.integers(0, batch))] = long_k
+    return make_layout("skewed_decode_bf16", "bf16", [1] * batch, sk, num_heads=32, num_heads_k=8,
+                       head_dim=128, page_block_size=32, seed=seed, spare=0.1)
+
+
 CONFIGS = {
     "tiny_fp16": tiny_fp16,
     "decode_bf16": decode_bf16,
@@ -171,6 +182,7 @@ CONFIGS = {
     "mixed_bf16": mixed_bf16,
     "long_bf16": long_bf16,
     "long_d512_bf16": long_d512_bf16,
+    "skewed_decode_bf16": skewed_decode_bf16,
 }
 
 

@@ -70,3 +70,23 @@ def test_ranking_pass_with_forced_splits(tiles, monkeypatch):
 
 def test_fp16_large_batch():
     _gpu.check_layout(skewed_layout(200, seed=36, dtype="f16"), limit=2048)
+
+
+def test_skewed_batch_one_very_long_sequence():
+    """The skewed decode workload at full size (63 sequences of 512..4,096 keys and one of
+    131,072): the long sequence's keys are split over many CTAs (at most 8,192 keys each) and
+    merged by the combine, the short ones stay whole.  All heads of the long sequence's query
+    and sampled rows of the others."""
+    import torch
+
+    lay = workloads.CONFIGS["skewed_decode_bf16"]()
+    long_b = int(np.argmax(lay.seqlens_k))
+    inp = workloads.materialize(lay, device="cuda")
+    out, lse = _gpu.run_cuda(inp)
+    cq, _ = lay.cu_seqlens()
+    t = int(cq[long_b])  # the long sequence's one query token
+    long_rows = np.arange(t * lay.num_heads, (t + 1) * lay.num_heads, dtype=np.int64)
+    rows = np.unique(np.concatenate([_gpu.sample_rows(lay, 512), long_rows]))
+    ref_o, ref_l = _gpu.oracle_for(inp.to("cpu"), rows)
+    _gpu.compare(lay, out, lse, ref_o, ref_l, rows)
+    torch.cuda.synchronize()

@@ -146,8 +146,25 @@ def test_prefill_fp16():
 
 @pytest.mark.parametrize("H,Hkv", [(6, 2), (12, 1), (8, 8)])
 def test_group_sizes(H, Hkv):
-    """G = 3 and 12 do not divide the 128-row tensor-core tile (general path); G = 1 does."""
+    """G = 3 and 12 do not divide the 128-row tensor-core tile (42 and 10 whole queries a
+    tile, 2 and 8 padding rows); G = 1 does."""
     _gpu.check_layout(_custom([70, 1, 150], [70, 300, 200], H=H, Hkv=Hkv, D=64))
+
+
+@pytest.mark.parametrize("G", [3, 5, 6, 7, 12, 24])
+@pytest.mark.parametrize("D", [64, 128])
+def test_prefill_group_sizes_not_dividing_the_tile(G, D):
+    """Long query rows on the tensor-core prefill kernel with G not dividing 128: several
+    tile pairs per sequence, a ragged last pair, chunked prefill (sk > sq) and a window."""
+    lay = _custom([300, 77, 1, 129], [300, 500, 40, 200], H=2 * G, Hkv=2, D=D, seed=70 + G)
+    _gpu.check_layout(lay, limit=4096)
+    lay = _custom([260, 33], [900, 33], H=G, Hkv=1, D=D, wl=100, wr=0, seed=80 + G, dtype="f16")
+    _gpu.check_layout(lay, limit=4096)
+
+
+def test_prefill_group_not_dividing_with_bias():
+    lay = _custom([200, 90], [500, 90], H=6, Hkv=2, D=128, seed=91)
+    _gpu.check_layout(lay, alibi=_gpu.alibi_slopes(6), limit=4096)
 
 
 def test_long_prefill_spans_many_tiles_and_pages():
