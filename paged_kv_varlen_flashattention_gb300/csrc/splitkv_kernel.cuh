@@ -106,14 +106,16 @@ __device__ __forceinline__ bool tile_view(const SplitParams& p, int b, int rt, T
     return true;
 }
 
-// NW warps: 4, or 8 for the widest heads, where two warps share each key slice of
-// Q.K^T (one half of the head dim each, partial scores summed by the softmax) and each
-// warp owns DP / 8 output columns of P.V -- two warps per scheduler hide the latency of
-// the long MMA chains.
+// NW warps: 4, each taking a quarter of the tile's keys in Q.K^T over the whole head dim;
+// or 8 for the widest heads, each taking every key of the tile over one eighth of the head
+// dim (4 k-steps: eight independent accumulator chains of 4 MMAs instead of two chains of
+// 16, measured latency-bound), the softmax summing the 8 partial scores.  In P.V each warp
+// owns DP / NW output columns.
 template <int DP, int MT, int NT, int STAGES, int NW = 4>
 struct SplitCfg {
     static constexpr int NTHR = NW * 32;
-    static constexpr int KSPLIT = NW / 4;           // head-dim parts of Q.K^T
+    static constexpr int KSLICES = NW == 8 ? 1 : 4;  // key slices of Q.K^T
+    static constexpr int KSPLIT = NW / KSLICES;      // head-dim parts of Q.K^T
     static constexpr int M = 16 * MT;               // query rows per CTA
     static constexpr int CH = DP / 64;              // 64-element (128-byte) column chunks of a row
     static constexpr int TILE_BYTES = CH * NT * 128;  // one K (or V) tile of NT keys
@@ -129,7 +131,7 @@ struct SplitCfg {
     static constexpr int OFF_ROW = OFF_S + S_BYTES;
     static constexpr int OFF_BAR = (OFF_ROW + 7 * M * 4 + 15) & ~15;
     static constexpr int SMEM = OFF_BAR + STAGES * 8 + 1024;  // + slack for 1024-byte alignment
-    static constexpr int KW = NT / 4;               // keys per warp in Q.K^T
+    static constexpr int KW = NT / KSLICES;         // keys per warp in Q.K^T
     static constexpr int DW = DP / NW;              // output columns per warp in P.V
     static_assert(NW == 4 || NW == 8, "warps");
     static_assert(NT == 64 || NT == 32, "tile width");
@@ -294,7 +296,7 @@ __global__ void __launch_bounds__(NW * 32) splitkv_kernel(const __grid_constant_
         }
 
         // S = Q K^T for keys [ws*KW, ws*KW + KW) of the tile, over head-dim part kp
-        const int ws = warp & 3, kp = warp >> 2;
+        const int ws = warp % C::KSLICES, kp = warp / C::KSLICES;
         float s_acc[MT][C::KW / 8][4];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
@@ -308,9 +310,13 @@ __global__ void __launch_bounds__(NW * 32) splitkv_kernel(const __grid_constant_
             const int ks = kp * (DP / 16 / C::KSPLIT) + kq;
             const int c = ks >> 2, u0 = (ks & 3) * 2;
             uint32_t bf[C::KW / 8][2];
-            if constexpr (C::KW == 16) {
-                const int key = ws * 16 + rr + ((mi >> 1) << 3);
-                ldsm_x4(k_base + c * NT * 128 + swz128(key, u0 + (mi & 1)), bf[0][0], bf[0][1], bf[1][0], bf[1][1]);
+            if constexpr (C::KW >= 16) {
+#pragma unroll
+                for (int np = 0; np < C::KW / 16; ++np) {
+                    const int key = ws * C::KW + np * 16 + rr + ((mi >> 1) << 3);
+                    ldsm_x4(k_base + c * NT * 128 + swz128(key, u0 + (mi & 1)), bf[2 * np][0], bf[2 * np][1],
+                            bf[2 * np + 1][0], bf[2 * np + 1][1]);
+                }
             } else {
                 const int key = ws * 8 + rr;
                 ldsm_x2(k_base + c * NT * 128 + swz128(key, u0 + (mi & 1)), bf[0][0], bf[0][1]);
@@ -356,7 +362,8 @@ __global__ void __launch_bounds__(NW * 32) splitkv_kernel(const __grid_constant_
             const float ab = row_ab[r];
             auto score = [&](int col) {
                 float sv = S[r * C::S_STRIDE + col];
-                if (C::KSPLIT == 2) sv += S[(M + r) * C::S_STRIDE + col];
+#pragma unroll
+                for (int kp2 = 1; kp2 < C::KSPLIT; ++kp2) sv += S[(kp2 * M + r) * C::S_STRIDE + col];
                 const int j = kt + col;
                 return (j >= lo && j <= hi) ? biased_log2(sv, p.scale_log2, ab, dg, j) : -INFINITY;
             };
