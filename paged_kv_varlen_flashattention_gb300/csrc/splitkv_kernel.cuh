@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(NW * 32) splitkv_kernel(const __grid_constant_
     if (tid == 0) {
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
-        for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
+        for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], NW);  // one arrival per warp
         fence_mbar_init();
     }
     // Q rows of the tile -> shared memory (128-byte swizzled rows, zero padded).
@@ -211,7 +211,10 @@ __global__ void __launch_bounds__(NW * 32) splitkv_kernel(const __grid_constant_
     __syncthreads();
 
     const uint64_t policy = l2_policy_evict_first();
-    // Producer (thread 0): pull K/V boxes of key tile `it` of this split into its stage.
+    // Producers (lane 0 of every warp): pull the K/V boxes of key tile `it` of this split into
+    // its stage, warp w taking the 64-column chunks c = w, w + NW, ...  One thread issuing all
+    // of a stage's copies (16 at head_dim 512) held its warp, and with it the next barrier,
+    // for thousands of cycles; each warp posts the bytes of its own copies before issuing them.
     auto issue = [&](int it) {
         const int stage = it % STAGES;
         const int kt = tv.kt0 + (t_begin + it) * NT;
@@ -241,19 +244,19 @@ __global__ void __launch_bounds__(NW * 32) splitkv_kernel(const __grid_constant_
                 cb[j] = 0;
             }
             live[j] = true;
-            bytes += 2u * C::CH * p.box_rows * 128u;
+            bytes += 2u * ((C::CH - warp + NW - 1) / NW) * p.box_rows * 128u;
         }
         mbar_arrive_expect_tx(&full[stage], bytes);
         for (int j = 0; j < p.boxes_per_tile; ++j) {
             if (!live[j]) continue;
-            for (int c = 0; c < C::CH; ++c) {
+            for (int c = warp; c < C::CH; c += NW) {
                 const int off = (c * NT + j * p.box_rows) * 128;
                 tma_load_4d(kst + off, &tm_k, &full[stage], c * 64, hk, cs[j], cb[j], policy);
                 tma_load_4d(vst + off, &tm_v, &full[stage], c * 64, hk, cs[j], cb[j], policy);
             }
         }
     };
-    if (tid == 0 && !p.withhold) {
+    if (lane == 0 && !p.withhold) {
         for (int it = 0; it < min(STAGES - 1, n_iter); ++it) issue(it);
     }
 
@@ -348,7 +351,7 @@ __global__ void __launch_bounds__(NW * 32) splitkv_kernel(const __grid_constant_
             return;
         }
         // the stage used by the previous iteration is free: refill it
-        if (tid == 0 && it + STAGES - 1 < n_iter && !p.withhold) {
+        if (lane == 0 && it + STAGES - 1 < n_iter && !p.withhold) {
             fence_proxy_async_smem();
             issue(it + STAGES - 1);
         }
