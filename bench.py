@@ -443,13 +443,15 @@ def cpu_baseline(lay, inp_cpu, budget_s=20.0):
 def kernel_names(lay):
     """Kernel class -> kernel name for a workload, mirroring the library's choice for the
     split-KV class: rows of at most 32 (q_len x group) go to the warp-sliced decode kernel for
-    head_dim up to 256 (to the tensor-core decode kernel under PA_DECODE_TC=1); longer rows the
-    prefill kernel does not take, and head_dim above 256, go to the general kernel."""
+    head_dim up to 256 and to the quarter-column decode kernel above (to the tensor-core decode
+    kernel under PA_DECODE_TC=1); longer rows the prefill kernel does not take go to the
+    general kernel."""
     G = lay.num_heads // lay.num_heads_k
     rows = max(q for q in lay.seqlens_q) * G if not kernel_class_seqs(lay)["prefill"] else 32
     dp = 64 if lay.head_dim <= 64 else 128 if lay.head_dim <= 128 else 256 if lay.head_dim <= 256 else 512
     tc = dp >= 128 and os.environ.get("PA_DECODE_TC", "") == "1"
-    dec = ("decode_tc_kernel" if tc else "decode_kernel") if rows <= 32 and (tc or dp <= 256) else "splitkv_kernel"
+    dec = ("splitkv_kernel" if rows > 32 else "decode_tc_kernel" if tc else
+           "decode_kernel" if dp <= 256 else "decode512_kernel")
     return {"prefill": "prefill_kernel", "combine": "combine_kernel", "splitkv": dec}
 
 

@@ -654,7 +654,7 @@ SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, int num_sms)
     }
     // the decode kernels launch sequences longest first (a one-CTA ranking pass) for
     // batches they can rank; the order sits at the start of the scratch
-    const bool decode_kernel = pl.tc || (pl.row_tiles == 1 && pl.dp <= 256 && !force_generic);
+    const bool decode_kernel = pl.tc || (pl.row_tiles == 1 && !force_generic);
     pl.rank_in_cta = decode_kernel && a.batch >= 2 && a.batch <= kRankInCta;
     pl.order_bytes = decode_kernel && a.batch > kRankInCta && a.batch <= kMaxOrderBatch
                          ? ((size_t)a.batch * sizeof(int) + 255) / 256 * 256

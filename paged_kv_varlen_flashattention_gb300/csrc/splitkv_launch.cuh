@@ -8,6 +8,7 @@
 #include <cstdlib>
 
 #include "decode_kernel.cuh"
+#include "decode_wide.cuh"
 
 namespace pa {
 
@@ -152,6 +153,58 @@ static int run_decode(const CUtensorMap& tk, const CUtensorMap& tv, const SplitP
     return PA_OK;
 }
 
+// Head dim 257..512, at most 32 rows: the quarter-column decode kernel (32-key tiles, one
+// 32-row box per tile; pages are multiples of 32).
+constexpr int kWideStages = 3;
+
+template <typename T, int MG>
+static int run_decode512(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& sp, const SplitPlan& plan,
+                         cudaStream_t stream, char* msg, size_t msg_len) {
+    using C = WideCfg<MG, kWideStages>;
+    auto kern = decode512_kernel<T, MG, kWideStages>;
+    if (sp.box_rows != C::NT || sp.boxes_per_tile != 1) {
+        snprintf(msg, msg_len, "decode512: box of %d rows, %d a tile (expected one of %d)", sp.box_rows,
+                 sp.boxes_per_tile, C::NT);
+        return PA_ERR_UNSUPPORTED;
+    }
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) {
+            snprintf(msg, msg_len, "cudaFuncSetAttribute(decode512, %d bytes): %s", C::SMEM, cudaGetErrorString(e));
+            return PA_ERR_CUDA;
+        }
+        configured = true;
+    }
+    if (sp.order) {
+        const int rc = launch_longest_first(sp.cu_k, sp.batch, const_cast<int*>(sp.order), stream, msg, msg_len);
+        if (rc != PA_OK) return rc;
+    }
+    dim3 grid(plan.max_splits, sp.Hkv, sp.batch);
+    NvtxRange nv("pa::decode512_kernel");
+    timer_begin(PA_KC_SPLITKV, stream);
+    kern<<<grid, C::THREADS, C::SMEM, stream>>>(tk, tv, sp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        snprintf(msg, msg_len, "decode512 launch: %s", cudaGetErrorString(e));
+        return PA_ERR_CUDA;
+    }
+    timer_end(PA_KC_SPLITKV, stream);
+    count_launches(1);
+    if (plan.max_splits > 1) {
+        dim3 g2(((plan.tile_rows + kCombineRows - 1) / kCombineRows) * ((sp.D + 63) / 64), sp.Hkv, sp.batch);
+        timer_begin(PA_KC_COMBINE, stream);
+        e = launch_combine<T, C::M, C::NT>(g2, sp, stream);
+        if (e != cudaSuccess) {
+            snprintf(msg, msg_len, "decode512 combine launch: %s", cudaGetErrorString(e));
+            return PA_ERR_CUDA;
+        }
+        timer_end(PA_KC_COMBINE, stream);
+        count_launches(1);
+    }
+    return PA_OK;
+}
+
 // Resident CTAs per SM of the kernel a plan dispatches to (occupancy API, once per
 // instantiation), for sizing the split count to whole waves.
 template <typename KernelT>
@@ -175,6 +228,13 @@ static int decode_occupancy() {
     return n;
 }
 
+template <typename T, int MG>
+static int decode512_occupancy() {
+    using C = WideCfg<MG, kWideStages>;
+    static const int n = resident_ctas(decode512_kernel<T, MG, kWideStages>, C::THREADS, C::SMEM);
+    return n;
+}
+
 template <typename T, int DP, int MT>
 static int generic_occupancy() {
     constexpr int NT = SplitShape<DP>::NT, STAGES = SplitShape<DP>::STAGES, NW = SplitShape<DP>::NW;
@@ -186,7 +246,9 @@ static int generic_occupancy() {
 template <typename T>
 static int splitkv_occupancy_t(const SplitPlan& plan) {
     static const bool force_generic = std::getenv("PA_FORCE_GENERIC") != nullptr;
-    if (plan.row_tiles == 1 && plan.dp <= 256 && !force_generic) {  // the same choice as launch_splitkv_t
+    if (plan.row_tiles == 1 && plan.dp == 512 && !force_generic)  // the same choice as launch_splitkv_t
+        return plan.mt == 1 ? decode512_occupancy<T, 1>() : decode512_occupancy<T, 2>();
+    if (plan.row_tiles == 1 && plan.dp <= 256 && !force_generic) {
         if (plan.dp == 64) return plan.mt == 1 ? decode_occupancy<T, 64, 1>() : decode_occupancy<T, 64, 2>();
         if (plan.dp == 128) return plan.mt == 1 ? decode_occupancy<T, 128, 1>() : decode_occupancy<T, 128, 2>();
         return plan.mt == 1 ? decode_occupancy<T, 256, 1>() : decode_occupancy<T, 256, 2>();
@@ -304,8 +366,12 @@ static int launch_splitkv_t(const Args& a, const SplitPlan& plan, void* workspac
         }
         return launch_decode_tc(tk, tv, sp, plan, a.dtype, a.stream, msg, msg_len);
     }
-    // decode class (one row tile of at most 32 rows, head dim <= 256): warp-sliced kernel
+    // decode class (one row tile of at most 32 rows): warp-sliced kernel up to head dim 256,
+    // quarter-column kernel above
     static const bool force_generic = std::getenv("PA_FORCE_GENERIC") != nullptr;
+    if (plan.row_tiles == 1 && plan.dp == 512 && !force_generic)
+        return plan.mt == 1 ? run_decode512<T, 1>(tk, tv, sp, plan, a.stream, msg, msg_len)
+                            : run_decode512<T, 2>(tk, tv, sp, plan, a.stream, msg, msg_len);
     if (plan.row_tiles == 1 && plan.dp <= 256 && !force_generic) {
         if (plan.dp == 64) return plan.mt == 1 ? run_decode<T, 64, 1>(tk, tv, sp, plan, a.stream, msg, msg_len)
                                                : run_decode<T, 64, 2>(tk, tv, sp, plan, a.stream, msg, msg_len);
