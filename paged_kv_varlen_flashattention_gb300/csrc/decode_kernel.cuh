@@ -8,7 +8,8 @@
 // mma.sync, runs the online softmax inside the warp (quad shuffles only), feeds P from
 // registers straight into the P.V mma, and releases the stage.  No CTA-wide barrier
 // runs inside the key loop; the per-warp (max, sum, O) triples are merged once at the
-// end through shared memory.
+// end through shared memory, each warp of a row group merging and storing a share of the
+// columns.
 #pragma once
 
 #include "splitkv_kernel.cuh"
@@ -28,13 +29,12 @@ struct DecCfg {
     static constexpr int Q_BYTES = CH * M * 128;
     static constexpr int OFF_Q = STAGES * STAGE_BYTES;
     static constexpr int OFF_ROW = OFF_Q + Q_BYTES;            // row_lo[M], row_hi[M], row_dg[M], row_ab[M]
-    static constexpr int OFF_ML = OFF_ROW + 4 * M * 4;         // m[4][16], l[4][16] of the merge
-    static constexpr int OFF_BAR = (OFF_ML + 2 * 4 * 16 * 4 + 15) & ~15;
+    static constexpr int OFF_BAR = (OFF_ROW + 4 * M * 4 + 15) & ~15;
     static constexpr int OFF_FLAG = OFF_BAR + 2 * STAGES * 8;
     static constexpr int OFF_IDS = OFF_FLAG + 16;              // block id of every TMA box of the split
     static constexpr int MAX_BOXES = 512;
     static constexpr int SMEM = OFF_IDS + MAX_BOXES * 4 + 1024;
-    static constexpr int MERGE_BYTES = 4 * 16 * DP * 4;        // O of every warp, reuses the stages
+    static constexpr int MERGE_BYTES = 4 * (DP / 8) * 32 * 16 + 4 * 32 * 16;  // O, m, l of every warp, in the stages
     static constexpr bool Q_IN_REGS = DP <= 128;
     static_assert(KPW % 16 == 0, "keys per warp");
     static_assert(MERGE_BYTES <= STAGES * STAGE_BYTES, "merge scratch");
@@ -102,8 +102,6 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const __grid_con
     int* row_hi = row_lo + M;
     int* row_dg = row_hi + M;
     float* row_ab = reinterpret_cast<float*>(row_dg + M);
-    float* m_sm = reinterpret_cast<float*>(smem + C::OFF_ML);
-    float* l_sm = m_sm + 4 * 16;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* empty = full + STAGES;
     volatile uint32_t* abort_flag = reinterpret_cast<uint32_t*>(smem + C::OFF_FLAG);
@@ -132,20 +130,34 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const __grid_con
         *abort_flag = 0u;
         fence_mbar_init();
     }
-    if (tid < 128) {  // q rows -> shared memory (128-byte swizzled rows, zero padded)
+    if (tid < 128) {  // q rows -> shared memory (128-byte swizzled rows, zero padded); each
+                      // thread issues its loads in batches ahead of their stores
         const T* q = static_cast<const T*>(p.q);
         constexpr int UNITS = DP / 8;
+        constexpr int QI = (M * UNITS + 127) / 128;
+        constexpr int QB = QI < 4 ? QI : 4;
         uint8_t* qs = smem + C::OFF_Q;
-        for (int idx = tid; idx < M * UNITS; idx += 128) {
-            const int r = idx / UNITS, u = idx - r * UNITS;
-            int4 val = make_int4(0, 0, 0, 0);
-            if (r < tv.rows && u * 8 < p.D) {
-                const int rho = tv.row0 + r;
-                const int i = rho / p.G, g = rho - i * p.G;
-                val = __ldg(reinterpret_cast<const int4*>(q + (int64_t)(tv.q0 + i) * p.q_s0 +
-                                                          (int64_t)(hk * p.G + g) * p.q_s1 + u * 8));
+#pragma unroll
+        for (int j0 = 0; j0 < QI; j0 += QB) {
+            int4 val[QB];
+#pragma unroll
+            for (int j = 0; j < QB; ++j) {
+                const int idx = tid + (j0 + j) * 128;
+                const int r = idx / UNITS, u = idx - r * UNITS;
+                val[j] = make_int4(0, 0, 0, 0);
+                if (idx < M * UNITS && r < tv.rows && u * 8 < p.D) {
+                    const int rho = tv.row0 + r;
+                    const int i = rho / p.G, g = rho - i * p.G;
+                    val[j] = __ldg(reinterpret_cast<const int4*>(q + (int64_t)(tv.q0 + i) * p.q_s0 +
+                                                                 (int64_t)(hk * p.G + g) * p.q_s1 + u * 8));
+                }
             }
-            *reinterpret_cast<int4*>(qs + (u >> 3) * (M * 128) + swz128(r, u & 7)) = val;
+#pragma unroll
+            for (int j = 0; j < QB; ++j) {
+                const int idx = tid + (j0 + j) * 128;
+                const int r = idx / UNITS, u = idx - r * UNITS;
+                if (idx < M * UNITS) *reinterpret_cast<int4*>(qs + (u >> 3) * (M * 128) + swz128(r, u & 7)) = val[j];
+            }
         }
     }
     __syncthreads();
@@ -347,58 +359,74 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const __grid_con
     }
 
     // ---- merge the KW key slices of each row group, then write ----
+    // Every warp leaves its (O, m, l) in shared memory lane for lane; warp kq of a row group
+    // then merges the KW slices of the kq-th share of the columns and stores them.
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    named_barrier_sync(1, 128);  // every consumer is done with the stages (reused below)
-    if (*abort_flag) return;     // set before the barrier by whichever role gave up
-    float* o_sm = reinterpret_cast<float*>(smem);  // [warp][16][DP]
-    if (tq == 0) {
-        m_sm[warp * 16 + gq] = m0;
-        m_sm[warp * 16 + gq + 8] = m1;
-        l_sm[warp * 16 + gq] = l0;
-        l_sm[warp * 16 + gq + 8] = l1;
-    }
+    // every consumer is done with the stages (reused below); stop together if any role gave up
+    if (named_barrier_or(1, 128, !ok || *abort_flag != 0u)) return;
+    float4* xo = reinterpret_cast<float4*>(smem);  // [warp][n8 tile][lane]
+    float4* xml = xo + 4 * (DP / 8) * 32;          // [warp][lane]: m0, m1, l0, l1
 #pragma unroll
-    for (int n = 0; n < DP / 8; ++n) {
-        const int d = n * 8 + tq * 2;
-        *reinterpret_cast<float2*>(o_sm + (warp * 16 + gq) * DP + d) = make_float2(o[n][0], o[n][1]);
-        *reinterpret_cast<float2*>(o_sm + (warp * 16 + gq + 8) * DP + d) = make_float2(o[n][2], o[n][3]);
-    }
+    for (int n = 0; n < DP / 8; ++n) xo[(warp * (DP / 8) + n) * 32 + lane] = make_float4(o[n][0], o[n][1], o[n][2], o[n][3]);
+    xml[warp * 32 + lane] = make_float4(m0, m1, l0, l1);
     named_barrier_sync(1, 128);
 
-    T* out = static_cast<T*>(p.out);
-    // each thread: pairs of columns of one row
-    for (int idx = tid; idx < M * (DP / 2); idx += 128) {
-        const int row = idx / (DP / 2), d = (idx - row * (DP / 2)) * 2;
-        if (row >= tv.rows || d >= p.D) continue;
-        const int g16 = row >> 4, rw = row & 15;
-        float mm = -INFINITY;
+    float f0[C::KW], f1[C::KW];
+    float L0 = 0.f, L1 = 0.f, mm0 = -INFINITY, mm1 = -INFINITY;
 #pragma unroll
-        for (int k = 0; k < C::KW; ++k) mm = fmaxf(mm, m_sm[(g16 * C::KW + k) * 16 + rw]);
-        const float mu = mm == -INFINITY ? 0.f : mm;
-        float L = 0.f, x0 = 0.f, x1 = 0.f;
+    for (int k = 0; k < C::KW; ++k) {
+        const float4 ml = xml[(rg * C::KW + k) * 32 + lane];
+        mm0 = fmaxf(mm0, ml.x);
+        mm1 = fmaxf(mm1, ml.y);
+    }
+    {
+        const float u0 = mm0 == -INFINITY ? 0.f : mm0, u1 = mm1 == -INFINITY ? 0.f : mm1;
 #pragma unroll
         for (int k = 0; k < C::KW; ++k) {
-            const int w = g16 * C::KW + k;
-            const float f = fast_exp2(m_sm[w * 16 + rw] - mu);
-            L += f * l_sm[w * 16 + rw];
-            const float2 ov = *reinterpret_cast<const float2*>(o_sm + (w * 16 + rw) * DP + d);
-            x0 += f * ov.x;
-            x1 += f * ov.y;
+            const float4 ml = xml[(rg * C::KW + k) * 32 + lane];
+            f0[k] = fast_exp2(ml.x - u0);
+            f1[k] = fast_exp2(ml.y - u1);
+            L0 += f0[k] * ml.z;
+            L1 += f1[k] * ml.w;
         }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
+    }
+    const float inv0 = L0 > 0.f ? 1.f / L0 : 0.f, inv1 = L1 > 0.f ? 1.f / L1 : 0.f;
+    constexpr int NPW = (DP / 8) / C::KW;  // n8 column tiles this warp stores
+    T* out = static_cast<T*>(p.out);
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+        const int row = hr ? r1 : r0;
+        if (row >= tv.rows) continue;
         const int rho = tv.row0 + row;
         const int i = rho / p.G, g = rho - i * p.G;
         const int64_t t = tv.q0 + i;
         const int h = hk * p.G + g;
-        if (single)
-            *reinterpret_cast<uint32_t*>(out + t * p.o_s0 + (int64_t)h * p.o_s1 + d) = pack2<T>(x0 * inv, x1 * inv);
-        else
-            *reinterpret_cast<float2*>(p.part_o + ((int64_t)split * p.part_stride + t * p.H + h) * p.D + d) =
-                make_float2(x0 * inv, x1 * inv);
-        if (d == 0) {
+        T* orow = out + t * p.o_s0 + (int64_t)h * p.o_s1;
+        float* prow = p.part_o + ((int64_t)split * p.part_stride + t * p.H + h) * p.D;
+        const float inv = hr ? inv1 : inv0;
+#pragma unroll
+        for (int nn = 0; nn < NPW; ++nn) {
+            const int n = kq * NPW + nn;
+            const int d = n * 8 + tq * 2;
+            if (d >= p.D) continue;
+            float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+            for (int k = 0; k < C::KW; ++k) {
+                const float4 ov = xo[((rg * C::KW + k) * (DP / 8) + n) * 32 + lane];
+                const float f = hr ? f1[k] : f0[k];
+                x0 += f * (hr ? ov.z : ov.x);
+                x1 += f * (hr ? ov.w : ov.y);
+            }
+            if (single)
+                *reinterpret_cast<uint32_t*>(orow + d) = pack2<T>(x0 * inv, x1 * inv);
+            else
+                *reinterpret_cast<float2*>(prow + d) = make_float2(x0 * inv, x1 * inv);
+        }
+        if (kq == 0 && tq == 0) {
+            const float L = hr ? L1 : L0, mm = hr ? mm1 : mm0;
             const float lse = L > 0.f ? (mm + log2f(L)) * 0.69314718055994531f : -INFINITY;
             if (single)
                 p.lse[(int64_t)h * p.lse_s0 + t + (int64_t)b * p.lse_sb] = lse;

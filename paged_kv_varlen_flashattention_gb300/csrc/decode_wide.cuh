@@ -54,21 +54,6 @@ struct WideCfg {
     static_assert(SMEM + (kRankInCta + 1) * 4 <= 227 * 1024, "shared memory per CTA");
 };
 
-// Barrier among `nthreads` threads on hardware barrier `id` that also returns whether `pred`
-// held in any of them (every participant gets the same answer).
-__device__ __forceinline__ bool named_barrier_or(int id, int nthreads, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.or.pred po, %2, %3, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
-        : "memory");
-    return r != 0;
-}
-
 template <typename T, int MG, int STAGES>
 __global__ void __launch_bounds__(WideCfg<MG, STAGES>::THREADS, 1)
     decode512_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
