@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const __grid_con
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    allow_dependent_launch();
     // Sequences longest first (ties by index): their CTAs start first and the short ones
     // fill the tail of the grid.  Small batches are ranked here, one sequence per thread;
     // larger ones come with an order from a ranking pass.

@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(WideCfg<MG, STAGES>::THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    allow_dependent_launch();
     // sequences longest first, as in the warp-sliced decode kernel
     __shared__ int rank_len[kRankInCta];
     __shared__ int rank_pick;
@@ -208,19 +209,17 @@ __global__ void __launch_bounds__(WideCfg<MG, STAGES>::THREADS, 1)
     const int gq = lane >> 2, tq = lane & 3;
     const int mi = lane >> 3, rr = lane & 7;
     const int r0 = rg * 16 + gq, r1 = r0 + 8;  // the two rows this lane holds
-    const int lo0 = row_lo[r0], hi0 = row_hi[r0], lo1 = row_lo[r1], hi1 = row_hi[r1];
-    const int dg0 = row_dg[r0], dg1 = row_dg[r1];
-    const float ab0 = row_ab[r0], ab1 = row_ab[r1];
-    // Key interval every real row of this warp attends: tiles inside it need no mask.
-    // Padding rows (past the tile's rows) are never written and do not restrict it.
+    // Key interval every real row of this warp attends: tiles inside it need no mask (the
+    // rows' own bounds are read from shared memory only for the tiles that do).  Padding
+    // rows (past the tile's rows) are never written and do not restrict it.
     int wlo = INT_MIN, whi = INT_MAX;
     if (r0 < tv.rows) {
-        wlo = max(wlo, lo0);
-        whi = min(whi, hi0);
+        wlo = max(wlo, row_lo[r0]);
+        whi = min(whi, row_hi[r0]);
     }
     if (r1 < tv.rows) {
-        wlo = max(wlo, lo1);
-        whi = min(whi, hi1);
+        wlo = max(wlo, row_lo[r1]);
+        whi = min(whi, row_hi[r1]);
     }
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
@@ -260,7 +259,7 @@ __global__ void __launch_bounds__(WideCfg<MG, STAGES>::THREADS, 1)
         const int kt = tv.kt0 + (t_begin + it) * NT;
         uint8_t* kst = smem + stage * C::STAGE_BYTES;
         uint8_t* vst = kst + C::TILE_BYTES;
-        float* xb = reinterpret_cast<float*>(smem + C::OFF_X + (it & 1) * C::XBUF_BYTES);
+        const uint32_t xb = smem_addr(smem + C::OFF_X + (it & 1) * C::XBUF_BYTES);
         float s[C::NSC][4];
 #pragma unroll
         for (int n = 0; n < C::NSC; ++n)
@@ -297,8 +296,7 @@ __global__ void __launch_bounds__(WideCfg<MG, STAGES>::THREADS, 1)
             }
 #pragma unroll
             for (int n = 0; n < C::NSC; ++n)
-                *reinterpret_cast<float4*>(xb + ((warp * C::NSC + n) * 32 + lane) * 4) =
-                    make_float4(s[n][0], s[n][1], s[n][2], s[n][3]);
+                st_shared_f4(xb + ((warp * C::NSC + n) * 32 + lane) * 16, make_float4(s[n][0], s[n][1], s[n][2], s[n][3]));
         }
         // every quarter of the group has posted its partial (or one of them gave up)
         if (named_barrier_or(2 + grp, 128, !ok)) {
@@ -308,10 +306,10 @@ __global__ void __launch_bounds__(WideCfg<MG, STAGES>::THREADS, 1)
         // full scores: the four partials in quarter order (identical in all four warps)
 #pragma unroll
         for (int n = 0; n < C::NSC; ++n) {
-            float4 a = *reinterpret_cast<const float4*>(xb + (((grp * 4) * C::NSC + n) * 32 + lane) * 4);
+            float4 a = ld_shared_f4(xb + (((grp * 4) * C::NSC + n) * 32 + lane) * 16);
 #pragma unroll
             for (int w4 = 1; w4 < 4; ++w4) {
-                const float4 v = *reinterpret_cast<const float4*>(xb + (((grp * 4 + w4) * C::NSC + n) * 32 + lane) * 4);
+                const float4 v = ld_shared_f4(xb + (((grp * 4 + w4) * C::NSC + n) * 32 + lane) * 16);
                 a.x += v.x;
                 a.y += v.y;
                 a.z += v.z;
@@ -325,24 +323,31 @@ __global__ void __launch_bounds__(WideCfg<MG, STAGES>::THREADS, 1)
         // scale into the log2 domain, mask by select (unless the tile is inside every row's
         // interval and there is no position bias), and take the row maxima
         const bool inside = !p.alibi && kt + key0 >= wlo && kt + key0 + C::KPW - 1 <= whi;
-        float mx0 = -INFINITY, mx1 = -INFINITY;
+        if (inside) {
 #pragma unroll
-        for (int n = 0; n < C::NSC; ++n)
+            for (int n = 0; n < C::NSC; ++n)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const bool up = e < 2;
-                if (inside) {
-                    s[n][e] *= p.scale_log2;
-                } else {
+                for (int e = 0; e < 4; ++e) s[n][e] *= p.scale_log2;
+        } else {
+            const int lo0 = row_lo[r0], hi0 = row_hi[r0], lo1 = row_lo[r1], hi1 = row_hi[r1];
+            const int dg0 = row_dg[r0], dg1 = row_dg[r1];
+            const float ab0 = row_ab[r0], ab1 = row_ab[r1];
+#pragma unroll
+            for (int n = 0; n < C::NSC; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const bool up = e < 2;
                     const int key = kt + key0 + n * 8 + tq * 2 + (e & 1);
                     const bool in = up ? (key >= lo0 && key <= hi0) : (key >= lo1 && key <= hi1);
                     s[n][e] = in ? biased_log2(s[n][e], p.scale_log2, up ? ab0 : ab1, up ? dg0 : dg1, key) : -INFINITY;
                 }
-                if (up)
-                    mx0 = fmaxf(mx0, s[n][e]);
-                else
-                    mx1 = fmaxf(mx1, s[n][e]);
-            }
+        }
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int n = 0; n < C::NSC; ++n) {
+            mx0 = max3f(mx0, s[n][0], s[n][1]);
+            mx1 = max3f(mx1, s[n][2], s[n][3]);
+        }
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));

@@ -114,6 +114,26 @@ __device__ __forceinline__ bool named_barrier_or(int id, int nthreads, bool pred
     return r != 0;
 }
 
+// Lets the grid launched after this one as its programmatic dependent (the split-KV
+// combine) start on SMs this grid leaves free once every CTA of it has started; the
+// dependent still reads nothing this grid writes before its griddepcontrol.wait.
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// 16-byte shared-memory store and load by shared-window address (explicit .shared: a
+// pointer rebuilt from an integer would otherwise be accessed through the generic path).
+__device__ __forceinline__ void st_shared_f4(uint32_t addr, float4 v) {
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 // ---- TMA ---------------------------------------------------------------------------------
 // Tiled 4-D tensor load into shared memory, completing on `bar` (complete_tx bytes).
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0,

@@ -149,6 +149,7 @@ __global__ void __launch_bounds__(NW * 32) splitkv_kernel(const __grid_constant_
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    allow_dependent_launch();
     const int b = blockIdx.z, hk = blockIdx.y % p.Hkv, rt = blockIdx.y / p.Hkv, split = blockIdx.x;
 
     TileView tv;
@@ -488,26 +489,29 @@ int launch_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const SplitPa
 // row: the split weights are computed once per row into shared memory, then each lane
 // accumulates pairs of output columns over the splits (reads of the partials coalesce
 // along the head dimension).
-constexpr int kCombineRows = 4;
-constexpr int kCombineMaxSplits = 1024;  // weights kept in shared memory per warp
+constexpr int kCombineRows = 1;          // output rows per CTA (grid.x = rows x 64-column chunks)
+constexpr int kCombineMaxSplits = 1024;  // split weights kept in shared memory
 
+// (A minimum of 8 CTAs an SM caps it at 64 registers; with the thread count alone ptxas
+// chose 32 and issued the partial loads a few at a time.)
 template <typename T, int M, int NT>
-__global__ void __launch_bounds__(128) combine_kernel(const SplitParams p) {
-    // grid.x = row blocks x 64-column chunks: one warp per (row, 64 output columns), so a
-    // handful of long rows with many splits still spreads over many warps
-    __shared__ float wsm[kCombineRows][kCombineMaxSplits];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(128, 8) combine_kernel(const SplitParams p) {
+    // One CTA per (row, 64 output columns).  Its 128 threads load the row's split LSEs at
+    // once and turn them into weights in shared memory; warp w then sums the partial rows
+    // of splits w, w + 4, ... with all of its loads in flight together, and warp 0 adds the
+    // four sums: three dependent memory round trips however many splits there are (<= 256).
+    __shared__ float wsm[kCombineMaxSplits];
+    __shared__ float red[2][4];
+    __shared__ float2 part[4][32];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.z, hk = blockIdx.y % p.Hkv, rt = blockIdx.y / p.Hkv;
     const int n_chunks = (p.D + 63) / 64;
-    // launched as a programmatic dependent of the split kernel (its launch overlaps that
-    // kernel's tail): the partial results are read only after it has completed
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int chunk = blockIdx.x % n_chunks;
-    TileView tv;
+    TileView tv;  // from the sequence bounds alone, which the split kernel does not write
     if (!tile_view<M, NT>(p, b, rt, tv, false)) return;
     if (tv.nsplit <= 1) return;
     const int ns = min(tv.nsplit, kCombineMaxSplits);
-    const int r = (blockIdx.x / n_chunks) * kCombineRows + warp;
+    const int r = blockIdx.x / n_chunks;
     if (r >= tv.rows) return;
     T* out = static_cast<T*>(p.out);
     const int rho = tv.row0 + r;
@@ -515,57 +519,65 @@ __global__ void __launch_bounds__(128) combine_kernel(const SplitParams p) {
     const int64_t t = tv.q0 + i;
     const int h = hk * p.G + g;
     const int64_t row = t * p.H + h;
-    float* w = wsm[warp];
+    // launched as a programmatic dependent of the split kernel (its launch and the lines
+    // above overlap that kernel's tail): the partial results are read only after it completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
     float mx = -INFINITY;
-    for (int s = lane; s < ns; s += 32) {
+    for (int s = tid; s < ns; s += 128) {
         const float l = p.part_lse[(int64_t)s * p.part_stride + row];
-        w[s] = l;
+        wsm[s] = l;
         mx = fmaxf(mx, l);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) red[0][warp] = mx;
+    __syncthreads();
+    mx = fmaxf(fmaxf(red[0][0], red[0][1]), fmaxf(red[0][2], red[0][3]));
     const float m_use = (mx == -INFINITY) ? 0.f : mx;
     float sum = 0.f;
-    for (int s = lane; s < ns; s += 32) {
-        const float e = fast_exp2((w[s] - m_use) * 1.4426950408889634f);
-        w[s] = e;
+    for (int s = tid; s < ns; s += 128) {
+        const float e = fast_exp2((wsm[s] - m_use) * 1.4426950408889634f);
+        wsm[s] = e;
         sum += e;
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    __syncwarp();
-    const float inv = sum > 0.f ? 1.f / sum : 0.f;
+    if (lane == 0) red[1][warp] = sum;
+    __syncthreads();
+    sum = (red[1][0] + red[1][1]) + (red[1][2] + red[1][3]);
+
     const int d = chunk * 64 + lane * 2;
+    float x0 = 0.f, x1 = 0.f;
     if (d < p.D) {
         const float* po = p.part_o + row * p.D + d;
         const int64_t split_stride = p.part_stride * p.D;
-        // eight splits per step with independent accumulators: eight loads in flight
-        float a0[8], a1[8];
+        constexpr int U = 16;
+        for (int s0 = warp; s0 < ns; s0 += 4 * U) {
+            // indices past the last split re-read the last one (in bounds, unconditional, so
+            // that every load is issued before the first is used) and weigh it 0
+            float2 v[U];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) a0[u] = a1[u] = 0.f;
-        int s = 0;
-        for (; s + 8 <= ns; s += 8) {
+            for (int u = 0; u < U; ++u)
+                v[u] = __ldg(reinterpret_cast<const float2*>(po + (int64_t)min(s0 + 4 * u, ns - 1) * split_stride));
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const float2 o = *reinterpret_cast<const float2*>(po + (int64_t)(s + u) * split_stride);
-                a0[u] = fmaf(w[s + u], o.x, a0[u]);
-                a1[u] = fmaf(w[s + u], o.y, a1[u]);
+            for (int u = 0; u < U; ++u) {
+                const int s = s0 + 4 * u;
+                const float wgt = s < ns ? wsm[min(s, ns - 1)] : 0.f;
+                x0 = fmaf(wgt, v[u].x, x0);
+                x1 = fmaf(wgt, v[u].y, x1);
             }
         }
-        for (; s < ns; ++s) {
-            const float2 o = *reinterpret_cast<const float2*>(po + (int64_t)s * split_stride);
-            a0[0] = fmaf(w[s], o.x, a0[0]);
-            a1[0] = fmaf(w[s], o.y, a1[0]);
-        }
-        float x0 = 0.f, x1 = 0.f;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            x0 += a0[u];
-            x1 += a1[u];
-        }
-        *reinterpret_cast<uint32_t*>(out + t * p.o_s0 + (int64_t)h * p.o_s1 + d) = pack2<T>(x0 * inv, x1 * inv);
     }
-    if (chunk == 0 && lane == 0)
+    part[warp][lane] = make_float2(x0, x1);
+    __syncthreads();
+    if (warp == 0 && d < p.D) {
+        const float inv = sum > 0.f ? 1.f / sum : 0.f;
+        const float2 a = part[0][lane], c = part[1][lane], e = part[2][lane], f = part[3][lane];
+        *reinterpret_cast<uint32_t*>(out + t * p.o_s0 + (int64_t)h * p.o_s1 + d) =
+            pack2<T>(((a.x + c.x) + (e.x + f.x)) * inv, ((a.y + c.y) + (e.y + f.y)) * inv);
+    }
+    if (chunk == 0 && tid == 0)
         p.lse[(int64_t)h * p.lse_s0 + t + (int64_t)b * p.lse_sb] = sum > 0.f ? m_use + logf(sum) : -INFINITY;
 }
 
