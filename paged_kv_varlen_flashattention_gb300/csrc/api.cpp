@@ -620,8 +620,12 @@ SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, int num_sms)
     const int64_t tiles_max = std::max<int64_t>(1, kspan / pl.nt + 2);
     int64_t split_tiles = tiles_max;
     const int64_t units = (int64_t)a.batch * a.Hkv * pl.row_tiles;
-    if (const char* env = std::getenv("PA_SPLIT_TILES")) {
-        split_tiles = std::max<int64_t>(1, std::atoll(env));
+    const char* env_tiles = std::getenv("PA_SPLIT_TILES");
+    if (pl.row_tiles == 1)
+        pl.slots = num_sms * (pl.tc ? decode_tc_occupancy(a.dtype, pl.dp, M)
+                              : a.dtype == PA_BF16 ? splitkv_occupancy_bf16(pl) : splitkv_occupancy_f16(pl));
+    if (env_tiles) {
+        split_tiles = std::max<int64_t>(1, std::atoll(env_tiles));
     } else if (pl.row_tiles == 1) {
         // Fewer (sequence, kv head) units than resident CTA slots: one wave, every unit's keys
         // split evenly over slots / units CTAs (each further wave would add a pipeline ramp,
@@ -631,9 +635,7 @@ SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, int num_sms)
         // 5.72 with two splits per unit and 5.61 with three).  A split is never shorter than
         // 4 tiles, nor than 8 M keys: its fp32 partial result (M rows x D x 4 bytes, written
         // and read back) then costs at most ~1/8 of the K/V bytes it reads.
-        const int64_t slots =
-            (int64_t)num_sms * (pl.tc ? decode_tc_occupancy(a.dtype, pl.dp, M)
-                                : a.dtype == PA_BF16 ? splitkv_occupancy_bf16(pl) : splitkv_occupancy_f16(pl));
+        const int64_t slots = pl.slots;
         int64_t splits = units < slots ? slots / units : 1;
         splits = std::max<int64_t>(1, std::min(splits, tiles_max));
         const int64_t min_tiles = std::max<int64_t>(4, (8ll * M + pl.nt - 1) / pl.nt);
@@ -642,7 +644,8 @@ SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, int num_sms)
         // lengths, so a batch where one sequence is far longer than the rest (a 131,072-key
         // sequence among 4,096-key ones) would otherwise leave that sequence's one CTA per kv
         // head as the tail of the grid; with the cap its keys spread over many CTAs, while
-        // sequences below the cap keep one CTA (their further split indices exit at once).
+        // sequences below the cap keep one CTA (their further split indices exit at once, or,
+        // in the persistent mode below, are never listed).
         split_tiles = std::min(split_tiles, std::max(min_tiles, kMaxSplitKeys / pl.nt));
     }
     split_tiles = std::min(split_tiles, tiles_max);
@@ -652,14 +655,23 @@ SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, int num_sms)
         pl.split_tiles = (int)((tiles_max + 1023) / 1024);
         pl.max_splits = (int)((tiles_max + pl.split_tiles - 1) / pl.split_tiles);
     }
-    // the decode kernels launch sequences longest first (a one-CTA ranking pass) for
-    // batches they can rank; the order sits at the start of the scratch
+    // Persistent mode of the warp-sliced decode kernel: when a batch of many sequences has
+    // some sequence split, the split indices of every shorter sequence would be CTAs without
+    // work (about 1.5 us of an SM slot each: 40 us of a 223 us call on a 64-sequence batch
+    // with one 131,072-key sequence).  A one-CTA pass then lists the (sequence, split) items
+    // on the device and one CTA per resident slot takes them in turn (that batch: 180 us;
+    // shorter splits measured no faster: 4,096 keys 179 us, 2,048 keys 184 us).
+    pl.work = !pl.tc && pl.row_tiles == 1 && pl.dp <= 256 && !force_generic && a.batch >= kWorkMinBatch &&
+              a.batch <= kMaxOrderBatch && pl.max_splits > 1 && pl.slots > 0;
+    // Otherwise the decode kernels launch sequences longest first (a one-CTA ranking pass)
+    // for batches they can rank; the order sits at the start of the scratch
     const bool decode_kernel = pl.tc || (pl.row_tiles == 1 && !force_generic);
-    pl.rank_in_cta = decode_kernel && a.batch >= 2 && a.batch <= kRankInCta;
-    pl.order_bytes = decode_kernel && a.batch > kRankInCta && a.batch <= kMaxOrderBatch
+    pl.rank_in_cta = !pl.work && decode_kernel && a.batch >= 2 && a.batch <= kRankInCta;
+    pl.order_bytes = !pl.work && decode_kernel && a.batch > kRankInCta && a.batch <= kMaxOrderBatch
                          ? ((size_t)a.batch * sizeof(int) + 255) / 256 * 256
                          : 0;
-    pl.ws_bytes = pl.order_bytes;
+    pl.work_bytes = pl.work ? ((2 + 2 * (size_t)a.batch * pl.max_splits) * sizeof(int) + 255) / 256 * 256 : 0;
+    pl.ws_bytes = pl.order_bytes + pl.work_bytes;
     if (pl.max_splits > 1) {
         const size_t rows = (size_t)a.total_q * a.H;
         pl.ws_bytes += (size_t)pl.max_splits * rows * ((size_t)a.D + 1) * sizeof(float) + 256;

@@ -56,48 +56,25 @@ __device__ __forceinline__ bool dec_wait(uint64_t* bar, uint32_t parity, volatil
     }
 }
 
+// The work of one (sequence b, kv head hk, key split) on a CTA: its rows' bounds and q into
+// shared memory, then the producer warp and the four consumer warps.  `g0` is the number of
+// key tiles the CTA's ring has carried before (ring stage and phase continue from it);
+// `n_done` returns the tiles of this unit (the same in every thread).  Every thread returns
+// from here: early (no work, uniformly), when its role ends, or after the epilogue.
 template <typename T, int DP, int MG, int NT, int STAGES>
-__global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const __grid_constant__ CUtensorMap tm_k,
-                                                     const __grid_constant__ CUtensorMap tm_v,
-                                                     const SplitParams p) {
+__device__ __forceinline__ void decode_unit(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const SplitParams& p,
+                                            uint8_t* smem, int b, int hk, int split, int g0, int& n_done) {
     using C = DecCfg<DP, MG, NT, STAGES>;
     constexpr int M = C::M;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    allow_dependent_launch();
-    // Sequences longest first (ties by index): their CTAs start first and the short ones
-    // fill the tail of the grid.  Small batches are ranked here, one sequence per thread;
-    // larger ones come with an order from a ranking pass.
-    __shared__ int rank_len[kDecodeThreads];
-    __shared__ int rank_pick;
-    int b = (int)blockIdx.z;
-    if (p.order) {
-        b = p.order[blockIdx.z];
-    } else if (p.rank_in_cta) {
-        if (tid < p.batch) rank_len[tid] = p.cu_k[tid + 1] - p.cu_k[tid];
-        if (tid == 0) rank_pick = (int)blockIdx.z;
-        __syncthreads();
-        if (tid < p.batch) {
-            const int ls = rank_len[tid];
-            int rank = 0;
-            for (int t = 0; t < p.batch; ++t) {
-                const int lt = rank_len[t];
-                rank += (lt > ls) || (lt == ls && t < tid);
-            }
-            if (rank == (int)blockIdx.z) rank_pick = tid;
-        }
-        __syncthreads();
-        b = rank_pick;
-    }
-    const int hk = blockIdx.y % p.Hkv, split = blockIdx.x;
-
     TileView tv;
+    n_done = 0;
     if (!tile_view<M, NT>(p, b, 0, tv, split == 0)) return;
     if (split >= max(tv.nsplit, 1)) return;
     const bool single = tv.nsplit <= 1;
     const int t_begin = split * p.split_tiles;
     const int n_iter = max(0, min(tv.ntiles, t_begin + p.split_tiles) - t_begin);
+    n_done = n_iter;
 
     int* row_lo = reinterpret_cast<int*>(smem + C::OFF_ROW);
     int* row_hi = row_lo + M;
@@ -122,14 +99,6 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const __grid_con
         row_hi[tid] = hi;
         row_dg[tid] = dg;
         row_ab[tid] = ab;
-    }
-    if (tid == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 4);
-        }
-        *abort_flag = 0u;
-        fence_mbar_init();
     }
     if (tid < 128) {  // q rows -> shared memory (128-byte swizzled rows, zero padded); each
                       // thread issues its loads in batches ahead of their stores
@@ -181,8 +150,9 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const __grid_con
             prefetch_tmap(&tm_v);
             const uint64_t policy = l2_policy_evict_first();
             for (int it = 0; it < n_iter; ++it) {
-                const int stage = it % STAGES;
-                if (it >= STAGES && !dec_wait(&empty[stage], ((it / STAGES) - 1) & 1, abort_flag, p.err, p.wait_ns)) break;
+                const int gi = g0 + it;  // position in the CTA's stream of tiles
+                const int stage = gi % STAGES;
+                if (gi >= STAGES && !dec_wait(&empty[stage], ((gi / STAGES) - 1) & 1, abort_flag, p.err, p.wait_ns)) break;
                 const int kt = kbeg + it * NT;
                 uint8_t* kst = smem + stage * C::STAGE_BYTES;
                 uint8_t* vst = kst + C::TILE_BYTES;
@@ -245,8 +215,9 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const __grid_con
     bool ok = true;
 
     for (int it = 0; it < n_iter; ++it) {
-        const int stage = it % STAGES;
-        ok = __all_sync(0xffffffffu, dec_wait(&full[stage], (it / STAGES) & 1, abort_flag, p.err, p.wait_ns));
+        const int gi = g0 + it;
+        const int stage = gi % STAGES;
+        ok = __all_sync(0xffffffffu, dec_wait(&full[stage], (gi / STAGES) & 1, abort_flag, p.err, p.wait_ns));
         if (!ok) break;
         const int kt = tv.kt0 + (t_begin + it) * NT;
         uint8_t* kst = smem + stage * C::STAGE_BYTES;
@@ -435,6 +406,78 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const __grid_con
                 p.part_lse[(int64_t)split * p.part_stride + t * p.H + h] = lse;
         }
     }
+}
+
+template <typename T, int DP, int MG, int NT, int STAGES>
+__global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                     const __grid_constant__ CUtensorMap tm_v,
+                                                     const SplitParams p) {
+    using C = DecCfg<DP, MG, NT, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x;
+    allow_dependent_launch();
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* empty = full + STAGES;
+    volatile uint32_t* abort_flag = reinterpret_cast<uint32_t*>(smem + C::OFF_FLAG);
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 4);
+        }
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (p.work) {
+        // Persistent: the CTA takes (sequence, split) x kv head items in list order (longest
+        // sequences first) until none is left; the stage ring carries on from item to item.
+        __shared__ int s_item;
+        const int total = p.work[1] * p.Hkv;
+        int g0 = 0;
+        for (;;) {
+            if (tid == 0) s_item = atomicAdd(p.work, 1);
+            __syncthreads();  // also orders the barrier set-up before the first item
+            const int w = s_item;
+            if (w >= total) break;
+            const int pair = w / p.Hkv;
+            int n_done = 0;
+            decode_unit<T, DP, MG, NT, STAGES>(tm_k, tm_v, p, smem, p.work[2 + 2 * pair], w - pair * p.Hkv,
+                                               p.work[3 + 2 * pair], g0, n_done);
+            // every role is done with the item (its stages, q and rows); the epilogue's
+            // shared-memory writes are ordered before the next item's TMA writes to the stages
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (*abort_flag) break;
+            g0 += n_done;
+        }
+        return;
+    }
+    // Sequences longest first (ties by index): their CTAs start first and the short ones
+    // fill the tail of the grid.  Small batches are ranked here, one sequence per thread;
+    // larger ones come with an order from a ranking pass.
+    __shared__ int rank_len[kDecodeThreads];
+    __shared__ int rank_pick;
+    int b = (int)blockIdx.z;
+    if (p.order) {
+        b = p.order[blockIdx.z];
+    } else if (p.rank_in_cta) {
+        if (tid < p.batch) rank_len[tid] = p.cu_k[tid + 1] - p.cu_k[tid];
+        if (tid == 0) rank_pick = (int)blockIdx.z;
+        __syncthreads();
+        if (tid < p.batch) {
+            const int ls = rank_len[tid];
+            int rank = 0;
+            for (int t = 0; t < p.batch; ++t) {
+                const int lt = rank_len[t];
+                rank += (lt > ls) || (lt == ls && t < tid);
+            }
+            if (rank == (int)blockIdx.z) rank_pick = tid;
+        }
+        __syncthreads();
+        b = rank_pick;
+    }
+    int n_done = 0;
+    decode_unit<T, DP, MG, NT, STAGES>(tm_k, tm_v, p, smem, b, (int)blockIdx.y % p.Hkv, (int)blockIdx.x, 0, n_done);
 }
 
 }  // namespace pa

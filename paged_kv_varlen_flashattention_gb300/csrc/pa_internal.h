@@ -64,10 +64,13 @@ struct SplitPlan {
     int tile_rows;    // most rows a row tile can hold: min(16 * mt, max_seqlen_q * G)
     int split_tiles;  // key tiles per split
     int max_splits;   // grid.x
-    size_t ws_bytes;     // scratch needed: the longest-first order, then the partial results
+    size_t ws_bytes;     // scratch needed: the longest-first order or the work list, then the partial results
     size_t order_bytes;  // bytes of the order at the start of the scratch (0: none)
+    size_t work_bytes;   // bytes of the persistent decode work list after it (0: not persistent)
+    int slots;           // resident CTAs of the split-KV kernel on the device (persistent grid)
     int rank_in_cta;     // decode kernel CTAs rank the batch themselves (small batches)
     int tc;              // decode class on the tensor-core decode kernel (128-key tiles)
+    int work;            // decode class on the persistent warp-sliced kernel (device work list)
 };
 
 // The decode kernel launches sequences longest first: batches of at most kRankInCta
@@ -76,6 +79,9 @@ constexpr int kRankInCta = 160;
 constexpr int kMaxOrderBatch = 1024;
 // Most keys one split-KV CTA of the decode class takes (the plan's cap for skewed batches).
 constexpr int64_t kMaxSplitKeys = 8192;
+// Persistent decode mode (a device-built work list taken by one CTA per resident slot) for
+// batches of at least kWorkMinBatch sequences whose plan splits some sequence.
+constexpr int kWorkMinBatch = 16;
 int launch_longest_first(const int32_t* cu_k, int batch, int* order, cudaStream_t stream, char* msg,
                          size_t msg_len);
 

@@ -43,6 +43,7 @@ struct SplitParams {
     int wl, wr;
     const float* alibi;  // per-query-head slopes of the linear position bias, or nullptr
     const int* order;    // decode kernel: sequence of grid z index (longest first), or nullptr
+    int* work;           // decode kernel, persistent mode: [take counter, item count, (sequence, split)...]
     int rank_in_cta;     // decode kernel: each CTA ranks the (<= kDecodeThreads) sequences itself
     int rows_cap, row_tiles, split_tiles, max_splits;
     float* part_o;
@@ -63,15 +64,18 @@ struct TileView {
     int ntiles, nsplit;
 };
 
+// Metadata out of range is flagged in the error word when `report` holds, by thread 0 of
+// the CTA or, with `any_thread`, by the calling thread.
 template <int M, int NT>
-__device__ __forceinline__ bool tile_view(const SplitParams& p, int b, int rt, TileView& v, bool report) {
+__device__ __forceinline__ bool tile_view(const SplitParams& p, int b, int rt, TileView& v, bool report,
+                                          bool any_thread = false) {
     const int q0 = p.cu_q[b], q1 = p.cu_q[b + 1];
     const int k0 = p.cu_k[b], k1 = p.cu_k[b + 1];
     const int sq = q1 - q0, sk = k1 - k0;
     const bool bad = sq < 0 || sk < 0 || sq > p.max_sq || sk > p.max_sk || q0 < 0 || q1 > p.total_q ||
                      (!p.paged && (k0 < 0 || k1 > p.num_blocks));
     if (bad) {
-        if (report && threadIdx.x == 0) flag_error(p.err, PA_ERR_DEVICE_BOUNDS);
+        if (report && (any_thread || threadIdx.x == 0)) flag_error(p.err, PA_ERR_DEVICE_BOUNDS);
         return false;
     }
     if (sq == 0) return false;
@@ -99,7 +103,7 @@ __device__ __forceinline__ bool tile_view(const SplitParams& p, int b, int rt, T
         v.nsplit = (v.ntiles + p.split_tiles - 1) / p.split_tiles;
     }
     if (v.nsplit > p.max_splits) {  // a sequence longer than max_seqlen_k promised
-        if (report && threadIdx.x == 0) flag_error(p.err, PA_ERR_DEVICE_BOUNDS);
+        if (report && (any_thread || threadIdx.x == 0)) flag_error(p.err, PA_ERR_DEVICE_BOUNDS);
         v.nsplit = p.max_splits;
         v.ntiles = min(v.ntiles, p.max_splits * p.split_tiles);
     }

@@ -109,6 +109,70 @@ struct DecShape<256> {
     static constexpr int STAGES = 3;
 };
 
+// Work list of the persistent decode mode, one CTA and one sequence per thread: work[0] =
+// the take counter (zeroed here), work[1] = the number of (sequence, split) items, then
+// the items, sequences longest first (by key tiles, ties by index) with each sequence's
+// splits in order.  A sequence's split count comes from the tile view the kernels use; a
+// sequence whose rows attend no key still gets one item (its rows are written as zeros),
+// one the prefill kernel owns or with no queries gets none.
+template <int M, int NT>
+__global__ void __launch_bounds__(kMaxOrderBatch) work_list_kernel(const SplitParams p, int* work) {
+    __shared__ int s_tiles[kMaxOrderBatch];
+    __shared__ int s_splits[kMaxOrderBatch];
+    __shared__ int s_at[kMaxOrderBatch];
+    __shared__ int s_warp[kMaxOrderBatch / 32];
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    int nt = 0, ns = 0;
+    if (t < p.batch) {
+        TileView tv;
+        if (tile_view<M, NT>(p, t, 0, tv, true, true)) {
+            nt = tv.ntiles;
+            ns = max(tv.nsplit, 1);
+        }
+        s_tiles[t] = nt;
+        s_splits[t] = ns;
+    }
+    __syncthreads();
+    if (t < p.batch) {
+        int rank = 0;
+        for (int u = 0; u < p.batch; ++u) {
+            const int lu = s_tiles[u];
+            rank += (lu > nt) || (lu == nt && u < t);
+        }
+        s_at[rank] = t;
+    }
+    __syncthreads();
+    const int seq = t < p.batch ? s_at[t] : 0;
+    const int v = t < p.batch ? s_splits[seq] : 0;  // items of the sequence of rank t
+    int x = v;                                      // inclusive scan over the ranks
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = s_warp[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, off);
+            if (lane >= off) w += y;
+        }
+        s_warp[lane] = w;
+    }
+    __syncthreads();
+    const int first = x - v + (warp > 0 ? s_warp[warp - 1] : 0);
+    for (int k = 0; k < v; ++k) {
+        work[2 + 2 * (first + k)] = seq;
+        work[3 + 2 * (first + k)] = k;
+    }
+    if (t == 0) {
+        work[0] = 0;
+        work[1] = s_warp[kMaxOrderBatch / 32 - 1];
+    }
+}
+
 template <typename T, int DP, int MG>
 static int run_decode(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& sp, const SplitPlan& plan,
                       cudaStream_t stream, char* msg, size_t msg_len) {
@@ -128,7 +192,22 @@ static int run_decode(const CUtensorMap& tk, const CUtensorMap& tv, const SplitP
         const int rc = launch_longest_first(sp.cu_k, sp.batch, const_cast<int*>(sp.order), stream, msg, msg_len);
         if (rc != PA_OK) return rc;
     }
-    dim3 grid(plan.max_splits, sp.Hkv, sp.batch);
+    if (sp.work) {
+        if (sp.batch < 1 || sp.batch > kMaxOrderBatch || plan.slots < 1) {
+            snprintf(msg, msg_len, "decode work list: batch %d, %d CTAs", sp.batch, plan.slots);
+            return PA_ERR_UNSUPPORTED;
+        }
+        NvtxRange nvw("pa::work_list_kernel");
+        work_list_kernel<C::M, NT><<<1, kMaxOrderBatch, 0, stream>>>(sp, sp.work);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) {
+            snprintf(msg, msg_len, "decode work list launch: %s", cudaGetErrorString(e));
+            return PA_ERR_CUDA;
+        }
+        count_launches(1);
+    }
+    // persistent mode: one CTA per resident slot; otherwise (split, kv head, sequence rank)
+    const dim3 grid = sp.work ? dim3(plan.slots, 1, 1) : dim3(plan.max_splits, sp.Hkv, sp.batch);
     NvtxRange nv("pa::decode_kernel");
     timer_begin(PA_KC_SPLITKV, stream);
     kern<<<grid, kDecodeThreads, C::SMEM, stream>>>(tk, tv, sp);
@@ -338,9 +417,10 @@ static int launch_splitkv_t(const Args& a, const SplitPlan& plan, void* workspac
     sp.max_splits = plan.max_splits;
     sp.part_stride = a.total_q * a.H;
     if (plan.order_bytes) sp.order = static_cast<const int*>(workspace);
+    if (plan.work_bytes) sp.work = reinterpret_cast<int*>(static_cast<char*>(workspace) + plan.order_bytes);
     sp.rank_in_cta = plan.rank_in_cta;
     if (plan.max_splits > 1) {
-        sp.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.order_bytes);
+        sp.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.order_bytes + plan.work_bytes);
         sp.part_lse = sp.part_o + (size_t)plan.max_splits * sp.part_stride * a.D;
     }
     sp.err = err;

@@ -1,9 +1,12 @@
 """Decode batches of serving size against the oracle (GPU).
 
-The decode kernel launches sequences longest first.  It ranks batches of up to 160
-sequences inside every CTA, batches of 161 to 1,024 through a separate one-CTA ranking
-pass whose order sits at the start of the call's scratch (the split partial results
-follow it), and keeps the index order above 1,024.  These cases reach each branch on
+The decode kernel launches sequences longest first.  When the plan splits some sequence
+of a batch of 16 to 1,024 sequences, a one-CTA pass lists the (sequence, split) items on
+the device, longest sequences first, and persistent CTAs take them in turn (the list sits
+at the start of the call's scratch, the split partial results after it).  Otherwise it
+ranks batches of up to 160 sequences inside every CTA, batches of 161 to 1,024 through a
+separate one-CTA ranking pass whose order sits at the start of the scratch, and keeps the
+index order above 1,024.  These cases reach each branch on
 both sides of its bounds, with skewed lengths (a few sequences far longer than the rest),
 q_len 1 and 4 mixed in one batch, sequences with fewer keys than queries (rows that attend
 nothing), a few prefill-class sequences in the same batch, and NaN in every cache slot
@@ -41,8 +44,36 @@ def skewed_layout(batch, seed, *, H=8, Hkv=2, D=128, P=32, long_n=3, long_k=2000
 
 @pytest.mark.parametrize("batch", [160, 161])
 def test_in_cta_ranking_bound(batch):
-    """160 sequences: ranked inside every CTA; 161: the first batch ranked by the separate pass."""
+    """160 and 161 sequences with a few long ones (split): the persistent work-list mode."""
     _gpu.check_layout(skewed_layout(batch, seed=31), limit=2048)
+
+
+@pytest.mark.parametrize("batch", [160, 161])
+def test_ranking_without_splits(batch):
+    """No sequence split (all under the split cap, more units than CTA slots): 160 ranked
+    inside every CTA, 161 by the separate ranking pass."""
+    _gpu.check_layout(skewed_layout(batch, seed=37, long_n=2, long_k=6000, short_hi=2000), limit=2048)
+
+
+def test_in_cta_ranking_with_splits_small_batch():
+    """Below 16 sequences the split plan keeps the grid of (split, kv head, rank) CTAs."""
+    _gpu.check_layout(skewed_layout(12, seed=38, long_n=2, long_k=30000, short_hi=700), limit=2048)
+
+
+def test_work_list_rows_without_keys_and_empty_sequences():
+    """Work-list mode with sequences whose rows attend nothing (fewer keys than queries, and
+    no keys at all) and sequences with no queries: every real row is written."""
+    rng = np.random.default_rng(39)
+    batch = 40
+    sk = rng.integers(1, 900, size=batch, endpoint=True)
+    sq = np.where(rng.random(batch) < 0.3, 4, 1)
+    sk[[3, 17]] = 25000  # split
+    sk[[5, 9]] = [2, 0]  # rows past the keys
+    sq[[5, 9]] = 4
+    sq[[11, 23]] = 0     # no queries
+    lay = workloads.make_layout("worklist_edges", "bf16", sq.tolist(), sk.tolist(), num_heads=8, num_heads_k=2,
+                                head_dim=128, page_block_size=32, seed=39, spare=0.05)
+    _gpu.check_layout(lay, limit=4096)
 
 
 def test_ranking_pass_group_of_eight_with_prefill_rows():
