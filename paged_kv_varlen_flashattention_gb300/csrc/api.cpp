@@ -594,7 +594,7 @@ int encode_tmap_4d(void* map, int dtype, const void* base, const uint64_t dims_[
 bool decode_tc_wanted(int dp) {
     // Opt-in (PA_DECODE_TC=1, read per call): on GB300 it measured below the warp-sliced
     // kernel at head dims 128 and 256 (0.50 / 0.73 of the copy peak against 0.93 / 0.91) and
-    // level with the general kernel at 512 (0.30 against 0.31).
+    // below the quarter-column kernel at 512 (0.30 against 0.54).
     const char* env = std::getenv("PA_DECODE_TC");
     return dp >= 128 && env && env[0] == '1';
 }
