@@ -170,10 +170,10 @@ def replica_throughput(work_per_rank, world, ms_max):
 
 def kernel_class_seqs(lay):
     """Sequences per kernel class, mirroring the library's dispatch: sequences with more
-    than 32 rows (sq * G) go to the tensor-core prefill kernel when it takes the call
-    (head_dim <= 128, G <= 128, softmax_scale > 0), the rest to the split-KV pass."""
+    than 32 rows (sq * G) go to the tensor-core prefill kernels when they take the call
+    (head_dim <= 256, G <= 128, softmax_scale > 0), the rest to the split-KV pass."""
     G = lay.num_heads // lay.num_heads_k
-    tc = (lay.head_dim <= 128 and G <= 128 and lay.softmax_scale > 0
+    tc = (lay.head_dim <= 256 and G <= 128 and lay.softmax_scale > 0
           and max(lay.seqlens_q) * G > 32 and not os.environ.get("PA_DISABLE_TC_PREFILL"))
     pre = [b for b in range(lay.batch) if tc and lay.seqlens_q[b] * G > 32]
     split = [b for b in range(lay.batch) if b not in set(pre)]
@@ -452,7 +452,8 @@ def kernel_names(lay):
     tc = dp >= 128 and os.environ.get("PA_DECODE_TC", "") == "1"
     dec = ("splitkv_kernel" if rows > 32 else "decode_tc_kernel" if tc else
            "decode_kernel" if dp <= 256 else "decode512_kernel")
-    return {"prefill": "prefill_kernel", "combine": "combine_kernel", "splitkv": dec}
+    return {"prefill": "prefill256_kernel" if lay.head_dim > 128 else "prefill_kernel", "combine": "combine_kernel",
+            "splitkv": dec}
 
 
 def roofline_of(binding, g, lay, steps, flush):

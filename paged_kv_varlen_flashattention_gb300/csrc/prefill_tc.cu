@@ -43,6 +43,8 @@ constexpr int kPrefillThreads = 384;  // three warpgroups
 constexpr int kRegsControl = 72, kRegsSoftmax = 216;
 
 struct PrefillParams {
+    const void* q;       // read by the head-dim-256 kernel (the others load q through a tensor map)
+    int64_t q_s0, q_s1;
     void* out;
     int64_t o_s0, o_s1;
     float* lse;
@@ -723,6 +725,596 @@ int run_prefill(const Args& a, const PrefillParams& pp, cudaStream_t stream, cha
     return PA_OK;
 }
 
+// ---------------------------------------------------------------------------------------------
+// Head dim 129..256: one 128-row query tile per CTA, q held in tensor memory.
+//
+// Two query tiles whose O takes 256 columns each would need more than the 512 TMEM columns,
+// and 128-key K/V stages (64 KB each) do not fit twice beside a 64 KB q tile in shared
+// memory.  So a CTA owns one query tile of one (sequence, kv head); the softmax warps write
+// its q rows into tensor memory once (lane = row, 128 columns of packed 16-bit pairs), and
+// Q K^T takes its A operand from there; K and V come in 64-key tiles (32 KB) through a
+// 4-deep K ring and a 3-deep V ring.  S is double-buffered over consecutive key tiles, so
+// the softmax of tile j runs while the tensor pipe computes P.V of tile j-1 and Q.K^T of
+// tile j+1.  TMEM columns: q [0,128), S0 [128,192), S1 [192,256), O [256,512).
+// Roles: warp 0 K producer, warp 2 V producer, warp 1 the MMA issuer (and TMEM owner),
+// warps 4..11 softmax (two warps per 32-lane TMEM quarter, 16 rows each).
+// The issuer runs S(0), S(1), PV(0), S(2), PV(1), S(3), ...: S(j+2) reuses the columns
+// P(j) was read from only after PV(j), in order on one thread.  The softmax releases K stage
+// j once S(j) is complete, waits for PV(j-1) (one commit per tile, waited in order) before it
+// hands over P(j) -- only then may it rescale O -- and releases V stage j-1 there.
+struct P2Cfg {
+    static constexpr int DP = 256, CH = 4, NT = 64;
+    static constexpr int KV_TILE = CH * NT * 128;  // 64 keys x 256 columns: 32 KB
+    static constexpr int KS = 4, VS = 3;
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = KS * KV_TILE;
+    static constexpr int OFF_BAR = OFF_V + VS * KV_TILE;
+    // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2], p_full[2], pv_done, drain
+    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 6;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag, picked tile
+    static constexpr int OFF_IDS = OFF_MISC + 16;
+    static constexpr int MAX_BOXES = 256;
+    static constexpr int SMEM = OFF_IDS + (MAX_BOXES + 4) * 4 + 1024;
+    static constexpr uint32_t T_Q = 0, T_S0 = 128, T_S1 = 192, T_O = 256;
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+// Issues the K (or V) boxes of the CTA's 64-key tile number `j` (first key kt0 + 64 j) into
+// `dst` (chunk-major: 64-column chunk c holds rows [64 c, 64 c + 64) of 128 bytes).
+__device__ __forceinline__ void issue_kv_tile64(const PrefillParams& p, const CUtensorMap* map, uint8_t* dst,
+                                                uint64_t* bar, const int* ids, int j, int hk, int kt0, int k0) {
+    const int kt = kt0 + j * 64;
+    int blk[2];
+    uint32_t bytes = 0;
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+        blk[jj] = jj < p.boxes_per_tile ? ids[j * p.boxes_per_tile + jj] : -1;
+        if (blk[jj] >= 0) bytes += (uint32_t)(P2Cfg::CH * p.box_rows * 128);
+    }
+    mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+        if (blk[jj] < 0) continue;
+        const int key = kt + jj * p.box_rows;
+        const int c2 = p.paged ? key - (key / p.P) * p.P : k0 + key;
+        const int c3 = p.paged ? blk[jj] : 0;
+        for (int c = 0; c < P2Cfg::CH; ++c)
+            tma_load_4d(dst + (c * 64 + jj * p.box_rows) * 128, map, bar, c * 64, hk, c2, c3, 0ull);
+    }
+}
+
+template <typename T, bool ALIBI>
+__global__ void __launch_bounds__(kPrefillThreads, 1)
+    prefill256_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                      const PrefillParams p) {
+    using C = P2Cfg;
+    constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int hk = blockIdx.y;
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* q_full = bars;
+    uint64_t* k_full = bars + 1;
+    uint64_t* k_empty = k_full + C::KS;
+    uint64_t* v_full = k_empty + C::KS;
+    uint64_t* v_empty = v_full + C::VS;
+    uint64_t* s_full = v_empty + C::VS;  // [S buffer]
+    uint64_t* p_full = s_full + 2;       // [S buffer]
+    uint64_t* pv_done = p_full + 2;      // one phase per key tile
+    uint64_t* drain = pv_done + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+    if (tid == 64) {
+        mbar_init(q_full, 8);  // one arrive per softmax warp: its q rows are in tensor memory
+        for (int s = 0; s < C::KS; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+        }
+        for (int s = 0; s < C::VS; ++s) {
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&s_full[x], 1);
+            mbar_init(&p_full[x], 8);
+        }
+        mbar_init(pv_done, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::tmem_relinquish();
+    }
+
+    // ---- which (sequence, query tile) this CTA owns: the blockIdx.x-th of all 128-row tiles of
+    // prefill-class sequences, sequence by sequence, each sequence's last tile first.
+    int* pick = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
+    const int qpt = 128 / p.G;    // whole queries per tile
+    const int trows = qpt * p.G;  // rows of the tile that hold queries (the rest are padding)
+    if (warp == 0) {
+        int remaining = (int)blockIdx.x, found_b = -1, found_u = 0;
+        for (int base = 0; base < p.batch && found_b < 0; base += 32) {
+            const int bb = base + lane;
+            int tiles = 0;
+            if (bb < p.batch) {
+                const int sqb = p.cu_q[bb + 1] - p.cu_q[bb];
+                tiles = (int64_t)sqb * p.G > p.rows_cap ? (sqb + qpt - 1) / qpt : 0;
+            }
+            int incl = tiles;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += v;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, remaining < incl);
+            if (hit) {
+                const int src = __ffs(hit) - 1;
+                const int excl = __shfl_sync(0xffffffffu, incl - tiles, src);
+                const int cnt = __shfl_sync(0xffffffffu, tiles, src);
+                found_b = base + src;
+                found_u = cnt - 1 - (remaining - excl);
+            } else {
+                remaining -= __shfl_sync(0xffffffffu, incl, 31);
+            }
+        }
+        if (lane == 0) {
+            pick[0] = found_b;
+            pick[1] = found_u;
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const int b = pick[0], u = pick[1];
+    auto leave = [&]() {  // every early exit below is uniform over the CTA
+        if (warp == 1) tc::tmem_dealloc(tmem, 512);
+    };
+    if (b < 0) {
+        leave();
+        return;
+    }
+    const int q0 = p.cu_q[b], q1 = p.cu_q[b + 1];
+    const int k0 = p.cu_k[b], k1 = p.cu_k[b + 1];
+    const int sq = q1 - q0, sk = k1 - k0;
+    if (sq < 0 || sk < 0 || sq > p.max_sq || sk > p.max_sk || q0 < 0 || q1 > p.total_q ||
+        (!p.paged && (k0 < 0 || k1 > p.num_blocks))) {
+        if (tid == 0) flag_error(p.err, PA_ERR_DEVICE_BOUNDS);
+        leave();
+        return;
+    }
+    const int64_t rows_total = (int64_t)sq * p.G;
+    const int i0 = u * qpt;  // first query of the tile
+    auto tile_rho = [&](int r) -> int64_t { return (int64_t)i0 * p.G + r; };
+    auto row_live = [&](int r) { return r < trows && tile_rho(r) < rows_total; };
+    const int i_last = min(sq - 1, i0 + qpt - 1);
+    const int64_t cdiag = (int64_t)sk - sq;
+    const int64_t lo = p.wl >= 0 ? max64(0, i0 + cdiag - p.wl) : 0;
+    const int64_t hi = p.wr >= 0 ? min64((int64_t)sk - 1, i_last + cdiag + p.wr) : (int64_t)sk - 1;
+    const int kt0 = hi >= lo ? (int)(lo & ~int64_t(63)) : 0;
+    const int n_tiles = hi >= lo ? (int)((hi - kt0) / 64 + 1) : 0;
+
+    T* out = static_cast<T*>(p.out);
+    if (n_tiles == 0) {  // no row of the tile attends any key: out = 0, lse = -inf
+        if (warp >= 4 && warp < 8) {
+            const int r = (warp & 3) * 32 + lane;
+            if (row_live(r)) {
+                const int64_t rho = tile_rho(r);
+                const int i = (int)(rho / p.G), g = (int)(rho - (int64_t)i * p.G);
+                const int64_t t = q0 + i;
+                const int h = hk * p.G + g;
+                for (int d = 0; d < p.D; d += 8)
+                    *reinterpret_cast<int4*>(out + t * p.o_s0 + (int64_t)h * p.o_s1 + d) = make_int4(0, 0, 0, 0);
+                p.lse[(int64_t)h * p.lse_s0 + t + (int64_t)b * p.lse_sb] = -INFINITY;
+            }
+        }
+        leave();
+        return;
+    }
+
+    if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
+    if (warp == 0 || warp == 2) {
+        // ---------------- TMA producers: warp 0 K tiles, warp 2 V tiles ----------------
+        int* ids = reinterpret_cast<int*>(smem + C::OFF_IDS);
+        const int n_boxes = min(n_tiles * p.boxes_per_tile, C::MAX_BOXES);
+        const int32_t* bt_row = p.paged ? p.bt + (int64_t)b * p.bt_s0 : nullptr;
+        if (warp == 0) {
+            for (int bi = lane; bi < n_boxes; bi += 32) {
+                const int key = kt0 + bi * p.box_rows;
+                ids[bi] = p.paged ? box_block(bt_row, p.bt_cols, p.num_blocks, p.P, key, sk, p.err)
+                                  : (key < sk ? 0 : -1);
+            }
+        }
+        named_barrier_sync(2, 64);  // warps 0 and 2: the staged ids are visible
+        const bool is_k = warp == 0;
+        if (lane == 0 && !p.withhold) {
+            const CUtensorMap* map = is_k ? &tm_k : &tm_v;
+            prefetch_tmap(map);
+            const int stages = is_k ? C::KS : C::VS;
+            uint64_t* fullb = is_k ? k_full : v_full;
+            uint64_t* emptyb = is_k ? k_empty : v_empty;
+            uint8_t* ring = smem + (is_k ? C::OFF_K : C::OFF_V);
+            int spill[2];  // block ids of one tile past the staged range
+            for (int j = 0; j < n_tiles; ++j) {
+                const int s = j % stages;
+                if (j >= stages && !wait_bar(&emptyb[s], ((j / stages) - 1) & 1, abort_flag, p.err, p.wait_ns))
+                    break;
+                const int* tile = ids;
+                int jt = j, kb = kt0;
+                if ((j + 1) * p.boxes_per_tile > C::MAX_BOXES) {
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const int key = kt0 + j * 64 + jj * p.box_rows;
+                        spill[jj] = jj >= p.boxes_per_tile ? -1
+                                    : p.paged ? box_block(bt_row, p.bt_cols, p.num_blocks, p.P, key, sk, p.err)
+                                              : (key < sk ? 0 : -1);
+                    }
+                    tile = spill;
+                    jt = 0;
+                    kb = kt0 + j * 64;
+                }
+                issue_kv_tile64(p, map, ring + s * C::KV_TILE, &fullb[s], tile, jt, hk, kb, k0);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        constexpr uint32_t IDESC_S = tc::idesc_f16(128, 64, kBF16, false, false);
+        constexpr uint32_t IDESC_O = tc::idesc_f16(128, 256, kBF16, false, true);
+        const uint64_t dk0 = tc::smem_desc_sw128(smem_addr(smem + C::OFF_K), 16, 1024);
+        const uint64_t dv0 = tc::smem_desc_sw128(smem_addr(smem + C::OFF_V), 64 * 128, 1024);
+        const uint32_t t_q = tmem + C::T_Q, t_o = tmem + C::T_O;
+        auto s_buf = [&](int j) { return tmem + ((j & 1) ? C::T_S1 : C::T_S0); };
+        auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+            const bool r = __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, p.err, p.wait_ns));
+            tc::fence_after_sync();
+            return r;
+        };
+        // S(j) = Q K_j^T into S buffer j % 2 (A: q in tensor memory, 8 columns per 16-column step)
+        auto issue_s = [&](int j) {
+            const uint64_t db = dk0 + (uint64_t)((j % C::KS) * (C::KV_TILE >> 4));
+#pragma unroll
+            for (int kk = 0; kk < C::DP / 16; ++kk) {
+                const uint64_t off = (uint64_t)((kk >> 2) * (64 * 128 / 16) + (kk & 3) * 2);
+                tc::mma_ts(s_buf(j), t_q + kk * 8, db + off, IDESC_S, kk > 0 ? 1u : 0u);
+            }
+            tc::commit(&s_full[j & 1]);
+        };
+        bool ok = wait_all(q_full, 0);
+        for (int j = 0; ok && j < 2 && j < n_tiles; ++j) {
+            if (!(ok = wait_all(&k_full[j], 0))) break;
+            if (lane == 0) issue_s(j);
+            __syncwarp();
+        }
+        for (int j = 0; ok && j < n_tiles; ++j) {
+            if (!(ok = wait_all(&v_full[j % C::VS], (j / C::VS) & 1))) break;
+            uint8_t* vst = smem + C::OFF_V + (j % C::VS) * C::KV_TILE;
+            const int valid = min(64, sk - (kt0 + j * 64));
+            if (valid < 64) {  // keys at or past sk: zero V rows so P = 0 never meets NaN
+                const int zr = 64 - valid;
+                for (int idx = lane; idx < C::CH * zr * 8; idx += 32) {
+                    const int c = idx / (zr * 8), rem = idx - c * zr * 8;
+                    *reinterpret_cast<int4*>(vst + (c * 64 + valid + (rem >> 3)) * 128 + ((rem & 7) << 4)) =
+                        make_int4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                tc::fence_after_sync();
+            }
+            const bool more = j + 2 < n_tiles;
+            if (more && !(ok = wait_all(&k_full[(j + 2) % C::KS], ((j + 2) / C::KS) & 1))) break;
+            if (!(ok = wait_all(&p_full[j & 1], (j >> 1) & 1))) break;
+            if (lane == 0) {
+                // O += P(j) V_j, P(j) in the first 32 columns of S buffer j % 2
+                const uint64_t db = dv0 + (uint64_t)((j % C::VS) * (C::KV_TILE >> 4));
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc::mma_ts(t_o, s_buf(j) + kk * 8, db + (uint64_t)(kk * (2048 / 16)), IDESC_O,
+                               kk > 0 ? 1u : (j > 0 ? 1u : 0u));
+                tc::commit(pv_done);
+                if (more) issue_s(j + 2);
+            }
+            __syncwarp();
+        }
+        // every MMA started has completed before tensor memory is released
+        if (lane == 0) {
+            tc::commit(drain);
+            mbar_wait(drain, 0, p.wait_ns);  // not cut short by an abort: MMAs may be in flight
+        }
+        __syncwarp();
+    }
+    } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    {
+        // ---------------- softmax: warps 4..11 ----------------
+        // Warp w reaches TMEM lanes 32 (w % 4) .. +31 and takes half hh = (w - 4) / 4 of them:
+        // lanes lb .. lb + 15, lb = 32 (w % 4) + 16 hh.  Thread t holds rows lb + t/4 (q = 0)
+        // and lb + t/4 + 8 (q = 1); the four threads of a quad split a row's 64 keys (keys
+        // 8k + 2 (t % 4) + {0, 1}, k = 0..7).
+        const int lg = warp & 3, hh = (warp - 4) >> 2;
+        const int gid = lane >> 2, tig = lane & 3;
+        const int lb = lg * 32 + hh * 16;
+        const uint32_t lane_addr = (uint32_t)lb << 16;
+
+        // q rows into tensor memory: warp (lg, hh) writes head-dim half hh (64 columns of
+        // packed pairs) of rows 32 lg .. 32 lg + 31, one row per thread (columns past D and
+        // rows without a query are zero)
+        {
+            const int r = lg * 32 + lane;
+            const T* q = static_cast<const T*>(p.q);
+            const bool live = row_live(r);
+            const int64_t rho = tile_rho(r);
+            const int i = live ? (int)(rho / p.G) : 0, g = live ? (int)(rho - (int64_t)i * p.G) : 0;
+            const T* src = q + (int64_t)(q0 + i) * p.q_s0 + (int64_t)(hk * p.G + g) * p.q_s1;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t w[32];
+#pragma unroll
+                for (int v4 = 0; v4 < 8; ++v4) {
+                    const int d = hh * 128 + half * 64 + v4 * 8;  // first of 8 elements
+                    int4 x = make_int4(0, 0, 0, 0);
+                    if (live && d < p.D) x = __ldg(reinterpret_cast<const int4*>(src + d));
+                    w[4 * v4] = (uint32_t)x.x;
+                    w[4 * v4 + 1] = (uint32_t)x.y;
+                    w[4 * v4 + 2] = (uint32_t)x.z;
+                    w[4 * v4 + 3] = (uint32_t)x.w;
+                }
+                tc::st_32x32b_x32(tmem + ((uint32_t)(lg * 32) << 16) + C::T_Q + hh * 64 + half * 32, w);
+            }
+            tc::wait_st();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_full);
+        }
+
+        int lo_r[2], hi_r[2], dg_r[2];
+        float ab_r[2], m_r[2], l_r[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int r = lb + gid + 8 * q;
+            lo_r[q] = 0;
+            hi_r[q] = -1;
+            dg_r[q] = 0;
+            ab_r[q] = 0.f;
+            if (row_live(r)) {
+                const int64_t rho = tile_rho(r);
+                const int64_t diag = rho / p.G + cdiag;
+                lo_r[q] = p.wl >= 0 ? (int)max64(0, diag - p.wl) : 0;
+                hi_r[q] = p.wr >= 0 ? (int)max64(-1, min64((int64_t)sk - 1, diag + p.wr)) : sk - 1;
+                if (ALIBI) {
+                    dg_r[q] = (int)diag;
+                    ab_r[q] = p.alibi[hk * p.G + (int)(rho - (rho / p.G) * p.G)] * kLog2e;
+                }
+            }
+            m_r[q] = -INFINITY;
+            l_r[q] = 0.f;
+        }
+        const uint32_t o_addr = tmem + lane_addr + C::T_O;
+
+        // One key tile: S -> running max -> P; O rescaled (rarely) once PV(j-1) is complete.
+        auto step = [&](int j) -> bool {
+            const int kt = kt0 + j * 64;
+            if (!__all_sync(0xffffffffu, wait_bar(&s_full[j & 1], (j >> 1) & 1, abort_flag, p.err, p.wait_ns)))
+                return false;
+            tc::fence_after_sync();
+            const uint32_t s_addr = tmem + lane_addr + ((j & 1) ? C::T_S1 : C::T_S0);
+            // sv[4k + 2q + e] = S[row q][key 8k + 2 tig + e]
+            float sv[32];
+            tc::ld_16x256b_x8(s_addr, sv);
+            if (warp == 4 && lane == 0) mbar_arrive(&k_empty[j % C::KS]);  // S(j) is complete: K stage j is free
+            tc::wait_ld();
+            if (!(kt >= max(lo_r[0], lo_r[1]) && kt + 63 <= min(hi_r[0], hi_r[1]))) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+#pragma unroll
+                    for (int q = 0; q < 2; ++q)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int key = kt + 8 * k + 2 * tig + e;
+                            float& v = sv[4 * k + 2 * q + e];
+                            v = (key >= lo_r[q] && key <= hi_r[q]) ? v : -INFINITY;
+                        }
+            }
+            float sl = p.scale_log2;  // softmax_scale > 0 on this path
+            if (ALIBI) {
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const float d0 = (float)(dg_r[q] - kt - 2 * tig);  // distance of key kt + 2 tig
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            float& v = sv[4 * k + 2 * q + e];
+                            v = fmaf(-ab_r[q], fabsf(d0 - (float)(8 * k + e)), v * sl);
+                        }
+                }
+                sl = 1.f;
+            }
+            // running max with the lazy rescale of the 128-key kernel: exact row maxima and
+            // an O rescale only when some row of the warp grew by more than 2^8
+            float lm[2];
+            bool grow = false;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                float c0 = fmaxf(sv[2 * q], sv[2 * q + 1]), c1 = fmaxf(sv[4 + 2 * q], sv[5 + 2 * q]);
+#pragma unroll
+                for (int k = 2; k < 8; k += 2) {
+                    c0 = max3f(c0, sv[4 * k + 2 * q], sv[4 * k + 2 * q + 1]);
+                    c1 = max3f(c1, sv[4 * k + 4 + 2 * q], sv[4 * k + 5 + 2 * q]);
+                }
+                lm[q] = fmaxf(c0, c1);
+                grow |= lm[q] * sl > m_r[q] + 8.f;
+            }
+            float alpha[2] = {1.f, 1.f};
+            bool resc = false;
+            if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    float mx = lm[q];
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                    const float m_cand = mx * sl;
+                    if (m_cand > m_r[q] + 8.f) {
+                        alpha[q] = fast_exp2(m_r[q] - m_cand);
+                        m_r[q] = m_cand;
+                        resc = true;
+                    }
+                }
+            }
+            float nm[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) nm[q] = m_r[q] == -INFINITY ? 0.f : -m_r[q];
+            float sums[4] = {0.f, 0.f, 0.f, 0.f};
+            // pk[2k + q] = P[row q][packed column 4k + tig] = (keys 8k + 2 tig, +1)
+            uint32_t pk[16];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    float x0, x1;
+                    ffma2(x0, x1, sv[4 * k + 2 * q], sv[4 * k + 2 * q + 1], sl, sl, nm[q], nm[q]);
+                    const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                    fadd2_acc(sums[2 * q], sums[2 * q + 1], p0, p1);
+                    pk[2 * k + q] = pack2<T>(p0, p1);
+                }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) l_r[q] = l_r[q] * alpha[q] + (sums[2 * q] + sums[2 * q + 1]);
+            if (j > 0) {
+                // PV(j-1) complete: O holds every earlier tile, V stage j-1 is free
+                if (!__all_sync(0xffffffffu, wait_bar(pv_done, (j - 1) & 1, abort_flag, p.err, p.wait_ns)))
+                    return false;
+                tc::fence_after_sync();
+                if (warp == 4 && lane == 0) mbar_arrive(&v_empty[(j - 1) % C::VS]);
+                if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+                    for (int cc = 0; cc < C::DP / 64; ++cc) {
+                        float o[32];
+                        tc::ld_16x256b_x8(o_addr + cc * 64, o);
+                        tc::wait_ld();
+                        uint32_t ob[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) ob[e] = __float_as_uint(o[e] * alpha[(e >> 1) & 1]);
+                        tc::st_16x256b_x8(o_addr + cc * 64, ob);
+                    }
+                }
+            }
+            // P overwrites the first 32 columns of the S it came from (this thread's own cells)
+            tc::st_16x128b_x8(s_addr, pk);
+            tc::wait_st();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[j & 1]);
+            return true;
+        };
+
+        bool ok = true;
+        for (int j = 0; ok && j < n_tiles; ++j) ok = step(j);
+        if (ok && __all_sync(0xffffffffu, wait_bar(pv_done, (n_tiles - 1) & 1, abort_flag, p.err, p.wait_ns))) {
+            tc::fence_after_sync();
+            float inv[2];
+            T* orow[2];
+            bool valid[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                float l = l_r[q];
+                l += __shfl_xor_sync(0xffffffffu, l, 1);
+                l += __shfl_xor_sync(0xffffffffu, l, 2);
+                inv[q] = l > 0.f ? 1.f / l : 0.f;
+                const int r = lb + gid + 8 * q;
+                const int64_t rho = tile_rho(r);
+                valid[q] = row_live(r);
+                const int i = (int)(rho / p.G), g = (int)(rho - (int64_t)i * p.G);
+                const int64_t t = q0 + i;
+                const int h = hk * p.G + g;
+                orow[q] = out + t * p.o_s0 + (int64_t)h * p.o_s1;
+                if (valid[q] && tig == 0)
+                    p.lse[(int64_t)h * p.lse_s0 + t + (int64_t)b * p.lse_sb] =
+                        l > 0.f ? (m_r[q] + log2f(l)) * 0.69314718055994531f : -INFINITY;
+            }
+#pragma unroll 1
+            for (int cc = 0; cc < C::DP / 64; ++cc) {
+                float o[32];
+                tc::ld_16x256b_x8(o_addr + cc * 64, o);
+                tc::wait_ld();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int d = cc * 64 + 8 * k + 2 * tig;
+#pragma unroll
+                    for (int q = 0; q < 2; ++q)
+                        if (valid[q] && d < p.D)
+                            *reinterpret_cast<uint32_t*>(orow[q] + d) =
+                                pack2<T>(o[4 * k + 2 * q] * inv[q], o[4 * k + 2 * q + 1] * inv[q]);
+                }
+            }
+        }
+        tc::fence_before_sync();
+    }
+    }
+    __syncwarp();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+template <typename T, bool ALIBI>
+int run_prefill256(const Args& a, const PrefillParams& pp, cudaStream_t stream, char* msg, size_t msg_len) {
+    using C = P2Cfg;
+    CUtensorMap tk, tv;
+    {
+        uint64_t dims[4], strides[3];
+        if (a.paged) {
+            dims[0] = (uint64_t)a.D;
+            dims[1] = (uint64_t)a.Hkv;
+            dims[2] = (uint64_t)a.page;
+            dims[3] = (uint64_t)a.num_blocks;
+            strides[0] = (uint64_t)a.kv_s2 * 2;
+            strides[1] = (uint64_t)a.kv_s1 * 2;
+            strides[2] = (uint64_t)a.kv_s0 * 2;
+        } else {
+            dims[0] = (uint64_t)a.D;
+            dims[1] = (uint64_t)a.Hkv;
+            dims[2] = (uint64_t)(a.num_blocks > 0 ? a.num_blocks : 1);
+            dims[3] = 1;
+            strides[0] = (uint64_t)a.kv_s2 * 2;
+            strides[1] = (uint64_t)a.kv_s0 * 2;
+            strides[2] = (uint64_t)a.kv_s0 * 2 * dims[2];
+        }
+        const uint32_t box[4] = {64u, 1u, (uint32_t)pp.box_rows, 1u};
+        int rc = encode_tmap_4d(&tk, a.dtype, a.k, dims, strides, box, 1, msg, msg_len);
+        if (rc != PA_OK) return rc;
+        rc = encode_tmap_4d(&tv, a.dtype, a.v, dims, strides, box, 1, msg, msg_len);
+        if (rc != PA_OK) return rc;
+    }
+    auto kern = prefill256_kernel<T, ALIBI>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) {
+            snprintf(msg, msg_len, "cudaFuncSetAttribute(prefill256, %d bytes): %s", C::SMEM, cudaGetErrorString(e));
+            return PA_ERR_CUDA;
+        }
+        configured = true;
+    }
+    dim3 grid(pp.pairs, a.Hkv, 1);
+    NvtxRange nv("pa::prefill256_kernel");
+    timer_begin(PA_KC_PREFILL, stream);
+    kern<<<grid, kPrefillThreads, C::SMEM, stream>>>(tk, tv, pp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        snprintf(msg, msg_len, "prefill256 launch: %s", cudaGetErrorString(e));
+        return PA_ERR_CUDA;
+    }
+    timer_end(PA_KC_PREFILL, stream);
+    count_launches(1);
+    return PA_OK;
+}
+
 }  // namespace
 
 int prefill_rows_threshold() { return 32; }
@@ -731,15 +1323,20 @@ bool prefill_supported(const Args& a) {
     static const bool disabled = std::getenv("PA_DISABLE_TC_PREFILL") != nullptr;
     if (disabled) return false;
     const int G = a.H / a.Hkv;
-    if (a.D > 128 || G > 128) return false;
+    if (a.D > 256 || G > 128) return false;
     if (!(a.scale > 0.f)) return false;
     if ((int64_t)a.max_sq * G <= prefill_rows_threshold()) return false;  // nothing for it to do
     if (a.total_q <= 0 || a.q_s1 * 2 % 16 != 0 || a.q_s0 * 2 % 16 != 0) return false;
+    // the head-dim-256 kernel reads q rows with 16-byte loads (the others through a tensor map)
+    if (a.D > 128 && reinterpret_cast<uintptr_t>(a.q) % 16 != 0) return false;
     return true;
 }
 
 int launch_prefill(const Args& a, unsigned int* err, char* msg, size_t msg_len) {
     PrefillParams pp{};
+    pp.q = a.q;
+    pp.q_s0 = a.q_s0;
+    pp.q_s1 = a.q_s1;
     pp.out = a.out;
     pp.o_s0 = a.o_s0;
     pp.o_s1 = a.o_s1;
@@ -781,8 +1378,21 @@ int launch_prefill(const Args& a, unsigned int* err, char* msg, size_t msg_len) 
     pp.err = err;
     pp.wait_ns = a.wait_ns;
     pp.withhold = a.withhold_loads;
-    const int dp = a.D <= 64 ? 64 : 128;
     const bool alibi = a.alibi != nullptr;
+    if (a.D > 128) {  // one 128-row query tile per CTA, 64-key K/V tiles
+        pp.box_rows = a.paged ? (a.page % 64 == 0 ? 64 : 32) : 64;
+        pp.boxes_per_tile = 64 / pp.box_rows;
+        // upper bound of the number of tiles: sum_b ceil(sq_b / qpt) <= ceil(total_q / qpt) + batch
+        const int64_t qpt = 128 / pp.G;
+        pp.pairs = (int)std::min<int64_t>(((int64_t)a.total_q + qpt - 1) / qpt + a.batch,
+                                          (int64_t)a.batch * (((int64_t)a.max_sq + qpt - 1) / qpt));
+        if (a.dtype == PA_BF16)
+            return alibi ? run_prefill256<__nv_bfloat16, true>(a, pp, a.stream, msg, msg_len)
+                         : run_prefill256<__nv_bfloat16, false>(a, pp, a.stream, msg, msg_len);
+        return alibi ? run_prefill256<__half, true>(a, pp, a.stream, msg, msg_len)
+                     : run_prefill256<__half, false>(a, pp, a.stream, msg, msg_len);
+    }
+    const int dp = a.D <= 64 ? 64 : 128;
     if (a.dtype == PA_BF16) {
         if (alibi)
             return dp == 64 ? run_prefill<__nv_bfloat16, 64, true>(a, pp, a.stream, msg, msg_len)

@@ -152,6 +152,15 @@ __device__ __forceinline__ void st_16x128b_x16(uint32_t taddr, const uint32_t (&
     asm volatile("tcgen05.st.sync.aligned.16x128b.x16.b32 [%0], " PA_OPS32_FROM1 ";" ::"r"(taddr), PA_R32(r)
                  : "memory");
 }
+// 16 lanes x 32 columns
+__device__ __forceinline__ void st_16x128b_x8(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x128b.x8.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
 // 32 lanes x 32 columns (thread t holds lane base + t, register i = column i), as ld_32cols
 // with the result as raw words; and the 16-column form of the same shape.
 __device__ __forceinline__ void ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
