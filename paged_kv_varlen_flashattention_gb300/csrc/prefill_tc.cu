@@ -736,12 +736,17 @@ int run_prefill(const Args& a, const PrefillParams& pp, cudaStream_t stream, cha
 // 4-deep K ring and a 3-deep V ring.  S is double-buffered over consecutive key tiles, so
 // the softmax of tile j runs while the tensor pipe computes P.V of tile j-1 and Q.K^T of
 // tile j+1.  TMEM columns: q [0,128), S0 [128,192), S1 [192,256), O [256,512).
-// Roles: warp 0 K producer, warp 2 V producer, warp 1 the MMA issuer (and TMEM owner),
-// warps 4..11 softmax (two warps per 32-lane TMEM quarter, 16 rows each).
-// The issuer runs S(0), S(1), PV(0), S(2), PV(1), S(3), ...: S(j+2) reuses the columns
-// P(j) was read from only after PV(j), in order on one thread.  The softmax releases K stage
-// j once S(j) is complete, waits for PV(j-1) (one commit per tile, waited in order) before it
-// hands over P(j) -- only then may it rescale O -- and releases V stage j-1 there.
+// Roles: warp 0 K producer, warp 2 V producer, warp 1 the Q.K^T issuer (and TMEM owner),
+// warp 3 the P.V issuer, warps 4..11 softmax (two warps per 32-lane TMEM quarter, 16 rows
+// each).  A 128x64x16 product keeps the tensor pipe ~32 cycles and costs its issuing thread
+// about twice that, so one thread issuing both products of a tile bounded the kernel
+// (40 % tensor-pipe activity, 935 TFLOP/s); two issuers share the work.  The P.V issuer
+// commits PV(j) to buf_free[j % 2]; the Q.K^T issuer waits for it before S(j+2) reuses the
+// columns P(j) was read from, and the softmax waits for PV(j-1) there before it hands over
+// P(j) -- only then may it rescale O -- and releases V stage j-1.  Each waiter takes a
+// buffer's phases in order, and the next phase of a buffer needs work the waiter has not yet
+// released, so no wait can see a barrier two phases ahead.  The softmax releases K stage j
+// once S(j) is complete.
 struct P2Cfg {
     static constexpr int DP = 256, CH = 4, NT = 64;
     static constexpr int KV_TILE = CH * NT * 128;  // 64 keys x 256 columns: 32 KB
@@ -749,8 +754,9 @@ struct P2Cfg {
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = KS * KV_TILE;
     static constexpr int OFF_BAR = OFF_V + VS * KV_TILE;
-    // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2], p_full[2], pv_done, drain
-    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 6;
+    // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2], p_full[2], buf_free[2],
+    // drain[2]
+    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 8;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag, picked tile
     static constexpr int OFF_IDS = OFF_MISC + 16;
     static constexpr int MAX_BOXES = 256;
@@ -802,8 +808,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     uint64_t* v_empty = v_full + C::VS;
     uint64_t* s_full = v_empty + C::VS;  // [S buffer]
     uint64_t* p_full = s_full + 2;       // [S buffer]
-    uint64_t* pv_done = p_full + 2;      // one phase per key tile
-    uint64_t* drain = pv_done + 1;
+    uint64_t* buf_free = p_full + 2;     // [S buffer]: the P.V that read it has completed
+    uint64_t* drain = buf_free + 2;      // [issuer]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile uint32_t* abort_flag = tmem_slot + 1;
     if (tid == 64) {
@@ -819,9 +825,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         for (int x = 0; x < 2; ++x) {
             mbar_init(&s_full[x], 1);
             mbar_init(&p_full[x], 8);
+            mbar_init(&buf_free[x], 1);
+            mbar_init(&drain[x], 1);
         }
-        mbar_init(pv_done, 1);
-        mbar_init(drain, 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -961,69 +967,73 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 issue_kv_tile64(p, map, ring + s * C::KV_TILE, &fullb[s], tile, jt, hk, kb, k0);
             }
         }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
+    } else {
+        // ---------------- MMA issuers: warp 1 Q.K^T, warp 3 P.V ----------------
         constexpr uint32_t IDESC_S = tc::idesc_f16(128, 64, kBF16, false, false);
         constexpr uint32_t IDESC_O = tc::idesc_f16(128, 256, kBF16, false, true);
-        const uint64_t dk0 = tc::smem_desc_sw128(smem_addr(smem + C::OFF_K), 16, 1024);
-        const uint64_t dv0 = tc::smem_desc_sw128(smem_addr(smem + C::OFF_V), 64 * 128, 1024);
-        const uint32_t t_q = tmem + C::T_Q, t_o = tmem + C::T_O;
+        const bool s_issuer = warp == 1;
         auto s_buf = [&](int j) { return tmem + ((j & 1) ? C::T_S1 : C::T_S0); };
         auto wait_all = [&](uint64_t* bar, uint32_t parity) {
             const bool r = __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, p.err, p.wait_ns));
             tc::fence_after_sync();
             return r;
         };
-        // S(j) = Q K_j^T into S buffer j % 2 (A: q in tensor memory, 8 columns per 16-column step)
-        auto issue_s = [&](int j) {
-            const uint64_t db = dk0 + (uint64_t)((j % C::KS) * (C::KV_TILE >> 4));
+        if (s_issuer) {
+            // S(j) = Q K_j^T into S buffer j % 2 (A: q in tensor memory, 8 columns per 16-column step)
+            const uint64_t dk0 = tc::smem_desc_sw128(smem_addr(smem + C::OFF_K), 16, 1024);
+            const uint32_t t_q = tmem + C::T_Q;
+            bool ok = wait_all(q_full, 0);
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                if (j >= 2 && !(ok = wait_all(&buf_free[j & 1], ((j - 2) >> 1) & 1))) break;
+                if (!(ok = wait_all(&k_full[j % C::KS], (j / C::KS) & 1))) break;
+                if (lane == 0) {
+                    const uint64_t db = dk0 + (uint64_t)((j % C::KS) * (C::KV_TILE >> 4));
 #pragma unroll
-            for (int kk = 0; kk < C::DP / 16; ++kk) {
-                const uint64_t off = (uint64_t)((kk >> 2) * (64 * 128 / 16) + (kk & 3) * 2);
-                tc::mma_ts(s_buf(j), t_q + kk * 8, db + off, IDESC_S, kk > 0 ? 1u : 0u);
-            }
-            tc::commit(&s_full[j & 1]);
-        };
-        bool ok = wait_all(q_full, 0);
-        for (int j = 0; ok && j < 2 && j < n_tiles; ++j) {
-            if (!(ok = wait_all(&k_full[j], 0))) break;
-            if (lane == 0) issue_s(j);
-            __syncwarp();
-        }
-        for (int j = 0; ok && j < n_tiles; ++j) {
-            if (!(ok = wait_all(&v_full[j % C::VS], (j / C::VS) & 1))) break;
-            uint8_t* vst = smem + C::OFF_V + (j % C::VS) * C::KV_TILE;
-            const int valid = min(64, sk - (kt0 + j * 64));
-            if (valid < 64) {  // keys at or past sk: zero V rows so P = 0 never meets NaN
-                const int zr = 64 - valid;
-                for (int idx = lane; idx < C::CH * zr * 8; idx += 32) {
-                    const int c = idx / (zr * 8), rem = idx - c * zr * 8;
-                    *reinterpret_cast<int4*>(vst + (c * 64 + valid + (rem >> 3)) * 128 + ((rem & 7) << 4)) =
-                        make_int4(0, 0, 0, 0);
+                    for (int kk = 0; kk < C::DP / 16; ++kk) {
+                        const uint64_t off = (uint64_t)((kk >> 2) * (64 * 128 / 16) + (kk & 3) * 2);
+                        tc::mma_ts(s_buf(j), t_q + kk * 8, db + off, IDESC_S, kk > 0 ? 1u : 0u);
+                    }
+                    tc::commit(&s_full[j & 1]);
                 }
-                fence_proxy_async_smem();
                 __syncwarp();
-                tc::fence_after_sync();
             }
-            const bool more = j + 2 < n_tiles;
-            if (more && !(ok = wait_all(&k_full[(j + 2) % C::KS], ((j + 2) / C::KS) & 1))) break;
-            if (!(ok = wait_all(&p_full[j & 1], (j >> 1) & 1))) break;
-            if (lane == 0) {
-                // O += P(j) V_j, P(j) in the first 32 columns of S buffer j % 2
-                const uint64_t db = dv0 + (uint64_t)((j % C::VS) * (C::KV_TILE >> 4));
+        } else {
+            // O += P(j) V_j, P(j) in the first 32 columns of S buffer j % 2
+            const uint64_t dv0 = tc::smem_desc_sw128(smem_addr(smem + C::OFF_V), 64 * 128, 1024);
+            const uint32_t t_o = tmem + C::T_O;
+            bool ok = true;
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                if (!(ok = wait_all(&v_full[j % C::VS], (j / C::VS) & 1))) break;
+                uint8_t* vst = smem + C::OFF_V + (j % C::VS) * C::KV_TILE;
+                const int valid = min(64, sk - (kt0 + j * 64));
+                if (valid < 64) {  // keys at or past sk: zero V rows so P = 0 never meets NaN
+                    const int zr = 64 - valid;
+                    for (int idx = lane; idx < C::CH * zr * 8; idx += 32) {
+                        const int c = idx / (zr * 8), rem = idx - c * zr * 8;
+                        *reinterpret_cast<int4*>(vst + (c * 64 + valid + (rem >> 3)) * 128 + ((rem & 7) << 4)) =
+                            make_int4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    tc::fence_after_sync();
+                }
+                if (!(ok = wait_all(&p_full[j & 1], (j >> 1) & 1))) break;
+                if (lane == 0) {
+                    const uint64_t db = dv0 + (uint64_t)((j % C::VS) * (C::KV_TILE >> 4));
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    tc::mma_ts(t_o, s_buf(j) + kk * 8, db + (uint64_t)(kk * (2048 / 16)), IDESC_O,
-                               kk > 0 ? 1u : (j > 0 ? 1u : 0u));
-                tc::commit(pv_done);
-                if (more) issue_s(j + 2);
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc::mma_ts(t_o, s_buf(j) + kk * 8, db + (uint64_t)(kk * (2048 / 16)), IDESC_O,
+                                   kk > 0 ? 1u : (j > 0 ? 1u : 0u));
+                    tc::commit(&buf_free[j & 1]);
+                }
+                __syncwarp();
             }
-            __syncwarp();
         }
-        // every MMA started has completed before tensor memory is released
+        // every MMA this issuer started has completed before tensor memory is released
         if (lane == 0) {
-            tc::commit(drain);
-            mbar_wait(drain, 0, p.wait_ns);  // not cut short by an abort: MMAs may be in flight
+            uint64_t* d = &drain[s_issuer ? 0 : 1];
+            tc::commit(d);
+            mbar_wait(d, 0, p.wait_ns);  // not cut short by an abort: MMAs may be in flight
         }
         __syncwarp();
     }
@@ -1185,7 +1195,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             for (int q = 0; q < 2; ++q) l_r[q] = l_r[q] * alpha[q] + (sums[2 * q] + sums[2 * q + 1]);
             if (j > 0) {
                 // PV(j-1) complete: O holds every earlier tile, V stage j-1 is free
-                if (!__all_sync(0xffffffffu, wait_bar(pv_done, (j - 1) & 1, abort_flag, p.err, p.wait_ns)))
+                if (!__all_sync(0xffffffffu,
+                                wait_bar(&buf_free[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.err, p.wait_ns)))
                     return false;
                 tc::fence_after_sync();
                 if (warp == 4 && lane == 0) mbar_arrive(&v_empty[(j - 1) % C::VS]);
@@ -1213,7 +1224,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
         bool ok = true;
         for (int j = 0; ok && j < n_tiles; ++j) ok = step(j);
-        if (ok && __all_sync(0xffffffffu, wait_bar(pv_done, (n_tiles - 1) & 1, abort_flag, p.err, p.wait_ns))) {
+        if (ok && __all_sync(0xffffffffu, wait_bar(&buf_free[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, abort_flag,
+                                                   p.err, p.wait_ns))) {
             tc::fence_after_sync();
             float inv[2];
             T* orow[2];
