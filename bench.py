@@ -41,9 +41,9 @@ NOMINAL_HBM_GBS = 7900.0
 NOMINAL_BF16_TFLOPS = 2250.0
 L2_BYTES = 129 * 1024 * 1024
 # the serving workloads measured beside the headline (chunked prefill + decode with a window,
-# long-context split-KV decode at head_dim 256 and 512, and the decode batch with one sequence
-# far longer than the rest)
-EXTRA_WORKLOADS = ("mixed_bf16", "long_bf16", "long_d512_bf16", "skewed_decode_bf16")
+# long-context split-KV decode at head_dim 256 and 512, the decode batch with one sequence
+# far longer than the rest, and the causal prefill batch at head_dim 256)
+EXTRA_WORKLOADS = ("mixed_bf16", "long_bf16", "long_d512_bf16", "skewed_decode_bf16", "prefill_d256_bf16")
 
 
 # ---- algorithmic work (closed form per query row) -----------------------------------------

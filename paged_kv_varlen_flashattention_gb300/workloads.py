@@ -137,6 +137,15 @@ def prefill_bf16(batch=8, lo=1024, hi=8192, seed=3) -> Layout:
                        head_dim=128, page_block_size=64, seed=seed)
 
 
+def prefill_d256_bf16(batch=8, lo=1024, hi=8192, seed=3) -> Layout:
+    """The causal prefill batch at head_dim 256: 8 sequences, sq = sk ~ U[1024, 8192];
+    H=16, Hkv=4, D=256, P=64; exact pool."""
+    rng = np.random.default_rng(seed)
+    s = rng.integers(lo, hi, size=batch, endpoint=True)
+    return make_layout("prefill_d256_bf16", "bf16", s, s, num_heads=16, num_heads_k=4,
+                       head_dim=256, page_block_size=64, seed=seed)
+
+
 def mixed_bf16(n_chunks=4, chunk=512, ctx_lo=2048, ctx_hi=16384, n_decode=120, dec_lo=256,
                dec_hi=32768, seed=4) -> Layout:
     """4 chunked-prefill sequences (512 queries over 2048-16384 cached keys) then 120
@@ -179,6 +188,7 @@ CONFIGS = {
     "tiny_fp16": tiny_fp16,
     "decode_bf16": decode_bf16,
     "prefill_bf16": prefill_bf16,
+    "prefill_d256_bf16": prefill_d256_bf16,
     "mixed_bf16": mixed_bf16,
     "long_bf16": long_bf16,
     "long_d512_bf16": long_d512_bf16,

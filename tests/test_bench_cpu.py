@@ -26,7 +26,8 @@ def test_flush_decision_and_labels():
     assert "flushed" in bench.l2_label(small) and "no flush" in bench.l2_label(large)
     assert not bench.L2Flush(large)  # large pools: no buffer, calls timed back to back
     for name, flushed in [("decode_bf16", False), ("long_bf16", False), ("mixed_bf16", False),
-                          ("prefill_bf16", True), ("long_d512_bf16", True), ("skewed_decode_bf16", False)]:
+                          ("prefill_bf16", True), ("long_d512_bf16", True), ("skewed_decode_bf16", False),
+                          ("prefill_d256_bf16", True)]:
         lay = workloads.CONFIGS[name]()
         assert (bench.pool_bytes(lay) <= 2 * bench.L2_BYTES) == flushed, name
 
