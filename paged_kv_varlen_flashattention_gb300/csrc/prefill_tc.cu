@@ -43,8 +43,6 @@ constexpr int kPrefillThreads = 384;  // three warpgroups
 constexpr int kRegsControl = 72, kRegsSoftmax = 216;
 
 struct PrefillParams {
-    const void* q;       // read by the head-dim-256 kernel (the others load q through a tensor map)
-    int64_t q_s0, q_s1;
     void* out;
     int64_t o_s0, o_s1;
     float* lse;
@@ -730,38 +728,40 @@ int run_prefill(const Args& a, const PrefillParams& pp, cudaStream_t stream, cha
 //
 // Two query tiles whose O takes 256 columns each would need more than the 512 TMEM columns,
 // and 128-key K/V stages (64 KB each) do not fit twice beside a 64 KB q tile in shared
-// memory.  So a CTA owns one query tile of one (sequence, kv head); the softmax warps write
-// its q rows into tensor memory once (lane = row, 128 columns of packed 16-bit pairs), and
-// Q K^T takes its A operand from there; K and V come in 64-key tiles (32 KB) through a
-// 4-deep K ring and a 3-deep V ring.  S is double-buffered over consecutive key tiles, so
-// the softmax of tile j runs while the tensor pipe computes P.V of tile j-1 and Q.K^T of
-// tile j+1.  TMEM columns: q [0,128), S0 [128,192), S1 [192,256), O [256,512).
+// memory.  So a CTA owns one query tile of one (sequence, kv head) (q by TMA into shared
+// memory, 64 KB); K and V come in 64-key tiles (32 KB) through a 3-deep K ring and a 2-deep
+// V ring.  S is quadruple-buffered over consecutive key tiles (64 columns each), so the
+// Q.K^T issuer runs up to three tiles ahead of the softmax while the pipe also computes P.V.
+// TMEM columns: S0..S3 [0,256), O [256,512).  (With q in tensor memory and two S buffers
+// the chain P.V(j) -> Q.K^T(j+2) -> softmax(j+2) bounded the kernel at ~1,950 cycles a tile.)
 // Roles: warp 0 K producer, warp 2 V producer, warp 1 the Q.K^T issuer (and TMEM owner),
 // warp 3 the P.V issuer, warps 4..11 softmax (two warps per 32-lane TMEM quarter, 16 rows
 // each).  A 128x64x16 product keeps the tensor pipe ~32 cycles and costs its issuing thread
 // about twice that, so one thread issuing both products of a tile bounded the kernel
 // (40 % tensor-pipe activity, 935 TFLOP/s); two issuers share the work.  The P.V issuer
-// commits PV(j) to buf_free[j % 2]; the Q.K^T issuer waits for it before S(j+2) reuses the
+// commits PV(j) to buf_free[j % 4]; the Q.K^T issuer waits for it before S(j+4) reuses the
 // columns P(j) was read from, and the softmax waits for PV(j-1) there before it hands over
 // P(j) -- only then may it rescale O -- and releases V stage j-1.  Each waiter takes a
 // buffer's phases in order, and the next phase of a buffer needs work the waiter has not yet
 // released, so no wait can see a barrier two phases ahead.  The softmax releases K stage j
 // once S(j) is complete.
 struct P2Cfg {
-    static constexpr int DP = 256, CH = 4, NT = 64;
+    static constexpr int DP = 256, CH = 4, NT = 64, NSB = 4;  // NSB: S buffers
+    static constexpr int Q_TILE = CH * 128 * 128;  // one 128-row q tile: 64 KB
     static constexpr int KV_TILE = CH * NT * 128;  // 64 keys x 256 columns: 32 KB
-    static constexpr int KS = 4, VS = 3;
-    static constexpr int OFF_K = 0;
-    static constexpr int OFF_V = KS * KV_TILE;
+    static constexpr int KS = 3, VS = 2;
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = Q_TILE;
+    static constexpr int OFF_V = OFF_K + KS * KV_TILE;
     static constexpr int OFF_BAR = OFF_V + VS * KV_TILE;
-    // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2], p_full[2], buf_free[2],
-    // drain[2]
-    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 8;
+    // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[NSB], p_full[NSB],
+    // buf_free[NSB], drain[2]
+    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 3 * NSB + 2;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag, picked tile
     static constexpr int OFF_IDS = OFF_MISC + 16;
     static constexpr int MAX_BOXES = 256;
     static constexpr int SMEM = OFF_IDS + (MAX_BOXES + 4) * 4 + 1024;
-    static constexpr uint32_t T_Q = 0, T_S0 = 128, T_S1 = 192, T_O = 256;
+    static constexpr uint32_t T_S = 0, T_O = 256;  // S buffer x at T_S + 64 x
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
@@ -791,8 +791,8 @@ __device__ __forceinline__ void issue_kv_tile64(const PrefillParams& p, const CU
 
 template <typename T, bool ALIBI>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
-    prefill256_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                      const PrefillParams p) {
+    prefill256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
     using C = P2Cfg;
     constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
     extern __shared__ uint8_t smem_raw[];
@@ -806,14 +806,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     uint64_t* k_empty = k_full + C::KS;
     uint64_t* v_full = k_empty + C::KS;
     uint64_t* v_empty = v_full + C::VS;
-    uint64_t* s_full = v_empty + C::VS;  // [S buffer]
-    uint64_t* p_full = s_full + 2;       // [S buffer]
-    uint64_t* buf_free = p_full + 2;     // [S buffer]: the P.V that read it has completed
-    uint64_t* drain = buf_free + 2;      // [issuer]
+    uint64_t* s_full = v_empty + C::VS;     // [S buffer]
+    uint64_t* p_full = s_full + C::NSB;     // [S buffer]
+    uint64_t* buf_free = p_full + C::NSB;   // [S buffer]: the P.V that read it has completed
+    uint64_t* drain = buf_free + C::NSB;    // [issuer]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile uint32_t* abort_flag = tmem_slot + 1;
     if (tid == 64) {
-        mbar_init(q_full, 8);  // one arrive per softmax warp: its q rows are in tensor memory
+        mbar_init(q_full, 1);
         for (int s = 0; s < C::KS; ++s) {
             mbar_init(&k_full[s], 1);
             mbar_init(&k_empty[s], 1);
@@ -822,12 +822,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
         }
-        for (int x = 0; x < 2; ++x) {
+        for (int x = 0; x < C::NSB; ++x) {
             mbar_init(&s_full[x], 1);
             mbar_init(&p_full[x], 8);
             mbar_init(&buf_free[x], 1);
-            mbar_init(&drain[x], 1);
         }
+        mbar_init(&drain[0], 1);
+        mbar_init(&drain[1], 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -930,6 +931,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const int n_boxes = min(n_tiles * p.boxes_per_tile, C::MAX_BOXES);
         const int32_t* bt_row = p.paged ? p.bt + (int64_t)b * p.bt_s0 : nullptr;
         if (warp == 0) {
+            if (lane == 0 && !p.withhold) {  // the q tile first: its latency overlaps the id lookups
+                prefetch_tmap(&tm_q);
+                mbar_arrive_expect_tx(q_full, C::CH * trows * 128);
+                for (int c = 0; c < C::CH; ++c)
+                    tma_load_4d(smem + C::OFF_Q + c * 128 * 128, &tm_q, q_full, c * 64, hk * p.G, q0 + i0, 0, 0ull);
+            }
             for (int bi = lane; bi < n_boxes; bi += 32) {
                 const int key = kt0 + bi * p.box_rows;
                 ids[bi] = p.paged ? box_block(bt_row, p.bt_cols, p.num_blocks, p.P, key, sk, p.err)
@@ -972,33 +979,35 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         constexpr uint32_t IDESC_S = tc::idesc_f16(128, 64, kBF16, false, false);
         constexpr uint32_t IDESC_O = tc::idesc_f16(128, 256, kBF16, false, true);
         const bool s_issuer = warp == 1;
-        auto s_buf = [&](int j) { return tmem + ((j & 1) ? C::T_S1 : C::T_S0); };
+        auto s_buf = [&](int j) { return tmem + C::T_S + 64 * (j % C::NSB); };
         auto wait_all = [&](uint64_t* bar, uint32_t parity) {
             const bool r = __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, p.err, p.wait_ns));
             tc::fence_after_sync();
             return r;
         };
         if (s_issuer) {
-            // S(j) = Q K_j^T into S buffer j % 2 (A: q in tensor memory, 8 columns per 16-column step)
+            // S(j) = Q K_j^T into S buffer j % NSB (A: the q tile, B: K stage, both K-major)
+            const uint64_t da = tc::smem_desc_sw128(smem_addr(smem + C::OFF_Q), 16, 1024);
             const uint64_t dk0 = tc::smem_desc_sw128(smem_addr(smem + C::OFF_K), 16, 1024);
-            const uint32_t t_q = tmem + C::T_Q;
             bool ok = wait_all(q_full, 0);
             for (int j = 0; ok && j < n_tiles; ++j) {
-                if (j >= 2 && !(ok = wait_all(&buf_free[j & 1], ((j - 2) >> 1) & 1))) break;
+                const int x = j % C::NSB;
+                if (j >= C::NSB && !(ok = wait_all(&buf_free[x], ((j / C::NSB) - 1) & 1))) break;
                 if (!(ok = wait_all(&k_full[j % C::KS], (j / C::KS) & 1))) break;
                 if (lane == 0) {
                     const uint64_t db = dk0 + (uint64_t)((j % C::KS) * (C::KV_TILE >> 4));
 #pragma unroll
                     for (int kk = 0; kk < C::DP / 16; ++kk) {
-                        const uint64_t off = (uint64_t)((kk >> 2) * (64 * 128 / 16) + (kk & 3) * 2);
-                        tc::mma_ts(s_buf(j), t_q + kk * 8, db + off, IDESC_S, kk > 0 ? 1u : 0u);
+                        const uint64_t oa = (uint64_t)((kk >> 2) * (128 * 128 / 16) + (kk & 3) * 2);
+                        const uint64_t ob = (uint64_t)((kk >> 2) * (64 * 128 / 16) + (kk & 3) * 2);
+                        tc::mma_ss(s_buf(j), da + oa, db + ob, IDESC_S, kk > 0 ? 1u : 0u);
                     }
-                    tc::commit(&s_full[j & 1]);
+                    tc::commit(&s_full[x]);
                 }
                 __syncwarp();
             }
         } else {
-            // O += P(j) V_j, P(j) in the first 32 columns of S buffer j % 2
+            // O += P(j) V_j, P(j) in the first 32 columns of S buffer j % NSB
             const uint64_t dv0 = tc::smem_desc_sw128(smem_addr(smem + C::OFF_V), 64 * 128, 1024);
             const uint32_t t_o = tmem + C::T_O;
             bool ok = true;
@@ -1017,14 +1026,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     __syncwarp();
                     tc::fence_after_sync();
                 }
-                if (!(ok = wait_all(&p_full[j & 1], (j >> 1) & 1))) break;
+                if (!(ok = wait_all(&p_full[j % C::NSB], (j / C::NSB) & 1))) break;
                 if (lane == 0) {
                     const uint64_t db = dv0 + (uint64_t)((j % C::VS) * (C::KV_TILE >> 4));
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         tc::mma_ts(t_o, s_buf(j) + kk * 8, db + (uint64_t)(kk * (2048 / 16)), IDESC_O,
                                    kk > 0 ? 1u : (j > 0 ? 1u : 0u));
-                    tc::commit(&buf_free[j & 1]);
+                    tc::commit(&buf_free[j % C::NSB]);
                 }
                 __syncwarp();
             }
@@ -1049,37 +1058,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const int gid = lane >> 2, tig = lane & 3;
         const int lb = lg * 32 + hh * 16;
         const uint32_t lane_addr = (uint32_t)lb << 16;
-
-        // q rows into tensor memory: warp (lg, hh) writes head-dim half hh (64 columns of
-        // packed pairs) of rows 32 lg .. 32 lg + 31, one row per thread (columns past D and
-        // rows without a query are zero)
-        {
-            const int r = lg * 32 + lane;
-            const T* q = static_cast<const T*>(p.q);
-            const bool live = row_live(r);
-            const int64_t rho = tile_rho(r);
-            const int i = live ? (int)(rho / p.G) : 0, g = live ? (int)(rho - (int64_t)i * p.G) : 0;
-            const T* src = q + (int64_t)(q0 + i) * p.q_s0 + (int64_t)(hk * p.G + g) * p.q_s1;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t w[32];
-#pragma unroll
-                for (int v4 = 0; v4 < 8; ++v4) {
-                    const int d = hh * 128 + half * 64 + v4 * 8;  // first of 8 elements
-                    int4 x = make_int4(0, 0, 0, 0);
-                    if (live && d < p.D) x = __ldg(reinterpret_cast<const int4*>(src + d));
-                    w[4 * v4] = (uint32_t)x.x;
-                    w[4 * v4 + 1] = (uint32_t)x.y;
-                    w[4 * v4 + 2] = (uint32_t)x.z;
-                    w[4 * v4 + 3] = (uint32_t)x.w;
-                }
-                tc::st_32x32b_x32(tmem + ((uint32_t)(lg * 32) << 16) + C::T_Q + hh * 64 + half * 32, w);
-            }
-            tc::wait_st();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(q_full);
-        }
 
         int lo_r[2], hi_r[2], dg_r[2];
         float ab_r[2], m_r[2], l_r[2];
@@ -1108,10 +1086,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         // One key tile: S -> running max -> P; O rescaled (rarely) once PV(j-1) is complete.
         auto step = [&](int j) -> bool {
             const int kt = kt0 + j * 64;
-            if (!__all_sync(0xffffffffu, wait_bar(&s_full[j & 1], (j >> 1) & 1, abort_flag, p.err, p.wait_ns)))
+            if (!__all_sync(0xffffffffu,
+                            wait_bar(&s_full[j % C::NSB], (j / C::NSB) & 1, abort_flag, p.err, p.wait_ns)))
                 return false;
             tc::fence_after_sync();
-            const uint32_t s_addr = tmem + lane_addr + ((j & 1) ? C::T_S1 : C::T_S0);
+            const uint32_t s_addr = tmem + lane_addr + C::T_S + 64 * (j % C::NSB);
             // sv[4k + 2q + e] = S[row q][key 8k + 2 tig + e]
             float sv[32];
             tc::ld_16x256b_x8(s_addr, sv);
@@ -1195,8 +1174,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             for (int q = 0; q < 2; ++q) l_r[q] = l_r[q] * alpha[q] + (sums[2 * q] + sums[2 * q + 1]);
             if (j > 0) {
                 // PV(j-1) complete: O holds every earlier tile, V stage j-1 is free
-                if (!__all_sync(0xffffffffu,
-                                wait_bar(&buf_free[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.err, p.wait_ns)))
+                if (!__all_sync(0xffffffffu, wait_bar(&buf_free[(j - 1) % C::NSB], ((j - 1) / C::NSB) & 1, abort_flag,
+                                                      p.err, p.wait_ns)))
                     return false;
                 tc::fence_after_sync();
                 if (warp == 4 && lane == 0) mbar_arrive(&v_empty[(j - 1) % C::VS]);
@@ -1218,14 +1197,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             tc::wait_st();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[j & 1]);
+            if (lane == 0) mbar_arrive(&p_full[j % C::NSB]);
             return true;
         };
 
         bool ok = true;
         for (int j = 0; ok && j < n_tiles; ++j) ok = step(j);
-        if (ok && __all_sync(0xffffffffu, wait_bar(&buf_free[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, abort_flag,
-                                                   p.err, p.wait_ns))) {
+        if (ok && __all_sync(0xffffffffu, wait_bar(&buf_free[(n_tiles - 1) % C::NSB], ((n_tiles - 1) / C::NSB) & 1,
+                                                   abort_flag, p.err, p.wait_ns))) {
             tc::fence_after_sync();
             float inv[2];
             T* orow[2];
@@ -1277,7 +1256,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 template <typename T, bool ALIBI>
 int run_prefill256(const Args& a, const PrefillParams& pp, cudaStream_t stream, char* msg, size_t msg_len) {
     using C = P2Cfg;
-    CUtensorMap tk, tv;
+    CUtensorMap tq, tk, tv;
+    {  // q as (D, H, total_q, 1), box (64, G, 128 / G, 1), as in the head-dim-128 kernel
+        const uint64_t dims[4] = {(uint64_t)a.D, (uint64_t)a.H, (uint64_t)a.total_q, 1};
+        const uint64_t strides[3] = {(uint64_t)a.q_s1 * 2, (uint64_t)a.q_s0 * 2, (uint64_t)a.q_s0 * 2 * a.total_q};
+        const uint32_t box[4] = {64u, (uint32_t)pp.G, (uint32_t)(128 / pp.G), 1u};
+        int rc = encode_tmap_4d(&tq, a.dtype, a.q, dims, strides, box, 1, msg, msg_len);
+        if (rc != PA_OK) return rc;
+    }
     {
         uint64_t dims[4], strides[3];
         if (a.paged) {
@@ -1316,7 +1302,7 @@ int run_prefill256(const Args& a, const PrefillParams& pp, cudaStream_t stream, 
     dim3 grid(pp.pairs, a.Hkv, 1);
     NvtxRange nv("pa::prefill256_kernel");
     timer_begin(PA_KC_PREFILL, stream);
-    kern<<<grid, kPrefillThreads, C::SMEM, stream>>>(tk, tv, pp);
+    kern<<<grid, kPrefillThreads, C::SMEM, stream>>>(tq, tk, tv, pp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "prefill256 launch: %s", cudaGetErrorString(e));
@@ -1339,16 +1325,13 @@ bool prefill_supported(const Args& a) {
     if (!(a.scale > 0.f)) return false;
     if ((int64_t)a.max_sq * G <= prefill_rows_threshold()) return false;  // nothing for it to do
     if (a.total_q <= 0 || a.q_s1 * 2 % 16 != 0 || a.q_s0 * 2 % 16 != 0) return false;
-    // the head-dim-256 kernel reads q rows with 16-byte loads (the others through a tensor map)
+    // a q tensor map needs a 16-byte aligned base: rows of wider heads then take the general kernel
     if (a.D > 128 && reinterpret_cast<uintptr_t>(a.q) % 16 != 0) return false;
     return true;
 }
 
 int launch_prefill(const Args& a, unsigned int* err, char* msg, size_t msg_len) {
     PrefillParams pp{};
-    pp.q = a.q;
-    pp.q_s0 = a.q_s0;
-    pp.q_s1 = a.q_s1;
     pp.out = a.out;
     pp.o_s0 = a.o_s0;
     pp.o_s1 = a.o_s1;
