@@ -121,3 +121,17 @@ def test_skewed_batch_one_very_long_sequence():
     ref_o, ref_l = _gpu.oracle_for(inp.to("cpu"), rows)
     _gpu.compare(lay, out, lse, ref_o, ref_l, rows)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("wl", [-1, 1000])
+def test_work_list_with_bias_and_window(wl):
+    """Work-list mode (40 sequences, two split) with the position bias, causal and windowed."""
+    rng = np.random.default_rng(40 + max(wl, 0))
+    sk = rng.integers(1, 900, size=40, endpoint=True)
+    sk[[4, 29]] = 22000
+    sq = np.where(rng.random(40) < 0.3, 4, 1)
+    lay = workloads.make_layout("worklist_bias", "bf16", sq.tolist(), sk.tolist(), num_heads=8, num_heads_k=2,
+                                head_dim=128, page_block_size=64, seed=41, spare=0.05, window_left=wl,
+                                window_right=0)
+    _gpu.check_layout(lay, limit=4096, alibi=_gpu.alibi_slopes(8, "random", seed=5))
+

@@ -73,6 +73,12 @@ def test_mixed_with_decode_rows():
     _gpu.check_layout(_lay([1, 200, 4, 1, 90, 4], [900, 250, 300, 17, 600, 5], H=8, Hkv=2, seed=100), limit=3000)
 
 
+@pytest.mark.parametrize("G", [16, 64, 128])
+def test_large_groups(G):
+    """128 / G queries per tile: 8, 2 and 1 (a group of 128 heads fills a tile with one query)."""
+    _gpu.check_layout(_lay([70, 9], [200, 9], H=G, Hkv=1, D=192, seed=102 + G), limit=3000)
+
+
 def test_long_causal():
     """Two sequences of 2,048 and 1,500 queries (16 and 12 query tiles over up to 32 key tiles)."""
     _gpu.check_layout(_lay([2048, 1500], [2048, 1500], H=16, Hkv=4, seed=101), limit=2048)

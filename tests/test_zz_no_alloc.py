@@ -44,13 +44,16 @@ def _fresh_outputs(lay):
 
 
 def _layout(name):
-    if name == "large":  # 300 sequences: the ranking pass's order slot, then the partials
+    if name == "large":  # 300 sequences: the work list, then the partials
         # (max_seqlen_k 500: nine one-tile splits of ~2.3 MB each fit the 32 MiB array)
         return skewed_layout(300, seed=41, long_k=500, short_hi=400)
+    if name == "wide":  # head_dim 256 prefill rows (their kernel) beside decode rows (split)
+        return workloads.make_layout("noalloc_wide", "bf16", [150, 1, 4, 1], [300, 700, 200, 90], num_heads=8,
+                                     num_heads_k=2, head_dim=256, page_block_size=64, seed=43, spare=0.1)
     return workloads.small(name)
 
 
-@pytest.mark.parametrize("name", ["decode", "long", "large"])
+@pytest.mark.parametrize("name", ["decode", "long", "large", "wide"])
 def test_noalloc_equals_pa_varlen_fwd_and_oracle(name, monkeypatch):
     # one 64-key tile per split forces several splits, so the scratch array is used
     monkeypatch.setenv("PA_SPLIT_TILES", "1")
