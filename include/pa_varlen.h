@@ -323,10 +323,10 @@ uint64_t pa_kernel_launches(void);
  * stops recording; what was recorded stays until it is read.
  * pa_kernel_times waits for the recorded events, writes to ms[c] the summed elapsed
  * milliseconds and to launches[c] the number of timed launches of kernel class c, and
- * clears the record.  Classes: PA_KC_PREFILL (the tensor-core prefill kernel),
- * PA_KC_SPLITKV (the split-KV pass: decode_kernel or splitkv_kernel), PA_KC_COMBINE (the
- * split-KV combine), PA_KC_APPEND (pa_kv_append's kernel).  ms and launches are caller-owned host arrays of PA_KERNEL_CLASSES
- * entries.  Returns PA_OK, PA_ERR_ARG for a null array, or PA_ERR_CUDA if an event
+ * clears the record.  Classes: PA_KC_PREFILL (the tensor-core prefill kernels),
+ * PA_KC_SPLITKV (the split-KV pass: decode_kernel, decode512_kernel, decode_tc_kernel or
+ * splitkv_kernel), PA_KC_COMBINE (the split-KV combine), PA_KC_APPEND (pa_kv_append's
+ * kernel).  ms and launches are caller-owned host arrays of PA_KERNEL_CLASSES entries.  Returns PA_OK, PA_ERR_ARG for a null array, or PA_ERR_CUDA if an event
  * query failed (message in pa_last_error; the record is cleared either way). */
 #define PA_KC_PREFILL 0
 #define PA_KC_SPLITKV 1

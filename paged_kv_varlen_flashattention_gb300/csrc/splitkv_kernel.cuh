@@ -489,10 +489,9 @@ int launch_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const SplitPa
                      int dtype, cudaStream_t stream, char* msg, size_t msg_len);
 
 // lse = ln sum_s exp(lse_s); out = sum_s exp(lse_s - lse) * O_s, for the tiles that
-// were split.  Grid: (row groups of 4, kv head x row tile, sequence); one warp per output
-// row: the split weights are computed once per row into shared memory, then each lane
-// accumulates pairs of output columns over the splits (reads of the partials coalesce
-// along the head dimension).
+// were split.  Grid: (rows x 64-column chunks, kv head x row tile, sequence); one CTA per
+// (output row, 64 columns), each lane accumulating a pair of columns (reads of the partials
+// coalesce along the head dimension).
 constexpr int kCombineRows = 1;          // output rows per CTA (grid.x = rows x 64-column chunks)
 constexpr int kCombineMaxSplits = 1024;  // split weights kept in shared memory
 
