@@ -79,7 +79,8 @@ enum {
                                    a page past the block table, non-monotone cu_seqlens, or a
                                    sequence longer than max_seqlen_q / max_seqlen_k; the offending
                                    work was skipped, its output is undefined */
-    PA_ERR_WORKSPACE = 15       /* split-KV workspace must grow while the stream is capturing */
+    PA_ERR_WORKSPACE = 15       /* the scratch must grow while the stream is capturing (or, for
+                                   pa_varlen_fwd_noalloc, exceeds its fixed array) */
 };
 
 /*
@@ -113,9 +114,10 @@ enum {
  * page size == k shape, page size % 32, head size <= 512; then device residency, then the
  * library's own argument checks.  Returns PA_OK or a status (message: pa_last_error()).
  * Memory: the library keeps one grow-only scratch per (device, stream) for the split-KV
- * partial results and the decode kernel's launch order or work list (longest sequence
- * first; the list, with its take counter, is rewritten on the device by every call); it is
- * allocated on first need with cudaMalloc and never while `stream` is capturing
+ * partial results, the decode kernel's launch order or work list (longest sequence first;
+ * the list, with its take counter, is rewritten on the device by every call) and the
+ * prefill kernels' item counter (256 bytes, zeroed on the device by every call that runs
+ * them); it is allocated on first need with cudaMalloc and never while `stream` is capturing
  * (PA_ERR_WORKSPACE): before capturing a call into a CUDA graph, make one call of the
  * largest shape on the capture stream.
  * Streams: a batch that holds prefill-class sequences (more than 32 rows of q_len x the
@@ -145,13 +147,14 @@ int pa_varlen_fwd(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor*
  * pa_varlen_fwd; the caller still provides every input and output.
  *
  * Scratch: split-KV partial results (and the decode launch order of batches of more than
- * 160 sequences, or the work list of batches of 16 or more that the plan splits) go to one
- * fixed 32 MiB array compiled into the library
+ * 160 sequences, or the work list of batches of 16 or more that the plan splits, and the
+ * prefill kernels' item counter) go to one fixed 32 MiB array compiled into the library
  * (a static device array: every GPU that loads the library holds it until the process
  * exits) instead of the library's growable workspace.  A call whose split plan needs more
  * than 32 MiB is rejected with PA_ERR_WORKSPACE and a message giving both sizes.  The
  * array keeps the last call's contents; nothing in it needs to start at zero (the work
- * list's take counter is zeroed on the device by the call that uses it).  All calls,
+ * list's and the prefill kernels' take counters are zeroed on the device by the call that
+ * uses them).  All calls,
  * on every stream and host thread, share this one array: calls that overlap on the GPU
  * race and give undefined results, so serialise them (one stream, or events).
  * The first call on each device looks up the array's device address

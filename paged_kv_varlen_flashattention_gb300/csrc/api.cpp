@@ -721,13 +721,17 @@ int launch_forward(pa::Args& a, void* stream, ScratchFn scratch, void* scratch_c
 
     const bool use_prefill = pa::prefill_supported(a);
     const pa::SplitPlan plan = pa::plan_splitkv(a, use_prefill, sm_count());
+    // the prefill kernels' item counter follows the split-KV scratch
+    const size_t counter_at = (plan.ws_bytes + 255) / 256 * 256;
+    const size_t ws_bytes = use_prefill ? counter_at + pa::kPrefillCounterBytes : plan.ws_bytes;
     void* ws = nullptr;
-    if (plan.ws_bytes) {
-        rc = scratch(scratch_ctx, a.stream, plan.ws_bytes, &ws, g_msg, sizeof g_msg);
+    if (ws_bytes) {
+        rc = scratch(scratch_ctx, a.stream, ws_bytes, &ws, g_msg, sizeof g_msg);
         if (rc != PA_OK) return rc;
     }
+    int* counter = use_prefill ? reinterpret_cast<int*>(static_cast<char*>(ws) + counter_at) : nullptr;
     if (!use_prefill || !side_stream_ok) {
-        if (use_prefill && (rc = pa::launch_prefill(a, err, g_msg, sizeof g_msg)) != PA_OK) return rc;
+        if (use_prefill && (rc = pa::launch_prefill(a, counter, err, g_msg, sizeof g_msg)) != PA_OK) return rc;
         rc = pa::launch_splitkv(a, plan, ws, err, g_msg, sizeof g_msg);
         if (rc != PA_OK) return rc;
         g_msg[0] = '\0';
@@ -742,7 +746,7 @@ int launch_forward(pa::Args& a, void* stream, ScratchFn scratch, void* scratch_c
     if (e != cudaSuccess) return fail(PA_ERR_CUDA, "forking the prefill stream: %s", cudaGetErrorString(e));
     pa::Args ap = a;
     ap.stream = ss->stream;
-    rc = pa::launch_prefill(ap, err, g_msg, sizeof g_msg);
+    rc = pa::launch_prefill(ap, counter, err, g_msg, sizeof g_msg);
     if (rc == PA_OK) rc = pa::launch_splitkv(a, plan, ws, err, g_msg, sizeof g_msg);
     // join even after a failed launch, so the caller's stream never runs ahead of the side stream
     e = cudaEventRecord(ss->join, ss->stream);

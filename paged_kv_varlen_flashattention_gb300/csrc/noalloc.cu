@@ -51,7 +51,7 @@ int scratch_address(void** ptr, char* msg, size_t msg_len) {
 int static_scratch(void*, cudaStream_t, size_t bytes, void** ptr, char* msg, size_t msg_len) {
     if (bytes > PA_NOALLOC_SCRATCH_BYTES) {
         snprintf(msg, msg_len,
-                 "this call needs %zu bytes of split-KV scratch; pa_varlen_fwd_noalloc has %u bytes (use "
+                 "this call needs %zu bytes of scratch; pa_varlen_fwd_noalloc has %u bytes (use "
                  "pa_varlen_fwd, fewer sequences per call, or a shorter max_seqlen_k)",
                  bytes, (unsigned)PA_NOALLOC_SCRATCH_BYTES);
         return PA_ERR_WORKSPACE;

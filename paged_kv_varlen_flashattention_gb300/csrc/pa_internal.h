@@ -88,7 +88,11 @@ int launch_longest_first(const int32_t* cu_k, int batch, int* order, cudaStream_
 // Dense-prefill (tcgen05) launch availability for these arguments.
 bool prefill_supported(const Args& a);
 int prefill_rows_threshold();  // sequences with sq*G > this go to the prefill kernel
-int launch_prefill(const Args& a, unsigned int* err, char* msg, size_t msg_len);
+// The prefill kernels are persistent (one CTA per SM over a device counter of work items):
+// each call takes kPrefillCounterBytes of scratch for the counter, which launch_prefill
+// zeroes on a.stream before the kernel.
+constexpr size_t kPrefillCounterBytes = 256;
+int launch_prefill(const Args& a, int* counter, unsigned int* err, char* msg, size_t msg_len);
 
 SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, int num_sms);
 int launch_splitkv(const Args& a, const SplitPlan& plan, void* workspace, unsigned int* err, char* msg,
