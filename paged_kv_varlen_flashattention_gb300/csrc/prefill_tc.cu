@@ -426,9 +426,15 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             if (x == 0 || it.has_b) {
                 if (!(ok = wait_all(q_full, lq & 1))) break;
                 if (!(ok = wait_all(&k_full[gk % C::KS], (gk / C::KS) & 1))) break;
+                // q_free takes two arrivals an item, each when an issuer's last Q.K^T of it has
+                // completed; without tile B both come from this issuer (were issuer 1 to arrive
+                // at once for such an item, it could arrive for the next one too before this
+                // issuer finished, and the next q tiles would overwrite q this item still reads)
+                const int qf = it.has_b ? 1 : 2;
                 if (lane == 0) {
                     issue_s(gk);
-                    if (n == 1) tc::commit(q_free);  // the item's last Q.K^T is issued
+                    if (n == 1)  // the item's last Q.K^T is issued
+                        for (int c = 0; c < qf; ++c) tc::commit(q_free);
                 }
                 __syncwarp();
                 for (int j = 0; ok && j < n; ++j) {
@@ -461,16 +467,15 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                         if (j + 1 == n) tc::commit(&pv_done[x]);
                         if (more) {
                             issue_s(g_k);
-                            if (j + 2 == n) tc::commit(q_free);
+                            if (j + 2 == n)
+                                for (int c = 0; c < qf; ++c) tc::commit(q_free);
                         }
                     }
                     __syncwarp();
                 }
                 if (!ok) break;
                 sx += n;
-            } else if (lane == 0) {
-                tc::commit(q_free);  // no tile B: nothing this issuer starts reads the q tiles
-            }
+            }  // no tile B: issuer 0 arrives on q_free for both
             __syncwarp();
             gk += n;
             gv += n;

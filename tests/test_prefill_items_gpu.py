@@ -1,0 +1,72 @@
+"""The persistent prefill kernels over many work items per CTA (GPU).
+
+Both prefill kernels run one CTA per SM and take (query-tile pair or query tile, kv head)
+items from a device counter; rings, S/P handshakes and barrier phases run on from item to
+item.  These batches hold a few hundred prefill-class sequences, so every CTA takes several
+items of different lengths: causal and chunked sequences, sequences whose first rows attend
+no key (more queries than keys), sequences with no keys at all, decode-class rows beside
+them (the split-KV pass), a window, and group sizes that do and do not divide 128.  Rows are
+sampled (always including each sequence's first and last query) and compared with the
+oracle at the stated tolerances."""
+import numpy as np
+import pytest
+
+from paged_kv_varlen_flashattention_gb300 import workloads
+from tests import _gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _default_kernels(monkeypatch):
+    monkeypatch.delenv("PA_DISABLE_TC_PREFILL", raising=False)
+    monkeypatch.delenv("PA_FORCE_GENERIC", raising=False)
+
+
+def _batch(n, seed, *, lo=20, hi=420, short_frac=0.15, nokv_frac=0.03):
+    """n sequences: q lengths U[lo, hi]; keys = queries plus U[0, 300] cached (chunked
+    prefill), fewer keys than queries for ~10 %, no keys for nokv_frac, and q_len 1..4
+    (decode class) for short_frac."""
+    rng = np.random.default_rng(seed)
+    sq, sk = [], []
+    for _ in range(n):
+        u = rng.random()
+        if u < short_frac:
+            q = int(rng.integers(1, 5))
+            sq.append(q)
+            sk.append(q + int(rng.integers(0, 500)))
+        elif u < short_frac + nokv_frac:
+            sq.append(int(rng.integers(lo, hi + 1)))
+            sk.append(0)
+        elif u < short_frac + nokv_frac + 0.1:
+            q = int(rng.integers(lo, hi + 1))
+            sq.append(q)
+            sk.append(int(rng.integers(1, q)))
+        else:
+            q = int(rng.integers(lo, hi + 1))
+            sq.append(q)
+            sk.append(q + int(rng.integers(0, 301)))
+    return sq, sk
+
+
+@pytest.mark.parametrize("D,H,Hkv", [(128, 32, 8), (64, 16, 4), (256, 16, 4), (128, 12, 4), (256, 24, 2)])
+def test_many_items_per_cta(D, H, Hkv):
+    """300 sequences: G = 4 (pairs of 32-query tiles), G = 3 and 12 (padding rows)."""
+    sq, sk = _batch(300, seed=200 + D + H)
+    lay = workloads.make_layout("items", "bf16", sq, sk, num_heads=H, num_heads_k=Hkv, head_dim=D,
+                                page_block_size=64, seed=201 + D, spare=0.1)
+    _gpu.check_layout(lay, limit=1500)
+
+
+def test_many_items_window_fp16():
+    sq, sk = _batch(200, seed=210, lo=40, hi=700)
+    lay = workloads.make_layout("items_w", "f16", sq, sk, num_heads=16, num_heads_k=2, head_dim=128,
+                                page_block_size=32, seed=211, spare=0.1, window_left=150, window_right=0)
+    _gpu.check_layout(lay, limit=1500)
+
+
+def test_many_items_bias():
+    sq, sk = _batch(160, seed=220, lo=33, hi=300)
+    lay = workloads.make_layout("items_b", "bf16", sq, sk, num_heads=16, num_heads_k=4, head_dim=256,
+                                page_block_size=64, seed=221, spare=0.1)
+    _gpu.check_layout(lay, alibi=_gpu.alibi_slopes(16, "random", seed=7), limit=1200)
