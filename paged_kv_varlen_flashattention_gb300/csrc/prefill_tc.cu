@@ -414,9 +414,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < DP / 16; ++kk) {
                 const uint64_t off = (uint64_t)((kk >> 2) * (128 * 128 / 16) + (kk & 3) * 2);
-                tc::mma_ss(d_s, da + off, db + off, IDESC_S, kk > 0 ? 1u : 0u);
+                tc::mma_ss_elect(d_s, da + off, db + off, IDESC_S, kk > 0 ? 1u : 0u);
             }
-            tc::commit(&s_full[x]);
+            tc::commit_elect(&s_full[x]);
         };
         for (int k = 0; ok; ++k) {
             PfItem it;
@@ -431,11 +431,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 // at once for such an item, it could arrive for the next one too before this
                 // issuer finished, and the next q tiles would overwrite q this item still reads)
                 const int qf = it.has_b ? 1 : 2;
-                if (lane == 0) {
-                    issue_s(gk);
-                    if (n == 1)  // the item's last Q.K^T is issued
-                        for (int c = 0; c < qf; ++c) tc::commit(q_free);
-                }
+                issue_s(gk);  // the whole warp, one elected lane issuing
+                if (n == 1)      // the item's last Q.K^T is issued
+                    for (int c = 0; c < qf; ++c) tc::commit_elect(q_free);
                 __syncwarp();
                 for (int j = 0; ok && j < n; ++j) {
                     const int g_v = gv + j;
@@ -457,18 +455,18 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     const int g_k = gk + j + 1;
                     if (more && !(ok = wait_all(&k_full[g_k % C::KS], (g_k / C::KS) & 1))) break;
                     if (!(ok = wait_all(&p_full[x], (sx + j) & 1))) break;
-                    if (lane == 0) {
+                    {  // the whole warp, one elected lane issuing
                         const uint64_t db = dv0 + (uint64_t)((g_v % C::VS) * (C::KV_TILE >> 4));
                         const uint32_t first = j > 0 ? 1u : 0u;
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
-                            tc::mma_ts(d_o, d_s + kk * 8, db + (uint64_t)(kk * (2048 / 16)), IDESC_O,
-                                       kk > 0 ? 1u : first);
-                        if (j + 1 == n) tc::commit(&pv_done[x]);
+                            tc::mma_ts_elect(d_o, d_s + kk * 8, db + (uint64_t)(kk * (2048 / 16)), IDESC_O,
+                                             kk > 0 ? 1u : first);
+                        if (j + 1 == n) tc::commit_elect(&pv_done[x]);
                         if (more) {
                             issue_s(g_k);
                             if (j + 2 == n)
-                                for (int c = 0; c < qf; ++c) tc::commit(q_free);
+                                for (int c = 0; c < qf; ++c) tc::commit_elect(q_free);
                         }
                     }
                     __syncwarp();
@@ -1098,17 +1096,17 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 if (g >= NSB && !(ok = wait_all(&buf_free[x], ((g / NSB) - 1) & 1))) break;
                 const int gkj = gk + j;
                 if (!(ok = wait_all(&k_full[gkj % KS], (gkj / KS) & 1))) break;
-                if (lane == 0) {
+                {  // the whole warp, one elected lane issuing
                     const uint64_t db = dk0 + (uint64_t)((gkj % KS) * (C::KV_TILE >> 4));
                     const uint32_t d_s = tmem + C::T_S + NT * x;
 #pragma unroll
                     for (int kk = 0; kk < DP / 16; ++kk) {
                         const uint64_t oa = (uint64_t)((kk >> 2) * (128 * 128 / 16) + (kk & 3) * 2);
                         const uint64_t ob = (uint64_t)((kk >> 2) * (NT * 128 / 16) + (kk & 3) * 2);
-                        tc::mma_ss(d_s, da + oa, db + ob, IDESC_S, kk > 0 ? 1u : 0u);
+                        tc::mma_ss_elect(d_s, da + oa, db + ob, IDESC_S, kk > 0 ? 1u : 0u);
                     }
-                    tc::commit(&s_full[x]);
-                    if (j + 1 == n) tc::commit(q_free);  // the item's last read of the q tile
+                    tc::commit_elect(&s_full[x]);
+                    if (j + 1 == n) tc::commit_elect(q_free);  // the item's last read of the q tile
                 }
                 __syncwarp();
             }
@@ -1150,14 +1148,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     tc::fence_after_sync();
                 }
                 if (!(ok = wait_all(&p_full[g % NSB], (g / NSB) & 1))) break;
-                if (lane == 0) {
+                {  // the whole warp, one elected lane issuing
                     const uint64_t db = dv0 + (uint64_t)((gvj % VS) * (C::KV_TILE >> 4));
                     const uint32_t a_p = tmem + C::T_S + NT * (g % NSB);
 #pragma unroll
                     for (int kk = 0; kk < NT / 16; ++kk)
-                        tc::mma_ts(t_o, a_p + kk * 8, db + (uint64_t)(kk * (2048 / 16)), IDESC_O,
-                                   kk > 0 ? 1u : (j > 0 ? 1u : 0u));
-                    tc::commit(&buf_free[g % NSB]);
+                        tc::mma_ts_elect(t_o, a_p + kk * 8, db + (uint64_t)(kk * (2048 / 16)), IDESC_O,
+                                         kk > 0 ? 1u : (j > 0 ? 1u : 0u));
+                    tc::commit_elect(&buf_free[g % NSB]);
                 }
                 __syncwarp();
             }
