@@ -351,15 +351,15 @@ __global__ void __launch_bounds__(TcRoles<NR>::THREADS, 1)
                 for (int h = 0; h < KH; ++h) {
                     const int u = j * KH + h, slot = u % KR;
                     if (!(ok = wait_all(&k_full[slot], (u / KR) & 1))) break;
-                    if (lane == 0) {
+                    {
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
                             const uint64_t a = d_k + (uint64_t)((slot * C::KUNIT + kk * 32) >> 4);
                             const uint64_t bq = d_q + (uint64_t)((h * C::Q_CHUNK + kk * 32) >> 4);
-                            tc::mma_ss(tmem + C::T_S + (j & 1) * NR, a, bq, IDESC_S, (h | kk) ? 1u : 0u);
+                            tc::mma_ss_elect(tmem + C::T_S + (j & 1) * NR, a, bq, IDESC_S, (h | kk) ? 1u : 0u);
                         }
-                        tc::commit(&k_empty[slot]);
-                        if (h == KH - 1) tc::commit(&s_full[j & 1]);
+                        tc::commit_elect(&k_empty[slot]);
+                        if (h == KH - 1) tc::commit_elect(&s_full[j & 1]);
                     }
                     __syncwarp();
                 }
@@ -386,16 +386,16 @@ __global__ void __launch_bounds__(TcRoles<NR>::THREADS, 1)
                         __syncwarp();
                         tc::fence_after_sync();
                     }
-                    if (lane == 0) {
+                    {
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
                             const uint64_t a = d_v + (uint64_t)((slot * C::VUNIT + kk * 2048) >> 4);
                             const uint64_t bp = d_p + (uint64_t)(((j & 1) * C::P_BUF + (kk >> 2) * (NR * 128) +
                                                                   (kk & 3) * 32) >> 4);
-                            tc::mma_ss(tmem + C::T_O + c * NR, a, bp, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+                            tc::mma_ss_elect(tmem + C::T_O + c * NR, a, bp, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
                         }
-                        tc::commit(&v_empty[slot]);
-                        if (c == CH - 1) tc::commit(&pv_done[j & 1]);
+                        tc::commit_elect(&v_empty[slot]);
+                        if (c == CH - 1) tc::commit_elect(&pv_done[j & 1]);
                     }
                     __syncwarp();
                 }
