@@ -70,3 +70,53 @@ def test_many_items_bias():
     lay = workloads.make_layout("items_b", "bf16", sq, sk, num_heads=16, num_heads_k=4, head_dim=256,
                                 page_block_size=64, seed=221, spare=0.1)
     _gpu.check_layout(lay, alibi=_gpu.alibi_slopes(16, "random", seed=7), limit=1200)
+
+
+N_RANDOM = 16
+
+
+def random_items_layout(seed):
+    """60..200 sequences drawn around the prefill kernels' item boundaries: query lengths
+    that end a tile pair inside its first tile (items without tile B), exactly on a tile,
+    just past one; chunked prefill, more queries than keys, no keys, and decode rows; a
+    random head dim, group size, page size, window, dtype and (sometimes) position bias."""
+    rng = np.random.default_rng(5000 + seed)
+    D = int(rng.choice([64, 96, 128, 192, 256]))
+    G = int(rng.choice([1, 2, 3, 4, 5, 8, 16]))
+    Hkv = int(rng.choice([1, 2, 4]))
+    P = int(rng.choice([32, 64, 128, 256]))
+    qpt = 128 // G
+    n = int(rng.integers(60, 201))
+    sq, sk = [], []
+    for _ in range(n):
+        kind = rng.choice(["pair_edge", "tile_edge", "chunk", "fewer_keys", "no_keys", "decode"],
+                          p=[0.25, 0.2, 0.25, 0.1, 0.05, 0.15])
+        if kind == "pair_edge":    # ends within the first tile of its last pair
+            q = int(rng.integers(0, 4)) * 2 * qpt + int(rng.integers(1, qpt + 1))
+            k = q + int(rng.integers(0, 200))
+        elif kind == "tile_edge":  # a multiple of the tile, or one past it
+            q = int(rng.integers(1, 6)) * qpt + int(rng.integers(0, 2))
+            k = q
+        elif kind == "chunk":
+            q = int(rng.integers(33, 300)); k = q + int(rng.integers(1, 600))
+        elif kind == "fewer_keys":
+            q = int(rng.integers(40, 300)); k = int(rng.integers(1, q))
+        elif kind == "no_keys":
+            q = int(rng.integers(40, 200)); k = 0
+        else:
+            q = int(rng.integers(1, 4)); k = int(rng.integers(1, 800))
+        sq.append(max(q, 1)); sk.append(k)
+    wl, wr = [(-1, 0), (-1, 0), (-1, -1), (int(rng.integers(0, 300)), 0), (int(rng.integers(0, 120)), int(rng.integers(0, 40)))][
+        int(rng.integers(0, 5))]
+    dtype = "bf16" if rng.random() < 0.6 else "f16"
+    lay = workloads.make_layout(f"items_random_{seed}", dtype, sq, sk, num_heads=Hkv * G, num_heads_k=Hkv,
+                                head_dim=D, page_block_size=P, seed=6000 + seed, spare=0.1, window_left=wl,
+                                window_right=wr)
+    alibi = _gpu.alibi_slopes(Hkv * G, "random", seed=seed) if rng.random() < 0.3 else None
+    return lay, alibi
+
+
+@pytest.mark.parametrize("seed", range(N_RANDOM))
+def test_random_many_items(seed):
+    lay, alibi = random_items_layout(seed)
+    _gpu.check_layout(lay, alibi=alibi, limit=1200)
