@@ -1495,6 +1495,12 @@ int launch_persistent(Kern kern, int smem, int& sms, const Args& a, const Prefil
     CUtensorMap tq, tk, tv;
     int rc = prefill_maps(a, pp, &tq, &tk, &tv, msg, msg_len);
     if (rc != PA_OK) return rc;
+    // the kernels count items, and every CTA claims one past the last, in int
+    if ((int64_t)pp.pairs * a.Hkv + sms >= (int64_t)INT32_MAX) {
+        snprintf(msg, msg_len, "%s: %lld work items (tiles x kv heads) exceed the item counter's range", name,
+                 (long long)pp.pairs * a.Hkv);
+        return PA_ERR_UNSUPPORTED;
+    }
     const int items = pp.pairs * a.Hkv;
     NvtxRange nv(name);
     cudaError_t e = cudaMemsetAsync(pp.counter, 0, sizeof(int), stream);
