@@ -18,7 +18,10 @@ namespace pa {
 
 constexpr int kDecodeThreads = 160;  // 4 consumer warps + 1 producer warp
 
-template <int DP, int MG, int NT, int STAGES>
+// ML: the row groups the shared-memory layout is sized for (>= MG).  A kernel built for two
+// row groups runs units of at most 16 rows with the one-group body (MG = 1) in its own
+// layout (ML = 2), so that the barriers and the ring it set up stay where they are.
+template <int DP, int MG, int NT, int STAGES, int ML = MG>
 struct DecCfg {
     static constexpr int M = 16 * MG;        // rows per CTA
     static constexpr int KW = 4 / MG;        // warps sharing one row group (key-slice ways)
@@ -26,10 +29,10 @@ struct DecCfg {
     static constexpr int CH = DP / 64;
     static constexpr int TILE_BYTES = CH * NT * 128;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-    static constexpr int Q_BYTES = CH * M * 128;
+    static constexpr int Q_BYTES = CH * 16 * ML * 128;
     static constexpr int OFF_Q = STAGES * STAGE_BYTES;
     static constexpr int OFF_ROW = OFF_Q + Q_BYTES;            // row_lo[M], row_hi[M], row_dg[M], row_ab[M]
-    static constexpr int OFF_BAR = (OFF_ROW + 4 * M * 4 + 15) & ~15;
+    static constexpr int OFF_BAR = (OFF_ROW + 4 * (16 * ML) * 4 + 15) & ~15;
     static constexpr int OFF_FLAG = OFF_BAR + 2 * STAGES * 8;
     static constexpr int OFF_IDS = OFF_FLAG + 16;              // block id of every TMA box of the split
     static constexpr int MAX_BOXES = 512;
@@ -61,10 +64,10 @@ __device__ __forceinline__ bool dec_wait(uint64_t* bar, uint32_t parity, volatil
 // key tiles the CTA's ring has carried before (ring stage and phase continue from it);
 // `n_done` returns the tiles of this unit (the same in every thread).  Every thread returns
 // from here: early (no work, uniformly), when its role ends, or after the epilogue.
-template <typename T, int DP, int MG, int NT, int STAGES>
+template <typename T, int DP, int MG, int NT, int STAGES, int ML = MG>
 __device__ __forceinline__ void decode_unit(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const SplitParams& p,
                                             uint8_t* smem, int b, int hk, int split, int g0, int& n_done) {
-    using C = DecCfg<DP, MG, NT, STAGES>;
+    using C = DecCfg<DP, MG, NT, STAGES, ML>;
     constexpr int M = C::M;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     TileView tv;
@@ -408,8 +411,11 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap& tm_k, const CUten
     }
 }
 
+// Resident CTAs per SM the register bound keeps possible: three at head dim 64, two at 128
+// (as many as the shared memory allows), one at 256.
 template <typename T, int DP, int MG, int NT, int STAGES>
-__global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const __grid_constant__ CUtensorMap tm_k,
+__global__ void __launch_bounds__(kDecodeThreads, DP <= 64 ? 3 : DP <= 128 ? 2 : 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                      const __grid_constant__ CUtensorMap tm_v,
                                                      const SplitParams p) {
     using C = DecCfg<DP, MG, NT, STAGES>;
@@ -428,6 +434,24 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const __grid_con
         *abort_flag = 0u;
         fence_mbar_init();
     }
+    // A two-group kernel (the plan's bound on rows was above 16) runs the units of sequences
+    // with at most 16 rows on the one-group body: its four warps split each tile's keys in
+    // quarters instead of leaving two warps on padding rows (decode rows of the mixed batch:
+    // 321 -> 293 us).  Both bodies see the same key interval and split count for such a unit.
+    auto run_unit = [&](int b, int hk, int split, int g0, int& n_done) {
+        if constexpr (MG == 2) {
+            // the one-group body must find the barriers, flag and ids where this kernel put them
+            using L1 = DecCfg<DP, 1, NT, STAGES, 2>;
+            static_assert(L1::OFF_Q == C::OFF_Q && L1::OFF_ROW == C::OFF_ROW && L1::OFF_BAR == C::OFF_BAR &&
+                              L1::OFF_FLAG == C::OFF_FLAG && L1::OFF_IDS == C::OFF_IDS && L1::SMEM == C::SMEM,
+                          "both bodies share one shared-memory layout");
+            if (b >= 0 && b < p.batch && (int64_t)(p.cu_q[b + 1] - p.cu_q[b]) * p.G <= 16) {
+                decode_unit<T, DP, 1, NT, STAGES, 2>(tm_k, tm_v, p, smem, b, hk, split, g0, n_done);
+                return;
+            }
+        }
+        decode_unit<T, DP, MG, NT, STAGES, MG>(tm_k, tm_v, p, smem, b, hk, split, g0, n_done);
+    };
     if (p.work) {
         // Persistent: the CTA takes (sequence, split) x kv head items in list order (longest
         // sequences first) until none is left; the stage ring carries on from item to item.
@@ -441,8 +465,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const __grid_con
             if (w >= total) break;
             const int pair = w / p.Hkv;
             int n_done = 0;
-            decode_unit<T, DP, MG, NT, STAGES>(tm_k, tm_v, p, smem, p.work[2 + 2 * pair], w - pair * p.Hkv,
-                                               p.work[3 + 2 * pair], g0, n_done);
+            run_unit(p.work[2 + 2 * pair], w - pair * p.Hkv, p.work[3 + 2 * pair], g0, n_done);
             // every role is done with the item (its stages, q and rows); the epilogue's
             // shared-memory writes are ordered before the next item's TMA writes to the stages
             fence_proxy_async_smem();
@@ -477,7 +500,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const __grid_con
         b = rank_pick;
     }
     int n_done = 0;
-    decode_unit<T, DP, MG, NT, STAGES>(tm_k, tm_v, p, smem, b, (int)blockIdx.y % p.Hkv, (int)blockIdx.x, 0, n_done);
+    run_unit(b, (int)blockIdx.y % p.Hkv, (int)blockIdx.x, 0, n_done);
 }
 
 }  // namespace pa
