@@ -135,3 +135,18 @@ def test_work_list_with_bias_and_window(wl):
                                 window_right=0)
     _gpu.check_layout(lay, limit=4096, alibi=_gpu.alibi_slopes(8, "random", seed=5))
 
+
+
+@pytest.mark.parametrize("D,batch,long_n,wl,bias", [(128, 12, 2, -1, False), (128, 60, 3, -1, False),
+                                                     (64, 200, 2, 300, False), (256, 40, 2, -1, True),
+                                                     (128, 300, 0, -1, False)])
+def test_two_group_kernel_with_narrow_units(D, batch, long_n, wl, bias):
+    """G = 8: q_len 1 gives 8 rows, q_len 4 gives 32, so the plan runs the two-row-group
+    decode kernel, and every unit of 16 rows or fewer takes the one-group body on the same
+    shared-memory layout.  The batches cover the grid of CTAs (12, 300 sequences), the
+    persistent work list with split sequences (60, 200, 40), a window and the bias."""
+    lay = skewed_layout(batch, seed=40 + batch + D, H=16, Hkv=2, D=D, long_n=long_n, long_k=9000, q4_frac=0.25,
+                        short_hi=1500)
+    lay.window_left = wl
+    alibi = _gpu.alibi_slopes(16, "random", seed=batch) if bias else None
+    _gpu.check_layout(lay, alibi=alibi, limit=2048)
