@@ -103,36 +103,8 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap& tm_k, const CUten
         row_dg[tid] = dg;
         row_ab[tid] = ab;
     }
-    if (tid < 128) {  // q rows -> shared memory (128-byte swizzled rows, zero padded); each
-                      // thread issues its loads in batches ahead of their stores
-        const T* q = static_cast<const T*>(p.q);
-        constexpr int UNITS = DP / 8;
-        constexpr int QI = (M * UNITS + 127) / 128;
-        constexpr int QB = QI < 4 ? QI : 4;
-        uint8_t* qs = smem + C::OFF_Q;
-#pragma unroll
-        for (int j0 = 0; j0 < QI; j0 += QB) {
-            int4 val[QB];
-#pragma unroll
-            for (int j = 0; j < QB; ++j) {
-                const int idx = tid + (j0 + j) * 128;
-                const int r = idx / UNITS, u = idx - r * UNITS;
-                val[j] = make_int4(0, 0, 0, 0);
-                if (idx < M * UNITS && r < tv.rows && u * 8 < p.D) {
-                    const int rho = tv.row0 + r;
-                    const int i = rho / p.G, g = rho - i * p.G;
-                    val[j] = __ldg(reinterpret_cast<const int4*>(q + (int64_t)(tv.q0 + i) * p.q_s0 +
-                                                                 (int64_t)(hk * p.G + g) * p.q_s1 + u * 8));
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < QB; ++j) {
-                const int idx = tid + (j0 + j) * 128;
-                const int r = idx / UNITS, u = idx - r * UNITS;
-                if (idx < M * UNITS) *reinterpret_cast<int4*>(qs + (u >> 3) * (M * 128) + swz128(r, u & 7)) = val[j];
-            }
-        }
-    }
+    // rows (and, for a CTA's first unit, the barrier set-up) visible to every role; the
+    // producer starts its loads at once, the consumers stage q meanwhile
     __syncthreads();
 
     if (warp == 4) {
@@ -188,6 +160,38 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap& tm_k, const CUten
         }
         return;  // the consumers synchronise among themselves with named barrier 1
     }
+
+    {  // q rows -> shared memory (128-byte swizzled rows, zero padded), by the 128 consumer
+       // threads, each issuing its loads in batches ahead of their stores
+        const T* q = static_cast<const T*>(p.q);
+        constexpr int UNITS = DP / 8;
+        constexpr int QI = (M * UNITS + 127) / 128;
+        constexpr int QB = QI < 4 ? QI : 4;
+        uint8_t* qs = smem + C::OFF_Q;
+#pragma unroll
+        for (int j0 = 0; j0 < QI; j0 += QB) {
+            int4 val[QB];
+#pragma unroll
+            for (int j = 0; j < QB; ++j) {
+                const int idx = tid + (j0 + j) * 128;
+                const int r = idx / UNITS, u = idx - r * UNITS;
+                val[j] = make_int4(0, 0, 0, 0);
+                if (idx < M * UNITS && r < tv.rows && u * 8 < p.D) {
+                    const int rho = tv.row0 + r;
+                    const int i = rho / p.G, g = rho - i * p.G;
+                    val[j] = __ldg(reinterpret_cast<const int4*>(q + (int64_t)(tv.q0 + i) * p.q_s0 +
+                                                                 (int64_t)(hk * p.G + g) * p.q_s1 + u * 8));
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < QB; ++j) {
+                const int idx = tid + (j0 + j) * 128;
+                const int r = idx / UNITS, u = idx - r * UNITS;
+                if (idx < M * UNITS) *reinterpret_cast<int4*>(qs + (u >> 3) * (M * 128) + swz128(r, u & 7)) = val[j];
+            }
+        }
+    }
+    named_barrier_sync(1, 128);  // q staged
 
     // ---------------- consumers ----------------
     const int rg = warp / C::KW, kq = warp % C::KW;

@@ -127,36 +127,8 @@ __global__ void __launch_bounds__(WideCfg<MG, STAGES>::THREADS, 1)
         *abort_flag = 0u;
         fence_mbar_init();
     }
-    {  // q rows -> the exchange area (128-byte swizzled rows, zero padded), read once below;
-       // each thread issues its loads in batches ahead of their stores
-        const T* q = static_cast<const T*>(p.q);
-        constexpr int UNITS = DP / 8;
-        constexpr int QI = (M * UNITS + C::THREADS - 1) / C::THREADS;
-        uint8_t* qs = smem + C::OFF_X;
-        constexpr int QB = QI < 3 ? QI : 3;  // loads in flight per batch
-#pragma unroll
-        for (int j0 = 0; j0 < QI; j0 += QB) {
-            int4 val[QB];
-#pragma unroll
-            for (int j = 0; j < QB; ++j) {
-                const int idx = tid + (j0 + j) * C::THREADS;
-                const int r = idx / UNITS, u = idx - r * UNITS;
-                val[j] = make_int4(0, 0, 0, 0);
-                if (idx < M * UNITS && r < tv.rows && u * 8 < p.D) {
-                    const int rho = tv.row0 + r;
-                    const int i = rho / p.G, g = rho - i * p.G;
-                    val[j] = __ldg(reinterpret_cast<const int4*>(q + (int64_t)(tv.q0 + i) * p.q_s0 +
-                                                                 (int64_t)(hk * p.G + g) * p.q_s1 + u * 8));
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < QB; ++j) {
-                const int idx = tid + (j0 + j) * C::THREADS;
-                const int r = idx / UNITS, u = idx - r * UNITS;
-                if (idx < M * UNITS) *reinterpret_cast<int4*>(qs + (u >> 3) * (M * 128) + swz128(r, u & 7)) = val[j];
-            }
-        }
-    }
+    // rows and barriers visible to every role; the producers start their loads at once, the
+    // consumers stage q meanwhile
     __syncthreads();
 
     if (warp >= C::CONS) {
@@ -202,6 +174,38 @@ __global__ void __launch_bounds__(WideCfg<MG, STAGES>::THREADS, 1)
         }
         return;  // the consumers synchronise among themselves with named barriers 1..3
     }
+
+    {  // q rows -> the exchange area (128-byte swizzled rows, zero padded), read once below, by
+       // the consumer threads, each issuing its loads in batches ahead of their stores
+        const T* q = static_cast<const T*>(p.q);
+        constexpr int UNITS = DP / 8;
+        constexpr int QI = (M * UNITS + C::CONS * 32 - 1) / (C::CONS * 32);
+        uint8_t* qs = smem + C::OFF_X;
+        constexpr int QB = QI < 4 ? QI : 4;  // loads in flight per batch
+#pragma unroll
+        for (int j0 = 0; j0 < QI; j0 += QB) {
+            int4 val[QB];
+#pragma unroll
+            for (int j = 0; j < QB; ++j) {
+                const int idx = tid + (j0 + j) * (C::CONS * 32);
+                const int r = idx / UNITS, u = idx - r * UNITS;
+                val[j] = make_int4(0, 0, 0, 0);
+                if (idx < M * UNITS && r < tv.rows && u * 8 < p.D) {
+                    const int rho = tv.row0 + r;
+                    const int i = rho / p.G, g = rho - i * p.G;
+                    val[j] = __ldg(reinterpret_cast<const int4*>(q + (int64_t)(tv.q0 + i) * p.q_s0 +
+                                                                 (int64_t)(hk * p.G + g) * p.q_s1 + u * 8));
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < QB; ++j) {
+                const int idx = tid + (j0 + j) * (C::CONS * 32);
+                const int r = idx / UNITS, u = idx - r * UNITS;
+                if (idx < M * UNITS) *reinterpret_cast<int4*>(qs + (u >> 3) * (M * 128) + swz128(r, u & 7)) = val[j];
+            }
+        }
+    }
+    named_barrier_sync(1, C::CONS * 32);  // q staged
 
     // ---------------- consumers ----------------
     const int dq = warp & 3, grp = warp >> 2;
