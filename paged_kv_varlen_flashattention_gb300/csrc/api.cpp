@@ -664,10 +664,14 @@ SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, int num_sms)
     pl.work = !pl.tc && pl.row_tiles == 1 && pl.dp <= 256 && !force_generic && a.batch >= kWorkMinBatch &&
               a.batch <= kMaxOrderBatch && pl.max_splits > 1 && pl.slots > 0;
     // Otherwise the decode kernels launch sequences longest first (a one-CTA ranking pass)
-    // for batches they can rank; the order sits at the start of the scratch
+    // for batches they can rank; the order sits at the start of the scratch.  A grid that
+    // fits the resident slots runs as one wave, where the order is moot: its CTAs skip the
+    // ranking and its dependent memory round trip
     const bool decode_kernel = pl.tc || (pl.row_tiles == 1 && !force_generic);
-    pl.rank_in_cta = !pl.work && decode_kernel && a.batch >= 2 && a.batch <= kRankInCta;
-    pl.order_bytes = !pl.work && decode_kernel && a.batch > kRankInCta && a.batch <= kMaxOrderBatch
+    const bool one_wave = pl.slots > 0 && units * pl.max_splits <= pl.slots;
+    const bool ranked = !pl.work && decode_kernel && !one_wave;
+    pl.rank_in_cta = ranked && a.batch >= 2 && a.batch <= kRankInCta;
+    pl.order_bytes = ranked && a.batch > kRankInCta && a.batch <= kMaxOrderBatch
                          ? ((size_t)a.batch * sizeof(int) + 255) / 256 * 256
                          : 0;
     pl.work_bytes = pl.work ? ((2 + 2 * (size_t)a.batch * pl.max_splits) * sizeof(int) + 255) / 256 * 256 : 0;

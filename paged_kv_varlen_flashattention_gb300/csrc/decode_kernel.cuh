@@ -121,8 +121,6 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap& tm_k, const CUten
         }
         __syncwarp();
         if (lane == 0 && !p.withhold) {
-            prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v);
             const uint64_t policy = l2_policy_evict_first();
             for (int it = 0; it < n_iter; ++it) {
                 const int gi = g0 + it;  // position in the CTA's stream of tiles
@@ -427,6 +425,10 @@ __global__ void __launch_bounds__(kDecodeThreads, DP <= 64 ? 3 : DP <= 128 ? 2 :
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x;
     allow_dependent_launch();
+    if (tid == 128) {  // the producer lane: descriptors on their way at once
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+    }
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* empty = full + STAGES;
     volatile uint32_t* abort_flag = reinterpret_cast<uint32_t*>(smem + C::OFF_FLAG);
@@ -503,6 +505,7 @@ __global__ void __launch_bounds__(kDecodeThreads, DP <= 64 ? 3 : DP <= 128 ? 2 :
         __syncthreads();
         b = rank_pick;
     }
+    if (tid >= 128) prefetch_split_pages<NT>(p, b, (int)blockIdx.x, tid - 128);  // overlaps tile_view's loads
     int n_done = 0;
     run_unit(b, (int)blockIdx.y % p.Hkv, (int)blockIdx.x, 0, n_done);
 }

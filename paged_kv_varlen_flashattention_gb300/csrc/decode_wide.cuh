@@ -64,6 +64,10 @@ __global__ void __launch_bounds__(WideCfg<MG, STAGES>::THREADS, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     allow_dependent_launch();
+    if (tid == C::CONS * 32) {  // the first producer lane: descriptors on their way at once
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+    }
     // sequences longest first, as in the warp-sliced decode kernel
     __shared__ int rank_len[kRankInCta];
     __shared__ int rank_pick;
@@ -87,6 +91,7 @@ __global__ void __launch_bounds__(WideCfg<MG, STAGES>::THREADS, 1)
         b = rank_pick;
     }
     const int hk = blockIdx.y % p.Hkv, split = blockIdx.x;
+    if (warp == C::CONS) prefetch_split_pages<NT>(p, b, split, lane);  // overlaps tile_view's loads
 
     TileView tv;
     if (!tile_view<M, NT>(p, b, 0, tv, split == 0)) return;
@@ -135,8 +140,6 @@ __global__ void __launch_bounds__(WideCfg<MG, STAGES>::THREADS, 1)
         // ---------------- producers: warp pw issues chunks 2 pw and 2 pw + 1 ----------------
         const int pw = warp - C::CONS;
         if (lane == 0 && !p.withhold) {
-            prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v);
             const uint64_t policy = l2_policy_evict_first();
             const int c_a = 2 * pw, c_b = 2 * pw + 1;
             const bool has_a = c_a * 64 < p.D, has_b = c_b * 64 < p.D;

@@ -110,6 +110,20 @@ __device__ __forceinline__ bool tile_view(const SplitParams& p, int b, int rt, T
     return true;
 }
 
+// At a CTA's entry, before its sequence's lengths are known: lane `lane` of a warp hints the
+// `lane`-th 128-byte line of the block-table entries of split `split` into L2, taking the
+// sequence's keys to start at tile 0 (no left window), so that the producer's lookups after
+// tile_view find them there instead of in HBM.  Every address stays inside row b of the
+// table whatever the lengths turn out to be.
+template <int NT>
+__device__ __forceinline__ void prefetch_split_pages(const SplitParams& p, int b, int split, int lane) {
+    if (!p.paged || b < 0 || b >= p.batch || p.bt_cols <= 0) return;
+    const int64_t first = (int64_t)split * p.split_tiles * NT / p.P;
+    const int64_t last = min64(((int64_t)(split + 1) * p.split_tiles * NT - 1) / p.P, (int64_t)p.bt_cols - 1);
+    const int64_t page = first + 32 * (int64_t)lane;
+    if (page <= last) prefetch_l2(p.bt + (int64_t)b * p.bt_s0 + page);
+}
+
 // NW warps: 4, each taking a quarter of the tile's keys in Q.K^T over the whole head dim;
 // or 8 for the widest heads, each taking every key of the tile over one eighth of the head
 // dim (4 k-steps: eight independent accumulator chains of 4 MMAs instead of two chains of

@@ -78,9 +78,14 @@ def test_alibi():
     _gpu.check_layout(lay, alibi=_gpu.alibi_slopes(8))
 
 
-def test_ranked_in_cta_and_by_pass():
-    """40 sequences (ranked inside every CTA) and 300 (the ranking pass's order in the scratch)."""
+@pytest.mark.parametrize("tiles", [None, "8"])
+def test_ranked_in_cta_and_by_pass(tiles, monkeypatch):
+    """40 sequences (one wave of 120 CTAs in index order with the plan's splits; ranked
+    inside every CTA over the 480 CTAs of 8-tile splits) and 300 (the ranking pass's order
+    in the scratch)."""
     from tests.test_large_batch_gpu import skewed_layout
+    if tiles:
+        monkeypatch.setenv("PA_SPLIT_TILES", tiles)
     _gpu.check_layout(skewed_layout(40, seed=84, H=8, Hkv=1, D=512, long_n=2, long_k=3000, short_hi=300),
                       limit=2048)
     _gpu.check_layout(skewed_layout(300, seed=85, H=16, Hkv=2, D=512, long_k=5000, short_hi=300), limit=2048)

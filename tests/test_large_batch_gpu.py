@@ -6,7 +6,7 @@ the device, longest sequences first, and persistent CTAs take them in turn (the 
 at the start of the call's scratch, the split partial results after it).  Otherwise it
 ranks batches of up to 160 sequences inside every CTA, batches of 161 to 1,024 through a
 separate one-CTA ranking pass whose order sits at the start of the scratch, and keeps the
-index order above 1,024.  These cases reach each branch on
+index order above 1,024 and for grids that fit one wave of resident CTAs.  These cases reach each branch on
 both sides of its bounds, with skewed lengths (a few sequences far longer than the rest),
 q_len 1 and 4 mixed in one batch, sequences with fewer keys than queries (rows that attend
 nothing), a few prefill-class sequences in the same batch, and NaN in every cache slot
@@ -55,8 +55,13 @@ def test_ranking_without_splits(batch):
     _gpu.check_layout(skewed_layout(batch, seed=37, long_n=2, long_k=6000, short_hi=2000), limit=2048)
 
 
-def test_in_cta_ranking_with_splits_small_batch():
-    """Below 16 sequences the split plan keeps the grid of (split, kv head, rank) CTAs."""
+@pytest.mark.parametrize("tiles", [None, "8"])
+def test_in_cta_ranking_with_splits_small_batch(tiles, monkeypatch):
+    """Below 16 sequences the split plan keeps the grid of (split, kv head, sequence) CTAs:
+    the plan's own splits fill one wave of resident CTAs (index order); 8-tile splits make
+    several waves, ranked inside every CTA."""
+    if tiles:
+        monkeypatch.setenv("PA_SPLIT_TILES", tiles)
     _gpu.check_layout(skewed_layout(12, seed=38, long_n=2, long_k=30000, short_hi=700), limit=2048)
 
 
