@@ -10,10 +10,15 @@
 //   * each warp forms the partial scores of its rows and keys over its 128 columns
 //     (Q fragments held in registers, K fragments from the TMA-swizzled stage);
 //   * the four quarter warps of a group exchange their fp32 partials through a
-//     double-buffered shared-memory slot and a 128-thread named barrier, and every one of
-//     them sums the four in the same order, so all four hold identical scores;
-//   * each runs the online softmax of its rows (quad shuffles only) and accumulates
-//     P.V for its 128 output columns, then releases the stage.
+//     double-buffered shared-memory slot and a 128-thread named barrier.  With 32 rows (one
+//     group per 16 rows, all 32 keys) the exchange is a reduce-scatter: warp dq sums the
+//     partials of the 8 keys 8 dq .. 8 dq + 7 only, runs the softmax of those keys and posts
+//     their probabilities (in the precision of V) and its row maxima; after a second barrier
+//     every warp reads the whole P tile.  The four warps share one running reference per
+//     row, raised (and O rescaled) only when some key exceeds it by more than 2^8, a
+//     decision all four take from the same posted maxima.  With 16 rows (two key halves)
+//     every warp sums all four partials of its 16 keys in quarter order;
+//   * each accumulates P.V for its 128 output columns, then releases the stage.
 // Four producer warps feed a three-stage ring of 64 KB K/V tiles with TMA: warp p issues
 // the 64-column chunks 2p and 2p + 1 of K and V and posts its own bytes on the stage's
 // full barrier before issuing them (one TMA issuing thread per warp keeps the per-thread
@@ -40,9 +45,18 @@ struct WideCfg {
     static constexpr int QW = 128;                // output columns per warp
     static constexpr int TILE_BYTES = CH * NT * 128;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-    static constexpr int XBUF_BYTES = CONS * NSC * 32 * 16;  // one float4 per (warp, score tile, lane)
+    // Score exchange per tile (two buffers, alternating by tile).  Two key slices (16 rows):
+    // one float4 per (warp, score tile, lane).  One slice (32 rows): a reduce-scatter, where
+    // warp dq owns score tile dq (keys 8 dq .. 8 dq + 7) and receives the other three quarters'
+    // partials of it (one float4 per (warp, slot, lane)), then posts its probabilities in the
+    // precision of V (one pair of words per (warp, lane)) and its rows' maxima.
+    static constexpr int XS_BYTES = CONS * 3 * 32 * 16;
+    static constexpr int XP_OFF = XS_BYTES;
+    static constexpr int XM_OFF = XP_OFF + CONS * 32 * 8;
+    static constexpr int XBUF_BYTES = KW == 2 ? CONS * NSC * 32 * 16 : XM_OFF + 2 * 16 * 4 * 4;
     static constexpr int Q_BYTES = CH * M * 128;
     static constexpr int X_BYTES = 2 * XBUF_BYTES > Q_BYTES ? 2 * XBUF_BYTES : Q_BYTES;
+    static_assert(KW == 2 || NSC == 4, "one score tile per quarter warp");
     static constexpr int OFF_X = STAGES * STAGE_BYTES;        // Q staging, then the score exchange
     static constexpr int OFF_ROW = OFF_X + X_BYTES;           // row_lo[M], row_hi[M], row_dg[M], row_ab[M]
     static constexpr int OFF_BAR = OFF_ROW + 4 * M * 4;
@@ -267,6 +281,7 @@ __global__ void __launch_bounds__(WideCfg<MG, STAGES>::THREADS, 1)
         uint8_t* kst = smem + stage * C::STAGE_BYTES;
         uint8_t* vst = kst + C::TILE_BYTES;
         const uint32_t xb = smem_addr(smem + C::OFF_X + (it & 1) * C::XBUF_BYTES);
+        float pr[4];  // one-slice layout: this warp's probabilities (keys 8 dq + 2 tq, + 1; rows r0, r1)
         float s[C::NSC][4];
 #pragma unroll
         for (int n = 0; n < C::NSC; ++n)
@@ -301,15 +316,114 @@ __global__ void __launch_bounds__(WideCfg<MG, STAGES>::THREADS, 1)
                     }
                 }
             }
+            if constexpr (C::KW == 1) {
+                // the partials of the three score tiles other quarters own
 #pragma unroll
-            for (int n = 0; n < C::NSC; ++n)
-                st_shared_f4(xb + ((warp * C::NSC + n) * 32 + lane) * 16, make_float4(s[n][0], s[n][1], s[n][2], s[n][3]));
+                for (int n = 0; n < C::NSC; ++n)
+                    if (n != dq)
+                        st_shared_f4(xb + ((warp * 3 + (n < dq ? n : n - 1)) * 32 + lane) * 16,
+                                     make_float4(s[n][0], s[n][1], s[n][2], s[n][3]));
+            } else {
+#pragma unroll
+                for (int n = 0; n < C::NSC; ++n)
+                    st_shared_f4(xb + ((warp * C::NSC + n) * 32 + lane) * 16,
+                                 make_float4(s[n][0], s[n][1], s[n][2], s[n][3]));
+            }
         }
         // every quarter of the group has posted its partial (or one of them gave up)
         if (named_barrier_or(2 + grp, 128, !ok)) {
             stopped = true;
             break;
         }
+        if constexpr (C::KW == 1) {
+            // score tile dq: the four quarters' partials in quarter order
+            float t4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int w4 = 0; w4 < 4; ++w4) {
+                float v[4];
+                if (w4 == dq) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        v[e] = dq == 0 ? s[0][e] : dq == 1 ? s[1][e] : dq == 2 ? s[2][e] : s[3][e];
+                } else {
+                    const float4 x = ld_shared_f4(xb + (((grp * 4 + w4) * 3 + (dq < w4 ? dq : dq - 1)) * 32 + lane) * 16);
+                    v[0] = x.x;
+                    v[1] = x.y;
+                    v[2] = x.z;
+                    v[3] = x.w;
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) t4[e] += v[e];
+            }
+            const bool inside = !p.alibi && kt >= wlo && kt + NT - 1 <= whi;
+            if (inside) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) t4[e] *= p.scale_log2;
+            } else {
+                const int lo0 = row_lo[r0], hi0 = row_hi[r0], lo1 = row_lo[r1], hi1 = row_hi[r1];
+                const int dg0 = row_dg[r0], dg1 = row_dg[r1];
+                const float ab0 = row_ab[r0], ab1 = row_ab[r1];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const bool up = e < 2;
+                    const int key = kt + dq * 8 + tq * 2 + (e & 1);
+                    const bool in = up ? (key >= lo0 && key <= hi0) : (key >= lo1 && key <= hi1);
+                    t4[e] = in ? biased_log2(t4[e], p.scale_log2, up ? ab0 : ab1, up ? dg0 : dg1, key) : -INFINITY;
+                }
+            }
+            float mx0 = fmaxf(t4[0], t4[1]), mx1 = fmaxf(t4[2], t4[3]);
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            // probabilities against the current reference, posted with the rows' maxima
+            const uint32_t xp = xb + C::XP_OFF + (warp * 32 + lane) * 8;
+            const uint32_t xm = xb + C::XM_OFF + (grp * 16 + gq) * 16;
+            {
+                const float u0 = m0 == -INFINITY ? 0.f : m0, u1 = m1 == -INFINITY ? 0.f : m1;
+                pr[0] = fast_exp2(t4[0] - u0);
+                pr[1] = fast_exp2(t4[1] - u0);
+                pr[2] = fast_exp2(t4[2] - u1);
+                pr[3] = fast_exp2(t4[3] - u1);
+                st_shared_u2(xp, pack2<T>(pr[0], pr[1]), pack2<T>(pr[2], pr[3]));
+                if (tq == 0) {
+                    st_shared_f(xm + dq * 4, mx0);
+                    st_shared_f(xm + 8 * 16 + dq * 4, mx1);
+                }
+            }
+            named_barrier_sync(2 + grp, 128);
+            // every row's maximum over the tile; above the reference by more than 2^8 (or a
+            // first finite score): all four quarters raise it, rescale and post P again
+            const float4 g0 = ld_shared_f4(xm), g1 = ld_shared_f4(xm + 8 * 16);
+            const float n0 = fmaxf(m0, fmaxf(fmaxf(g0.x, g0.y), fmaxf(g0.z, g0.w)));
+            const float n1 = fmaxf(m1, fmaxf(fmaxf(g1.x, g1.y), fmaxf(g1.z, g1.w)));
+            const bool raise0 = m0 == -INFINITY ? n0 > m0 : n0 > m0 + 8.f;
+            const bool raise1 = m1 == -INFINITY ? n1 > m1 : n1 > m1 + 8.f;
+            if (__any_sync(0xffffffffu, raise0 || raise1)) {  // the same decision in all four warps
+                const float a0 = (n0 == -INFINITY) ? 1.f : fast_exp2(m0 - n0);
+                const float a1 = (n1 == -INFINITY) ? 1.f : fast_exp2(m1 - n1);
+#pragma unroll
+                for (int n = 0; n < C::QW / 8; ++n) {
+                    o[n][0] *= a0;
+                    o[n][1] *= a0;
+                    o[n][2] *= a1;
+                    o[n][3] *= a1;
+                }
+                l0 *= a0;
+                l1 *= a1;
+                m0 = n0;
+                m1 = n1;
+                const float u0 = m0 == -INFINITY ? 0.f : m0, u1 = m1 == -INFINITY ? 0.f : m1;
+                pr[0] = fast_exp2(t4[0] - u0);
+                pr[1] = fast_exp2(t4[1] - u0);
+                pr[2] = fast_exp2(t4[2] - u1);
+                pr[3] = fast_exp2(t4[3] - u1);
+                st_shared_u2(xp, pack2<T>(pr[0], pr[1]), pack2<T>(pr[2], pr[3]));  // no quarter reads P yet
+                named_barrier_sync(2 + grp, 128);
+            }
+            l0 += pr[0] + pr[1];  // this quarter's keys; the quarters' sums are added at the end
+            l1 += pr[2] + pr[3];
+        } else {
         // full scores: the four partials in quarter order (identical in all four warps)
 #pragma unroll
         for (int n = 0; n < C::NSC; ++n) {
@@ -385,16 +499,26 @@ __global__ void __launch_bounds__(WideCfg<MG, STAGES>::THREADS, 1)
             l0 += s[n][0] + s[n][1];
             l1 += s[n][2] + s[n][3];
         }
+        }
         // O += P V over this warp's 128 columns; the score fragments of two n8 tiles are
         // the A fragment of one k16 step
         const uint32_t v_base = smem_addr(vst);
 #pragma unroll
         for (int kc = 0; kc < C::KPW / 16; ++kc) {
             uint32_t pa[4];
-            pa[0] = pack2<T>(s[2 * kc][0], s[2 * kc][1]);
-            pa[1] = pack2<T>(s[2 * kc][2], s[2 * kc][3]);
-            pa[2] = pack2<T>(s[2 * kc + 1][0], s[2 * kc + 1][1]);
-            pa[3] = pack2<T>(s[2 * kc + 1][2], s[2 * kc + 1][3]);
+            if constexpr (C::KW == 1) {  // score tiles 2 kc and 2 kc + 1, as their quarters posted them
+                const uint2 x = ld_shared_u2(xb + C::XP_OFF + ((grp * 4 + 2 * kc) * 32 + lane) * 8);
+                const uint2 y = ld_shared_u2(xb + C::XP_OFF + ((grp * 4 + 2 * kc + 1) * 32 + lane) * 8);
+                pa[0] = x.x;
+                pa[1] = x.y;
+                pa[2] = y.x;
+                pa[3] = y.y;
+            } else {
+                pa[0] = pack2<T>(s[2 * kc][0], s[2 * kc][1]);
+                pa[1] = pack2<T>(s[2 * kc][2], s[2 * kc][3]);
+                pa[2] = pack2<T>(s[2 * kc + 1][0], s[2 * kc + 1][1]);
+                pa[3] = pack2<T>(s[2 * kc + 1][2], s[2 * kc + 1][3]);
+            }
             const int key = key0 + kc * 16 + rr + ((mi & 1) << 3);
 #pragma unroll
             for (int np = 0; np < C::QW / 16; ++np) {
@@ -417,6 +541,18 @@ __global__ void __launch_bounds__(WideCfg<MG, STAGES>::THREADS, 1)
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
     // every consumer is done with the stages (reused below); stop together if any role gave up
     if (named_barrier_or(1, C::CONS * 32, stopped || *abort_flag != 0u)) return;
+    if constexpr (C::KW == 1) {
+        // each quarter summed its own keys' probabilities: the four sums in quarter order
+        const uint32_t xl = smem_addr(smem + C::OFF_X) + (grp * 16 + gq) * 16;  // [group][row][quarter]
+        if (tq == 0) {
+            st_shared_f(xl + dq * 4, l0);
+            st_shared_f(xl + 8 * 16 + dq * 4, l1);
+        }
+        named_barrier_sync(1, C::CONS * 32);
+        const float4 a = ld_shared_f4(xl), c = ld_shared_f4(xl + 8 * 16);
+        l0 = (a.x + a.y) + (a.z + a.w);
+        l1 = (c.x + c.y) + (c.z + c.w);
+    }
     if constexpr (C::KW == 2) {
         // 16-row CTA: the warp of the second key half hands its (O, m, l) to the warp of the
         // first, lane for lane (both hold the same rows and columns)

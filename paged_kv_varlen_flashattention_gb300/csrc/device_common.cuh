@@ -133,6 +133,17 @@ __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
                  : "memory");
     return v;
 }
+__device__ __forceinline__ void st_shared_f(uint32_t addr, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_shared_u2(uint32_t addr, uint32_t x, uint32_t y) {
+    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ uint2 ld_shared_u2(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+    return v;
+}
 
 // ---- TMA ---------------------------------------------------------------------------------
 // Tiled 4-D tensor load into shared memory, completing on `bar` (complete_tx bytes).
