@@ -7,8 +7,9 @@ every tile and are merged at the end.  These cases cover both row counts with pa
 head dims that leave quarters partly or wholly empty (264, 320, 448), every page size, the
 windows (tiles inside every row's interval skip the mask), forced split counts with the
 combine, more queries than keys (rows that attend nothing), fp16, the position bias, the
-non-paged mode, a batch ranked by the separate pass and the long-context workload at full
-size.  The caches hold NaN in every slot no sequence owns.  All rows are compared at the
+non-paged mode, a batch ranked by the separate pass, scores rising in steps along the keys
+(every row's running reference raised many times inside a split) and the long-context
+workload at full size.  The caches hold NaN in every slot no sequence owns.  All rows are compared at the
 stated tolerances."""
 import pytest
 
@@ -93,3 +94,34 @@ def test_ranked_in_cta_and_by_pass(tiles, monkeypatch):
 
 def test_long_context_full_size():
     _gpu.check_layout(workloads.CONFIGS["long_d512_bf16"](), limit=256)
+
+
+@pytest.mark.parametrize("G,q", [(8, 4), (4, 1)])
+def test_scores_rising_in_steps(G, q, monkeypatch):
+    """Scores that jump by about 10 (in log2 units) every 64 keys: every row's running
+    reference is raised many times inside one split, and with 32 rows the four quarter
+    warps of a group, each holding the softmax of its own 8 keys of a tile, must raise it
+    together; with 16 rows (two key halves) the halves are merged at the end.  q is all
+    ones, key j of a sequence is N(0, 0.1^2) + 0.3 floor(j / 64) in every column; the plan's
+    own splits, then forced 3-tile splits; every row compared with the oracle."""
+    import torch
+    sks = [700, 1000]
+    lay = _lay([q, q], sks, H=2 * G, Hkv=2, D=512, seed=91)
+    inp = workloads.materialize(lay, device="cuda").to("cuda")
+    gen = torch.Generator(device="cuda").manual_seed(91)
+    inp.q.fill_(1.0)
+    P = lay.page_block_size
+    for b, sk in enumerate(sks):
+        for page in range((sk + P - 1) // P):
+            blk = int(lay.block_table[b, page])
+            n = min(P, sk - page * P)
+            keys = torch.arange(page * P, page * P + n, device="cuda")
+            ramp = (0.3 * torch.div(keys, 64, rounding_mode="floor")).view(n, 1, 1)
+            noise = torch.randn((n, lay.num_heads_k, lay.head_dim), generator=gen, device="cuda") * 0.1
+            inp.k_cache[blk, :n] = (ramp + noise).to(inp.k_cache.dtype)
+    ref_o, ref_l = _gpu.oracle_for(inp.to("cpu"))
+    for tiles in (None, "3"):
+        if tiles:
+            monkeypatch.setenv("PA_SPLIT_TILES", tiles)
+        out, lse = _gpu.run_cuda(inp)
+        _gpu.compare(lay, out, lse, ref_o, ref_l)
