@@ -98,23 +98,29 @@ def load():
     return _lib
 
 
+_DTYPE_CODES = None
+
+
 def _dtype_code(t) -> int:
-    import torch
-    return {torch.float16: PA_F16, torch.bfloat16: PA_BF16, torch.float32: PA_F32, torch.int32: PA_I32}.get(t.dtype, -1)
+    global _DTYPE_CODES
+    if _DTYPE_CODES is None:
+        import torch
+        _DTYPE_CODES = {torch.float16: PA_F16, torch.bfloat16: PA_BF16, torch.float32: PA_F32, torch.int32: PA_I32}
+    return _DTYPE_CODES.get(t.dtype, -1)
+
+
+_I64x4 = ctypes.c_int64 * 4
 
 
 def describe(t) -> Optional[PaTensor]:
     """A pa_tensor descriptor borrowing a torch tensor's storage (None stays None)."""
     if t is None:
         return None
-    d = PaTensor()
-    d.data = t.data_ptr()
-    d.dtype = _dtype_code(t)
-    d.ndim = t.dim()
-    for i in range(min(t.dim(), 4)):
-        d.shape[i] = t.shape[i]
-        d.stride[i] = t.stride(i)
-    return d
+    shape, stride = t.shape, t.stride()
+    n = len(shape)
+    if n >= 4:
+        return PaTensor(t.data_ptr(), _dtype_code(t), n, _I64x4(*shape[:4]), _I64x4(*stride[:4]))
+    return PaTensor(t.data_ptr(), _dtype_code(t), n, _I64x4(*shape), _I64x4(*stride))
 
 
 def _ref(d):
