@@ -374,39 +374,57 @@ def time_device(binding, g, lay, steps, warmup, dist, flush=None):
 
 def time_e2e(binding, g, lay, steps, warmup):
     """Same step through the public call with host-resident inputs: pinned host -> device
-    copies of every input, the call, and device -> host copies of out and lse, all timed."""
+    copies of every input, the call, and device -> host copies of out and lse, all timed.
+    The inputs alternate between two device buffer sets, and their copies run on a copy
+    stream, so that step i + 1's copies (the host link is the limit: ~210 GB/s pinned, one
+    stream or several alike) overlap step i's call; a set is overwritten only after the
+    call that read it has finished."""
     import torch
     sl = _slopes_on("cpu")
     host = [t.cpu().pin_memory() if t is not None else None
             for t in (g.q, g.k_cache, g.v_cache, g.cu_seqlens_q, g.cu_seqlens_k, g.block_table, sl)]
-    dev = [torch.empty_like(t, device="cuda") if t is not None else None for t in host]
+    sets = [[torch.empty_like(t, device="cuda") if t is not None else None for t in host] for _ in range(2)]
     out_h = torch.empty(g.q.shape, dtype=g.q.dtype).pin_memory()
     lse_h = torch.empty((lay.num_heads, lay.total_q), dtype=torch.float32).pin_memory()
-    out_d = torch.empty_like(g.q)
-    lse_d = torch.empty((lay.num_heads, lay.total_q), dtype=torch.float32, device="cuda")
+    outs = [(torch.empty_like(g.q), torch.empty((lay.num_heads, lay.total_q), dtype=torch.float32, device="cuda"))
+            for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host if t is not None)
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+    main = torch.cuda.current_stream()
+    copy_stream = torch.cuda.Stream()
+    read_done = [None, None]  # event after the last call that read buffer set s
 
-    def step():
-        for d, h in zip(dev, host):
-            if d is not None:
-                d.copy_(h, non_blocking=True)
+    def step(i):
+        s = i % 2
+        dev = sets[s]
+        with torch.cuda.stream(copy_stream):
+            if read_done[s] is not None:
+                copy_stream.wait_event(read_done[s])
+            for d, h in zip(dev, host):
+                if d is not None:
+                    d.copy_(h, non_blocking=True)
+            copied = torch.cuda.Event()
+            copied.record(copy_stream)
+        main.wait_event(copied)
         binding.varlen_fwd(dev[0], dev[1], dev[2], dev[3], dev[4], dev[5], max_seqlen_q=lay.max_seqlen_q,
                            max_seqlen_k=lay.max_seqlen_k, softmax_scale=lay.softmax_scale,
-                           window_left=lay.window_left, window_right=lay.window_right, out=out_d,
-                           softmax_lse=lse_d, alibi_slopes=dev[6])
-        out_h.copy_(out_d, non_blocking=True)
-        lse_h.copy_(lse_d, non_blocking=True)
+                           window_left=lay.window_left, window_right=lay.window_right, out=outs[s][0],
+                           softmax_lse=outs[s][1], alibi_slopes=dev[6])
+        ev = torch.cuda.Event()
+        ev.record(main)
+        read_done[s] = ev
+        out_h.copy_(outs[s][0], non_blocking=True)
+        lse_h.copy_(outs[s][1], non_blocking=True)
 
-    for _ in range(warmup):
-        step()
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        step()
-    e1.record(stream)
+    e0.record(main)
+    copy_stream.wait_event(e0)  # no copy of the timed steps starts before the start event
+    for i in range(steps):
+        step(i)
+    e1.record(main)
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / steps, h2d, d2h
 
