@@ -147,8 +147,9 @@ int pa_varlen_fwd(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor*
  * pa_varlen_fwd; the caller still provides every input and output.
  *
  * Scratch: split-KV partial results (and the decode launch order of batches of more than
- * 160 sequences, or the work list of batches of 16 or more that the plan splits, and the
- * prefill kernels' item counter) go to one fixed 32 MiB array compiled into the library
+ * 160 sequences whose grid takes more than one wave of resident CTAs, or the work list of
+ * batches of 16 or more that the plan splits, and the prefill kernels' item counter) go
+ * to one fixed 32 MiB array compiled into the library
  * (a static device array: every GPU that loads the library holds it until the process
  * exits) instead of the library's growable workspace.  A call whose split plan needs more
  * than 32 MiB is rejected with PA_ERR_WORKSPACE and a message giving both sizes.  The
