@@ -94,7 +94,9 @@ int prefill_rows_threshold();  // sequences with sq*G > this go to the prefill k
 constexpr size_t kPrefillCounterBytes = 256;
 int launch_prefill(const Args& a, int* counter, unsigned int* err, char* msg, size_t msg_len);
 
-SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, int num_sms);
+// `prefill_takes_long_rows`: rows of sequences with sq*G above the threshold belong to the
+// prefill kernel; `beside_prefill`: this pass runs while the prefill kernel holds the SMs.
+SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, bool beside_prefill, int num_sms);
 int launch_splitkv(const Args& a, const SplitPlan& plan, void* workspace, unsigned int* err, char* msg,
                    size_t msg_len);
 int launch_splitkv_bf16(const Args& a, const SplitPlan& plan, void* workspace, unsigned int* err, char* msg,
