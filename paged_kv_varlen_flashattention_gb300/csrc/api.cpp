@@ -599,7 +599,7 @@ bool decode_tc_wanted(int dp) {
     return dp >= 128 && env && env[0] == '1';
 }
 
-SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, bool beside_prefill, int num_sms) {
+SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, int prefill_sms, int num_sms) {
     SplitPlan pl{};
     pl.dp = a.D <= 64 ? 64 : a.D <= 128 ? 128 : a.D <= 256 ? 256 : 512;
     pl.nt = pl.dp == 512 ? 32 : 64;
@@ -635,14 +635,17 @@ SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, bool beside_
         // 5.72 with two splits per unit and 5.61 with three).  A split is never shorter than
         // 4 tiles, nor than 8 M keys: its fp32 partial result (M rows x D x 4 bytes, written
         // and read back) then costs at most ~1/8 of the K/V bytes it reads.  When this pass runs
-        // beside the prefill kernel (on the caller's stream while the prefill kernel runs on
-        // the side stream), the persistent prefill kernel takes every SM, so there are no free
-        // slots to fill: one CTA per unit (the key cap below
-        // still spreads a very long sequence), and no combine grid whose CTAs, empty when the
-        // batch is all prefill, would hold the SMs the prefill CTAs wait for (causal batch:
-        // prefill CTAs starting ~6.5 us into the call behind 4,096 empty combine CTAs).
-        const int64_t slots = pl.slots;
-        int64_t splits = units < slots && !beside_prefill ? slots / units : 1;
+        // beside a prefill kernel whose persistent grid may take every SM (its item bound,
+        // from the sizes alone, reaches the SM count), there are no free slots to fill: one
+        // CTA per unit (the key cap below still spreads a very long sequence) and no combine
+        // grid, whose CTAs, empty when the batch is all prefill, would hold the SMs the
+        // prefill CTAs wait for (causal batch: prefill CTAs starting ~6.5 us into the call
+        // behind 4,096 empty combine CTAs).  A smaller prefill grid leaves the plan as it is
+        // (the bound counts every sequence as prefill-class, so it overstates such a grid:
+        // one 64-query prompt beside four 8,000-key decode sequences measured 5 % slower
+        // when the split was sized to the SMs the bound left).
+        const int64_t slots = prefill_sms >= num_sms ? 0 : pl.slots;
+        int64_t splits = units < slots ? slots / units : 1;
         splits = std::max<int64_t>(1, std::min(splits, tiles_max));
         const int64_t min_tiles = std::max<int64_t>(4, (8ll * M + pl.nt - 1) / pl.nt);
         split_tiles = std::max<int64_t>(min_tiles, (tiles_max + splits - 1) / splits);
@@ -730,7 +733,11 @@ int launch_forward(pa::Args& a, void* stream, ScratchFn scratch, void* scratch_c
     if (ce != cudaSuccess) return fail(PA_ERR_CUDA, "error word: %s", cudaGetErrorString((cudaError_t)ce));
 
     const bool use_prefill = pa::prefill_supported(a);
-    const pa::SplitPlan plan = pa::plan_splitkv(a, use_prefill, use_prefill && side_stream_ok, sm_count());
+    // SMs the persistent prefill grid may hold beside the decode-class pass (it runs before
+    // that pass, not beside it, when there is no side stream)
+    const int prefill_sms =
+        use_prefill && side_stream_ok ? (int)std::min<int64_t>(sm_count(), pa::prefill_items_bound(a)) : 0;
+    const pa::SplitPlan plan = pa::plan_splitkv(a, use_prefill, prefill_sms, sm_count());
     // the prefill kernels' item counter follows the split-KV scratch
     const size_t counter_at = (plan.ws_bytes + 255) / 256 * 256;
     const size_t ws_bytes = use_prefill ? counter_at + pa::kPrefillCounterBytes : plan.ws_bytes;

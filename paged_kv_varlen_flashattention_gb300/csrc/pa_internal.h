@@ -93,10 +93,13 @@ int prefill_rows_threshold();  // sequences with sq*G > this go to the prefill k
 // zeroes on a.stream before the kernel.
 constexpr size_t kPrefillCounterBytes = 256;
 int launch_prefill(const Args& a, int* counter, unsigned int* err, char* msg, size_t msg_len);
+// Upper bound of the prefill kernel's work items (its grid is min(SMs, items)).
+int64_t prefill_items_bound(const Args& a);
 
 // `prefill_takes_long_rows`: rows of sequences with sq*G above the threshold belong to the
-// prefill kernel; `beside_prefill`: this pass runs while the prefill kernel holds the SMs.
-SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, bool beside_prefill, int num_sms);
+// prefill kernel; `prefill_sms`: SMs the prefill kernel's grid may hold while this pass
+// runs (0 when the prefill kernel runs before it).
+SplitPlan plan_splitkv(const Args& a, bool prefill_takes_long_rows, int prefill_sms, int num_sms);
 int launch_splitkv(const Args& a, const SplitPlan& plan, void* workspace, unsigned int* err, char* msg,
                    size_t msg_len);
 int launch_splitkv_bf16(const Args& a, const SplitPlan& plan, void* workspace, unsigned int* err, char* msg,

@@ -1551,6 +1551,18 @@ bool prefill_supported(const Args& a) {
     return true;
 }
 
+// Upper bound of the prefill kernel's work items per kv head, from the call's sizes alone:
+// query tiles (head dim above 128) or tile pairs of 128 / G whole queries each, summed over
+// the sequences, is at most ceil(total_q / per item) + batch and at most batch x
+// ceil(max_seqlen_q / per item).
+static int64_t prefill_items_per_head(const Args& a) {
+    const int64_t per = (a.D > 128 ? 1 : 2) * (128 / (a.H / a.Hkv));
+    return std::min<int64_t>(((int64_t)a.total_q + per - 1) / per + a.batch,
+                             (int64_t)a.batch * (((int64_t)a.max_sq + per - 1) / per));
+}
+
+int64_t prefill_items_bound(const Args& a) { return prefill_items_per_head(a) * a.Hkv; }
+
 int launch_prefill(const Args& a, int* counter, unsigned int* err, char* msg, size_t msg_len) {
     if (!counter) {
         snprintf(msg, msg_len, "the prefill kernels need a device item counter");
@@ -1589,13 +1601,10 @@ int launch_prefill(const Args& a, int* counter, unsigned int* err, char* msg, si
     pp.wait_ns = a.wait_ns;
     pp.withhold = a.withhold_loads;
     const bool alibi = a.alibi != nullptr;
-    const int64_t qpt = 128 / pp.G;  // whole queries per 128-row tile
     if (a.D > 128) {  // items of one query tile, 64-key K/V tiles
         pp.box_rows = a.paged ? (a.page % 64 == 0 ? 64 : 32) : 64;
         pp.boxes_per_tile = 64 / pp.box_rows;
-        // tiles: sum_b ceil(sq_b / qpt) <= ceil(total_q / qpt) + batch
-        pp.pairs = (int)std::min<int64_t>(((int64_t)a.total_q + qpt - 1) / qpt + a.batch,
-                                          (int64_t)a.batch * (((int64_t)a.max_sq + qpt - 1) / qpt));
+        pp.pairs = (int)prefill_items_per_head(a);  // query tiles
         if (a.dtype == PA_BF16)
             return alibi ? run_prefill256<__nv_bfloat16, true>(a, pp, msg, msg_len)
                          : run_prefill256<__nv_bfloat16, false>(a, pp, msg, msg_len);
@@ -1604,9 +1613,7 @@ int launch_prefill(const Args& a, int* counter, unsigned int* err, char* msg, si
     // items of two query tiles, 128-key K/V tiles
     pp.box_rows = a.paged ? ((a.page % 128 == 0) ? 128 : (a.page % 64 == 0) ? 64 : 32) : 128;
     pp.boxes_per_tile = 128 / pp.box_rows;
-    // tile pairs (2 qpt queries each): sum_b ceil(sq_b / (2 qpt)) <= ceil(total_q / (2 qpt)) + batch
-    pp.pairs = (int)std::min<int64_t>(((int64_t)a.total_q + 2 * qpt - 1) / (2 * qpt) + a.batch,
-                                      (int64_t)a.batch * (((int64_t)a.max_sq + 2 * qpt - 1) / (2 * qpt)));
+    pp.pairs = (int)prefill_items_per_head(a);  // tile pairs (2 qpt queries each)
     const int dp = a.D <= 64 ? 64 : 128;
     if (a.dtype == PA_BF16) {
         if (alibi)
