@@ -5,7 +5,8 @@ items from a device counter; rings, S/P handshakes and barrier phases run on fro
 item.  These batches hold a few hundred prefill-class sequences, so every CTA takes several
 items of different lengths: causal and chunked sequences, sequences whose first rows attend
 no key (more queries than keys), sequences with no keys at all, decode-class rows beside
-them (the split-KV pass), a window, and group sizes that do and do not divide 128.  Rows are
+them (the split-KV pass, with or without key splits depending on how many SMs the prefill
+grid may take), a window, and group sizes that do and do not divide 128.  Rows are
 sampled (always including each sequence's first and last query) and compared with the
 oracle at the stated tolerances."""
 import numpy as np
@@ -120,3 +121,21 @@ def random_items_layout(seed):
 def test_random_many_items(seed):
     lay, alibi = random_items_layout(seed)
     _gpu.check_layout(lay, alibi=alibi, limit=1200)
+
+
+@pytest.mark.parametrize("case", ["prefill_takes_every_sm", "small_prefill"])
+def test_decode_pass_beside_prefill(case):
+    """The decode-class pass planned beside the prefill kernel.  Eight 1,024-query prompts
+    bound the prefill grid at every SM, so the decode sequences beside them (5,000 keys,
+    under the per-split key cap) run one CTA per (sequence, kv head) with no combine; one
+    64-query prompt leaves the plan's splits (and the combine) to four 8,000-key decode
+    sequences.  Sampled rows, always including every sequence's first and last query."""
+    if case == "prefill_takes_every_sm":
+        sq = [1024] * 8 + [1, 4, 1, 2, 1, 3]
+        sk = [1024 + 200 * i for i in range(8)] + [5000, 4990, 4321, 5000, 17, 3000]
+    else:
+        sq = [64, 1, 1, 4, 1]
+        sk = [64, 8000, 7999, 8000, 6500]
+    lay = workloads.make_layout(f"beside_{case}", "bf16", sq, sk, num_heads=32, num_heads_k=8, head_dim=128,
+                                page_block_size=32, seed=97, spare=0.1)
+    _gpu.check_layout(lay, limit=1536)
